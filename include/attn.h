@@ -1,0 +1,136 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) exact softmax attention library.
+ *
+ * The operation (all entry points): for every (batch b, head h) independently,
+ *
+ *     S = s * Q K^T               (N x N scores; s is the caller's score scale)
+ *     P = row-softmax(S)          (masked scores count as minus infinity)
+ *     O = P V,   LSE_i = ln sum_j exp(S_ij)
+ *
+ * as defined in "The I/O Complexity of Attention" exposition
+ * (blog.aeilot.top, attention-io-complexity), section "Attention as a
+ * mathematical problem" (the page omits the 1/sqrt(d) factor; here it is the
+ * caller's s).  The fused forward evaluates it with the stabilised online update
+ * of the section "Softmax without storing the score matrix" (running max m,
+ * sum l and accumulator u kept on chip, O = u / l); the backward is the
+ * recompute pass studied by "On Fine-Grained I/O Complexity of Attention
+ * Backward Passes" (gist.science 2410.09397); the materialising variant is the
+ * small-cache schedule of the first page's section "Small caches: when storing
+ * an intermediate matrix helps", which writes the exponentiated score matrix.
+ *
+ * Conventions common to every call
+ *   Layout      Q, K, V, O, dO, dQ, dK, dV: [B][H][N][d], dense, d innermost.
+ *               LSE and the backward's D: [B][H][N] fp32.  Element type is the
+ *               call's dtype (fp32 or bf16); LSE is always fp32, natural log of
+ *               the scaled scores.
+ *   Memory      Every pointer is a DEVICE pointer on the current CUDA device,
+ *               owned by the caller; the library allocates no device memory.
+ *               Pointers must be 16-byte aligned and must not alias each other.
+ *   Block mask  Optional (NULL = keep everything).  A device array of nb x nb
+ *               bytes, nb = ceil(N / 128), row-major, shared by all (b, h):
+ *               mask[i/128][j/128] == 0 removes score (i, j).  A row with no
+ *               kept score gets O = 0, LSE = -inf and passes no gradient.
+ *   Stream      `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *               default stream).  Every call only enqueues work; nothing waits.
+ *   Errors      Arguments are checked before anything is launched; a failed
+ *               check returns a status and launches nothing.  A failed launch
+ *               returns ATTN_ERR_CUDA.  Kernels never trap: every device-side
+ *               wait is bounded, and an expired wait sets a device status word
+ *               that attn_device_status() reports as ATTN_ERR_TIMEOUT.
+ *   Shapes      fp32: any N >= 1, 1 <= d <= 256 (SIMT kernels).
+ *               bf16: N a multiple of 128; forward d in {64, 128, 256};
+ *               backward d in {64, 128}; materialising forward d in
+ *               {64, 128, 256}.  Anything else returns ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned pointer */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype / d / N combination) */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+    ATTN_ERR_TIMEOUT = 4,      /* a bounded device-side wait expired (reported by attn_device_status) */
+    ATTN_ERR_WORKSPACE = 5     /* workspace pointer NULL or smaller than the size query returns */
+} attn_status;
+
+typedef enum {
+    ATTN_DTYPE_F32 = 0,
+    ATTN_DTYPE_BF16 = 1
+} attn_dtype;
+
+/*
+ * attn_fwd — fused streaming forward.
+ * In:  Q, K, V [B,H,N,d] (dtype), block_mask (nullable, see above), scale s.
+ * Out: O [B,H,N,d] (dtype) = softmax(s Q K^T) V; LSE [B,H,N] fp32.
+ * The bf16 path stages Q/K/V tiles with TMA, runs both products on tcgen05
+ * into tensor memory (fp32 accumulation) and never writes the score matrix.
+ */
+ATTN_API attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                     int B, int H, int N, int d, float scale, attn_dtype dtype,
+                     const uint8_t *block_mask, void *stream);
+
+/* Bytes of scratch attn_bwd needs for this shape (0 is a valid answer). */
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype);
+
+/*
+ * attn_bwd — recompute backward of attn_fwd (chain rule of the definition above):
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_t dO_it O_it,  dS = P o (dP - D),
+ *   dQ = s dS K,  dK = s dS^T Q.
+ * In:  Q, K, V, O, dO [B,H,N,d] (dtype), LSE [B,H,N] fp32 from attn_fwd on the
+ *      same inputs, the same block_mask and scale.
+ * Out: dQ, dK, dV [B,H,N,d] (dtype).
+ * workspace: device scratch of at least attn_bwd_workspace_size() bytes
+ *      (16-byte aligned, contents on entry ignored); it holds D and, for bf16,
+ *      the fp32 dQ accumulator.
+ */
+ATTN_API attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O,
+                     const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                     int B, int H, int N, int d, float scale, attn_dtype dtype,
+                     const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* Bytes of scratch attn_fwd_materialized needs (the N x N exp-score matrix and row terms). */
+ATTN_API size_t attn_fwd_materialized_workspace_size(int B, int H, int N, int d, attn_dtype dtype);
+
+/*
+ * attn_fwd_materialized — the small-cache comparison schedule: the exponentiated
+ * scores E = exp(s Q K^T - c) are written to HBM (bf16, N x N per head), then
+ * O = E V / l and LSE = c + ln l, with l the row sums of E and c_i a per-row
+ * upper bound of the scores (s |q_i| max_j |k_j|, so E never overflows).
+ * Same inputs and outputs as attn_fwd; bf16 only.  workspace as attn_bwd.
+ */
+ATTN_API attn_status attn_fwd_materialized(const void *Q, const void *K, const void *V, void *O,
+                                  float *LSE, int B, int H, int N, int d, float scale,
+                                  attn_dtype dtype, const uint8_t *block_mask,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * attn_device_status — synchronise `stream`, then read and clear the device
+ * status word shared by all kernels of this library on the current device.
+ * Returns ATTN_ERR_TIMEOUT if a bounded wait expired since the last call,
+ * ATTN_ERR_CUDA if the synchronisation failed, ATTN_OK otherwise.
+ */
+ATTN_API attn_status attn_device_status(void *stream);
+
+/* Static description of a status code (never NULL). */
+ATTN_API const char *attn_status_string(attn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

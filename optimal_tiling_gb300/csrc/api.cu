@@ -1,0 +1,235 @@
+// C-ABI host layer (include/attn.h): argument checks, dispatch by dtype and d,
+// TMA descriptor construction, workspace carving and launches on the caller's
+// stream.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/attn.h"
+#include "internal.h"
+
+namespace {
+
+// Device status word shared by every kernel of the library (per device: each
+// device that loads the library has its own copy of this variable).
+__device__ int g_dev_status;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices];
+std::mutex g_mu;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Address of the status word on the current device (looked up once per device).
+int *device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+EncodeTiledFn encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+// 2D bf16 tensor map over a dense [rows][cols] array: boxes of box_rows x 64
+// elements (128 bytes), 128-byte swizzle.
+bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status check_common(int B, int H, int N, int d, attn_dtype dt) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (dt != ATTN_DTYPE_F32 && dt != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+    // every index fits in 32-bit rows for the tensor maps and in size_t for offsets
+    if ((uint64_t)B * H * N > (1ull << 31)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+bool bf16_fwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128 || d == 256); }
+bool bf16_bwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
+
+attn_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return ATTN_OK;
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    return ATTN_ERR_CUDA;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char *attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+        case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                     int d, float scale, attn_dtype dtype, const uint8_t *block_mask, void *stream) {
+    attn_status s = check_common(B, H, N, d, dtype);
+    if (s != ATTN_OK) return s;
+    if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_DTYPE_BF16 && !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    attn::Problem p{B, H, N, d, scale, block_mask, status};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == ATTN_DTYPE_F32) {
+        return launch_status(attn::launch_fwd_f32(p, static_cast<const float *>(Q), static_cast<const float *>(K),
+                                                  static_cast<const float *>(V), static_cast<float *>(O), LSE, st));
+    }
+    const uint64_t rows = (uint64_t)B * H * N;
+    attn::FwdMaps maps;
+    if (!make_map_bf16(&maps.q, Q, d, rows, 128) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
+        !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.o, O, d, rows, 128))
+        return ATTN_ERR_CUDA;
+    return launch_status(attn::launch_fwd_bf16(p, maps, O, LSE, st));
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
+    if (check_common(B, H, N, d, dtype) != ATTN_OK) return 0;
+    const size_t rows = (size_t)B * H * N;
+    size_t bytes = align_up(rows * sizeof(float), 256);              // D
+    if (dtype == ATTN_DTYPE_BF16) bytes += align_up(rows * d * sizeof(float), 256);  // dQ accumulator
+    return bytes;
+}
+
+attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale,
+                     attn_dtype dtype, const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    attn_status s = check_common(B, H, N, d, dtype);
+    if (s != ATTN_OK) return s;
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_DTYPE_BF16 && !bf16_bwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_bwd_workspace_size(B, H, N, d, dtype);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    attn::Problem p{B, H, N, d, scale, block_mask, status};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t rows = (size_t)B * H * N;
+    float *D = static_cast<float *>(workspace);
+    if (dtype == ATTN_DTYPE_F32) {
+        return launch_status(attn::launch_bwd_f32(
+            p, static_cast<const float *>(Q), static_cast<const float *>(K), static_cast<const float *>(V),
+            static_cast<const float *>(O), static_cast<const float *>(dO), LSE, static_cast<float *>(dQ),
+            static_cast<float *>(dK), static_cast<float *>(dV), D, st));
+    }
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(rows * sizeof(float), 256));
+    attn::BwdMaps maps;
+    if (!make_map_bf16(&maps.q, Q, d, rows, 64) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
+        !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.dO, dO, d, rows, 64))
+        return ATTN_ERR_CUDA;
+    return launch_status(attn::launch_bwd_bf16(p, maps, O, dO, LSE, dQ, dK, dV, D, dQacc, st));
+}
+
+size_t attn_fwd_materialized_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
+    if (check_common(B, H, N, d, dtype) != ATTN_OK || dtype != ATTN_DTYPE_BF16) return 0;
+    const size_t heads = (size_t)B * H, rows = heads * N;
+    size_t bytes = align_up(heads * (size_t)N * N * 2, 256);   // E, bf16
+    bytes += align_up(rows * sizeof(float), 256);               // c (row bound)
+    bytes += align_up(rows * sizeof(float), 256);               // l (row sums)
+    bytes += align_up(heads * sizeof(float), 256);              // max_j |k_j| per head
+    return bytes;
+}
+
+attn_status attn_fwd_materialized(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H,
+                                  int N, int d, float scale, attn_dtype dtype, const uint8_t *block_mask,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    attn_status s = check_common(B, H, N, d, dtype);
+    if (s != ATTN_OK) return s;
+    if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_BF16 || !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_fwd_materialized_workspace_size(B, H, N, d, dtype);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    attn::Problem p{B, H, N, d, scale, block_mask, status};
+    const size_t heads = (size_t)B * H, rows = heads * N;
+    char *w = static_cast<char *>(workspace);
+    void *E = w;
+    w += align_up(heads * (size_t)N * N * 2, 256);
+    float *rowc = reinterpret_cast<float *>(w);
+    w += align_up(rows * sizeof(float), 256);
+    float *rowl = reinterpret_cast<float *>(w);
+    w += align_up(rows * sizeof(float), 256);
+    float *kmax = reinterpret_cast<float *>(w);
+    attn::MatMaps maps;
+    if (!make_map_bf16(&maps.q, Q, d, rows, 128) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
+        !make_map_bf16(&maps.e, E, N, heads * N, 128) || !make_map_bf16(&maps.v, V, d, rows, 128))
+        return ATTN_ERR_CUDA;
+    return launch_status(attn::launch_fwd_materialized_bf16(p, maps, Q, K, E, rowc, rowl, kmax, O, LSE,
+                                                            static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+        return ATTN_ERR_TIMEOUT;
+    }
+    return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,327 @@
+// Fused streaming attention forward for sm_103a (bf16 in, fp32 accumulation).
+//
+// Method: "The I/O Complexity of Attention" exposition (blog.aeilot.top,
+// attention-io-complexity), sections "Softmax without storing the score matrix"
+// (the stabilised online update: running max m, sum l, accumulator u, o = u/l)
+// and "Large caches: where FlashAttention's I/O comes from" (a query block and
+// its output state stay on chip while all of K, V is scanned).  The page's
+// schedule is for a generic two-level machine; this kernel is shaped for GB300:
+//
+//   * one CTA per 128-row query tile of one head; K/V are scanned in 128-row
+//     blocks through a TMA ring in shared memory (128-byte swizzle);
+//   * both products run on tcgen05 with fp32 accumulators in tensor memory:
+//     S = Q K^T into one of two 128-column S buffers, O += P V into a d-column
+//     O buffer; P (bf16) is written back over its own S buffer and fed to the
+//     second MMA straight from tensor memory;
+//   * warp roles: warps 0-3 own one query row per thread (TMEM lane = row) and
+//     run the softmax, the O rescale and the epilogue; warp 4 issues TMA; warp 5
+//     allocates tensor memory and issues the MMAs from one elected lane;
+//   * S for block j+1 is computed while the softmax of block j runs;
+//   * the running max is kept in the log2 domain (scores scaled by s*log2 e) and
+//     O is rescaled only when a row's max grows by more than 8 (a factor 256):
+//     the final division uses the same reference max, so the result is the same
+//     function and only rounding differs;
+//   * blocks removed by the 128x128 block mask are never loaded or multiplied.
+// Every mbarrier wait is bounded; an expired wait sets the device status word
+// and the CTA unwinds without touching the GPU's state.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;             // query rows per CTA
+constexpr int BN = 128;             // keys per streamed block
+constexpr int kThreads = 192;       // 4 softmax warps + TMA warp + MMA warp
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol0 = 0, kSCol1 = 128, kOCol = 256;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kChunks = D / 64;                     // 64-element (128 B) swizzle atoms per row
+    static constexpr int kStages = D == 64 ? 4 : (D == 128 ? 2 : 1);
+    static constexpr int kTileBytes = BM * D * 2;              // Q tile == K tile == V tile bytes
+    static constexpr int kChunkBytes = BM * 128;               // one 64-column slab of a tile
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kTileBytes;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;    // + slack to align the base to 1024
+    static_assert(kChunkBytes == 16384, "slab layout");
+    static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
+};
+
+struct Bars {
+    uint32_t base;
+    int stages;
+    __device__ uint32_t q() const { return base; }
+    __device__ uint32_t kfull(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t kempty(int s) const { return base + 8u * (1 + stages + s); }
+    __device__ uint32_t vfull(int s) const { return base + 8u * (1 + 2 * stages + s); }
+    __device__ uint32_t vempty(int s) const { return base + 8u * (1 + 3 * stages + s); }
+    __device__ uint32_t sfull(int b) const { return base + 8u * (1 + 4 * stages + b); }
+    __device__ uint32_t pfull(int b) const { return base + 8u * (3 + 4 * stages + b); }
+    __device__ uint32_t odone() const { return base + 8u * (5 + 4 * stages); }
+    __device__ uint32_t drain() const { return base + 8u * (6 + 4 * stages); }
+};
+
+__device__ __forceinline__ bool kept(const uint8_t *mrow, int j) { return mrow == nullptr || mrow[j] != 0; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const Problem p, __nv_bfloat16 *__restrict__ O,
+                float *__restrict__ LSE) {
+    using C = FwdCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Bars bars{smem_addr(sm + C::kBarOff), S};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, head = blockIdx.y;
+    const int nb = p.N / BN;
+    const uint8_t *mrow = p.mask ? p.mask + (size_t)tile * nb : nullptr;
+    int n = 0;  // kept key blocks of this query tile
+    for (int j = 0; j < nb; ++j) n += kept(mrow, j) ? 1 : 0;
+    const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bars.q(), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bars.kfull(s), 1);
+            mbar_init(bars.kempty(s), 1);
+            mbar_init(bars.vfull(s), 1);
+            mbar_init(bars.vempty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.sfull(b), 1);
+            mbar_init(bars.pfull(b), 4 * 32);
+        }
+        mbar_init(bars.odone(), 1);
+        mbar_init(bars.drain(), 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
+            int it = 0;
+            for (int j = 0; j < nb; ++j) {
+                if (!kept(mrow, j)) continue;
+                const int s = it % S;
+                const uint32_t ph = (uint32_t)(it / S) & 1u;
+                const int krow = head * p.N + j * BN;
+                if (it >= S && !mbar_wait(bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(bars.kfull(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sK + s * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(s));
+                if (it >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
+                ++it;
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
+            // S_it = Q K_it^T into S buffer (it & 1)
+            auto issue_s = [&](int it) -> bool {
+                const int s = it % S;
+                if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
+                tc_fence_after();
+                const uint32_t dcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
+                const uint32_t kb = sK + s * C::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                    mma_ss(dcol, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idS,
+                           ks > 0);
+                }
+                mma_commit(bars.kempty(s));
+                mma_commit(bars.sfull(it & 1));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int it = 0; it < n && ok; ++it) {
+                if (it + 1 < n && !(ok = issue_s(it + 1))) break;
+                const int s = it % S;
+                if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
+                const uint32_t vb = sV + s * C::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO,
+                           (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bars.vempty(s));
+                mma_commit(bars.odone());
+            }
+            if (!ok) {
+                // let every MMA already issued finish before tensor memory is released
+                mma_commit(bars.drain());
+                mbar_wait(bars.drain(), 0, abort_flag, p.dev_status);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps 0-3
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl2 = p.scale * kLog2e;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int it = 0; it < n; ++it) {
+            const int b = it & 1;
+            ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t scol = lane_base + (b ? kSCol1 : kSCol0);
+            uint32_t r[4][32];
+            tmem_ld32(scol + 0, r[0]);
+            tmem_ld32(scol + 32, r[1]);
+            tmem_ld32(scol + 64, r[2]);
+            tmem_ld32(scol + 96, r[3]);
+            tmem_wait_ld();
+            float mx = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(r[q][t]));
+            const float m_new = fmaxf(m_used, mx * sl2);
+            float alpha = 1.f;
+            if (m_new > m_used + kRescaleThreshold) {
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const float p0 = ex2(fmaf(__uint_as_float(r[q][2 * t]), sl2, -m_used));
+                    const float p1 = ex2(fmaf(__uint_as_float(r[q][2 * t + 1]), sl2, -m_used));
+                    rs += p0 + p1;
+                    pk[t] = pack_bf16(p0, p1);
+                }
+                tmem_st16(scol + q * 16, pk);
+            }
+            l = l * alpha + rs;
+            tmem_wait_st();
+            if (it > 0) {
+                ok = mbar_wait(bars.odone(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + kOCol + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                        tmem_st32(lane_base + kOCol + c0, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bars.pfull(b));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && n > 0) {
+            ok = mbar_wait(bars.odone(), (uint32_t)(n - 1) & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        const size_t grow = (size_t)row0 + tid;
+        uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
+        if (ok && n > 0) {
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + kOCol + c0, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+            LSE[grow] = (m_used + __log2f(l)) * kLn2;
+        } else if (n == 0) {
+            // every key block removed: O = 0, LSE = -inf
+            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
+            LSE[grow] = -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
+    auto kern = fwd_bf16_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.N / BM, p.B * p.H);
+    kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, p, static_cast<__nv_bfloat16 *>(O), LSE);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE, cudaStream_t st) {
+    if (p.B * p.H > 65535) return cudaErrorNotSupported;
+    switch (p.d) {
+        case 64: return launch_d<64>(p, maps, O, LSE, st);
+        case 128: return launch_d<128>(p, maps, O, LSE, st);
+        case 256: return launch_d<256>(p, maps, O, LSE, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace attn

@@ -1,0 +1,55 @@
+// Internal launch interface between the C-ABI host layer (api.cu) and the
+// kernel translation units.  Launchers only enqueue work on the given stream
+// and return the cudaError_t of the launch; arguments are validated by api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Device status word values (written by kernels, read by attn_device_status).
+enum : int {
+    kDevOk = 0,
+    kDevTimeout = 1,
+};
+
+// Problem description shared by every launcher.
+struct Problem {
+    int B, H, N, d;
+    float scale;
+    const uint8_t *mask;  // device, nb x nb, or nullptr
+    int *dev_status;      // device status word
+};
+
+// ---- fp32 SIMT path (any N, d <= 256) -------------------------------------
+cudaError_t launch_fwd_f32(const Problem &p, const float *Q, const float *K, const float *V,
+                           float *O, float *LSE, cudaStream_t st);
+cudaError_t launch_bwd_f32(const Problem &p, const float *Q, const float *K, const float *V,
+                           const float *O, const float *dO, const float *LSE, float *dQ,
+                           float *dK, float *dV, float *D, cudaStream_t st);
+
+// ---- bf16 tcgen05 path ------------------------------------------------------
+// Tensor maps are built by the host layer (see tma_desc in api.cu).
+struct FwdMaps {
+    CUtensorMap q, k, v, o;
+};
+cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE,
+                            cudaStream_t st);
+
+struct BwdMaps {
+    CUtensorMap q, k, v, dO;
+};
+cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O,
+                            const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                            float *D, float *dQacc, cudaStream_t st);
+
+struct MatMaps {
+    CUtensorMap q, k, e, v;
+};
+cudaError_t launch_fwd_materialized_bf16(const Problem &p, const MatMaps &maps, const void *Q,
+                                         const void *K, void *E, float *rowc, float *rowl,
+                                         float *kmax, void *O, float *LSE, cudaStream_t st);
+
+}  // namespace attn

@@ -1,0 +1,91 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every entry
+point include/attn.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from optimal_tiling_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_fwd_materialized", "attn_bwd_workspace_size",
+              "attn_fwd_materialized_workspace_size", "attn_device_status", "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(build.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(raw, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert len(attn.status_string(code)) > 0
+    assert attn.status_string(99) == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: every call below fails validation
+MIS = ctypes.c_void_p(0x10008)        # 8-byte aligned only
+
+
+def _fwd(lib, B=1, H=1, N=256, d=64, dt=attn.ATTN_DTYPE_BF16, q=FAKE, scale=1.0):
+    return lib.attn_fwd(q, FAKE, FAKE, FAKE, FAKE, B, H, N, d, scale, dt, None, None)
+
+
+def test_forward_argument_checks(lib):
+    assert _fwd(lib, B=0) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, N=-1) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, q=MIS) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, dt=7) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, N=200) == attn.ATTN_ERR_UNSUPPORTED          # bf16 needs N % 128 == 0
+    assert _fwd(lib, d=96) == attn.ATTN_ERR_UNSUPPORTED           # bf16 d in {64,128,256}
+    assert _fwd(lib, d=300, dt=attn.ATTN_DTYPE_F32) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_backward_argument_checks(lib):
+    def bwd(d=128, N=256, ws=FAKE, wsz=1 << 30, dt=attn.ATTN_DTYPE_BF16):
+        return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, N, d, 0.1, dt,
+                            None, ws, wsz, None)
+    assert bwd(d=256) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(N=100) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(ws=None) == attn.ATTN_ERR_WORKSPACE
+    need = lib.attn_bwd_workspace_size(1, 2, 256, 128, attn.ATTN_DTYPE_BF16)
+    assert need >= 2 * 256 * 4 + 2 * 256 * 128 * 4
+    assert bwd(wsz=need - 1) == attn.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd_workspace_size(1, 2, 256, 64, attn.ATTN_DTYPE_F32) >= 2 * 256 * 4
+    assert lib.attn_bwd_workspace_size(0, 2, 256, 64, attn.ATTN_DTYPE_F32) == 0
+
+
+def test_materialized_argument_checks(lib):
+    need = lib.attn_fwd_materialized_workspace_size(2, 3, 256, 64, attn.ATTN_DTYPE_BF16)
+    assert need >= 6 * 256 * 256 * 2
+    assert lib.attn_fwd_materialized_workspace_size(2, 3, 256, 64, attn.ATTN_DTYPE_F32) == 0
+    r = lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 256, 64, 0.1, attn.ATTN_DTYPE_BF16,
+                                  None, FAKE, need - 16, None)
+    assert r == attn.ATTN_ERR_WORKSPACE
+    r = lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 256, 64, 0.1, attn.ATTN_DTYPE_F32,
+                                  None, FAKE, need, None)
+    assert r == attn.ATTN_ERR_UNSUPPORTED
