@@ -1,7 +1,466 @@
+// Recompute backward of the fused attention for sm_103a (bf16 in, fp32
+// accumulation): the pass whose I/O "On Fine-Grained I/O Complexity of
+// Attention Backward Passes" (gist.science 2410.09397) bounds by
+// Theta((n^2 d^2 + n d^3) / M) in the large-cache regime M >= d^2, which is
+// where a GB300 SM sits for every supported d.
+//
+// The page prints no gradient formulas; this is the chain rule of
+// O = softmax(s Q K^T) V with upstream gradient dO:
+//   P = exp(s Q K^T - LSE),  dV = P^T dO,  dP = dO V^T,  D_i = sum_t dO_it O_it,
+//   dS = P o (dP - D),  dQ = s dS K,  dK = s dS^T Q.
+//
+// Three kernels on the caller's stream:
+//   1. bwd_pre:     D = rowsum(dO o O) in fp32, and the fp32 dQ accumulator zeroed;
+//   2. bwd_main:    one CTA per 128-row K/V tile of one head, looping over the
+//                   64-row query blocks that the block mask keeps.  Five tcgen05
+//                   products per block, all accumulating in tensor memory:
+//                     S^T  = K Q_i^T         (128 x 64, into S buffer)
+//                     dP^T = V dO_i^T        (128 x 64, into dP buffer)
+//                     dV  += P^T dO_i        (A = P^T from tensor memory)
+//                     dK  += dS^T Q_i        (A = dS^T from shared memory)
+//                     dQ_i^T = K^T dS_i^T    (M = d: into the dP buffer, which the
+//                                             softmax warps have already read)
+//                   dQ_i^T is drained by its own warpgroup into shared memory as
+//                   [q][d] fp32 and added into the accumulator with one bulk
+//                   reduction (cp.reduce.async.bulk .add.f32).  S/dP are double
+//                   buffered so that the next block's two products overlap the
+//                   elementwise work of this one.  dK and dV leave tensor memory
+//                   once, at the end.
+//   3. bwd_dq_convert: dQ = bf16(s * accumulator).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
 #include "internal.h"
+#include "sm103_ptx.cuh"
+
 namespace attn {
-cudaError_t launch_bwd_bf16(const Problem &, const BwdMaps &, const void *, const void *, const float *, void *,
-                            void *, void *, float *, float *, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+using namespace ptx;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int BKV = 128;   // key/value rows per CTA
+constexpr int BQ = 64;     // query rows per inner block
+constexpr int kThreads = 320;
+constexpr int kDqWarp0 = 4;     // warps 4-7 drain dQ
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kStages = 2;      // Q/dO/LSE/D ring depth
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct BwdCfg {
+    static_assert(D == 128, "tcgen05 backward is built for d = 128");
+    static constexpr int kKVTile = BKV * D * 2;          // 32 KB
+    static constexpr int kKVSlab = BKV * 128;            // 16 KB: 64 columns of the K/V tile
+    static constexpr int kQTile = BQ * D * 2;            // 16 KB
+    static constexpr int kQSlab = BQ * 128;              // 8 KB
+    static constexpr int kDsTile = BKV * BQ * 2;         // 16 KB: dS^T, 128 rows x 128 B
+    static constexpr int kDqTile = BQ * D * 4;           // 32 KB fp32
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + kKVTile;
+    static constexpr int kQOff = kVOff + kKVTile;
+    static constexpr int kdOOff = kQOff + kStages * kQTile;
+    static constexpr int kDsOff = kdOOff + kStages * kQTile;
+    static constexpr int kDqOff = kDsOff + 2 * kDsTile;
+    static constexpr int kLdOff = kDqOff + kDqTile;      // per stage: LSE[64], D[64]
+    static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
+    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull[2], dqfree[2], kvdone, drain
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 5 + 2;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+    // tensor memory columns
+    static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 2 * BQ;
+    static_assert(kColDP + 2 * BQ <= kTmemCols, "tensor memory budget");
+};
+
+struct BwdBars {
+    uint32_t base;
+    __device__ uint32_t kv() const { return base; }
+    __device__ uint32_t qfull(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t qempty(int s) const { return base + 8u * (1 + kStages + s); }
+    __device__ uint32_t sfull(int b) const { return base + 8u * (1 + 2 * kStages + b); }
+    __device__ uint32_t pfull(int b) const { return base + 8u * (3 + 2 * kStages + b); }
+    __device__ uint32_t dsfree(int b) const { return base + 8u * (5 + 2 * kStages + b); }
+    __device__ uint32_t dqfull(int b) const { return base + 8u * (7 + 2 * kStages + b); }
+    __device__ uint32_t dqfree(int b) const { return base + 8u * (9 + 2 * kStages + b); }
+    __device__ uint32_t kvdone() const { return base + 8u * (11 + 2 * kStages); }
+    __device__ uint32_t drain() const { return base + 8u * (12 + 2 * kStages); }
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+
+// ------------------------------------------------------------------------- 1
+// D_i = sum_t dO_it O_it; the dQ accumulator row is zeroed.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
+                                                      const __nv_bfloat16 *__restrict__ dO,
+                                                      float *__restrict__ Dv, float *__restrict__ dQacc,
+                                                      size_t rows) {
+    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    constexpr int E = D / 32;  // elements per lane (2 or 4)
+    const __nv_bfloat16 *o = O + row * D + lane * E;
+    const __nv_bfloat16 *g = dO + row * D + lane * E;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + e));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + e));
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+    }
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) Dv[row] = acc;
+    float4 *z = reinterpret_cast<float4 *>(dQacc + row * D);
+    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------------- 2
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const Problem p, const float *__restrict__ LSE, const float *__restrict__ Dv,
+                float *__restrict__ dQacc, __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const BwdBars bars{smem_addr(sm + C::kBarOff)};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kvt = blockIdx.x, head = blockIdx.y;
+    const int nb = p.N / 128;                  // 128-row mask blocks
+    const int kv0 = head * p.N + kvt * BKV;    // first K/V row of this CTA in the [B*H*N, D] view
+    // query blocks (64 rows) kept for this key tile: both halves of each kept 128-row mask block
+    int n = 0;
+    for (int bi = 0; bi < nb; ++bi) n += (p.mask == nullptr || p.mask[(size_t)bi * nb + kvt]) ? 2 : 0;
+    auto qblock = [&](int it) -> int {  // it-th kept 64-row query block
+        if (p.mask == nullptr) return it;
+        int c = 0;
+        for (int bi = 0; bi < nb; ++bi)
+            if (p.mask[(size_t)bi * nb + kvt]) {
+                if (c + 2 > it) return 2 * bi + (it - c);
+                c += 2;
+            }
+        return 0;
+    };
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bars.kv(), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bars.qfull(s), 1);
+            mbar_init(bars.qempty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.sfull(b), 1);
+            mbar_init(bars.pfull(b), 128);
+            mbar_init(bars.dsfree(b), 1);
+            mbar_init(bars.dqfull(b), 1);
+            mbar_init(bars.dqfree(b), 128);
+        }
+        mbar_init(bars.kvdone(), 1);
+        mbar_init(bars.drain(), 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sdO = smem_addr(sm + C::kdOOff);
+    const uint32_t sDs = smem_addr(sm + C::kDsOff), sDq = smem_addr(sm + C::kDqOff);
+    const uint32_t sLd = smem_addr(sm + C::kLdOff);
+    const float *ld_f = reinterpret_cast<const float *>(sm + C::kLdOff);
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            tma_prefetch_desc(&tmdO);
+            mbar_arrive_expect_tx(bars.kv(), 2 * C::kKVTile);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_2d(sK + c * C::kKVSlab, &tmK, c * 64, kv0, bars.kv());
+                tma_load_2d(sV + c * C::kKVSlab, &tmV, c * 64, kv0, bars.kv());
+            }
+            for (int it = 0; it < n; ++it) {
+                const int s = it % kStages;
+                if (it >= kStages &&
+                    !mbar_wait(bars.qempty(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, abort_flag, p.dev_status))
+                    break;
+                const int q0 = head * p.N + qblock(it) * BQ;
+                mbar_arrive_expect_tx(bars.qfull(s), 2 * C::kQTile + 2 * BQ * 4);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_2d(sQ + s * C::kQTile + c * C::kQSlab, &tmQ, c * 64, q0, bars.qfull(s));
+                    tma_load_2d(sdO + s * C::kQTile + c * C::kQSlab, &tmdO, c * 64, q0, bars.qfull(s));
+                }
+                bulk_load(sLd + s * 2 * BQ * 4, LSE + q0, BQ * 4, bars.qfull(s));
+                bulk_load(sLd + s * 2 * BQ * 4 + BQ * 4, Dv + q0, BQ * 4, bars.qfull(s));
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idSP = idesc_bf16_f32(BKV, BQ, false, false);  // S^T, dP^T
+            constexpr uint32_t idKV = idesc_bf16_f32(BKV, D, false, true);    // dV, dK
+            constexpr uint32_t idQ = idesc_bf16_f32(D, BQ, true, true);       // dQ^T
+            bool ok = mbar_wait(bars.kv(), 0, abort_flag, p.dev_status);
+            // S^T_it and dP^T_it into buffer it & 1
+            auto issue_sdp = [&](int it) -> bool {
+                const int s = it % kStages, b = it & 1;
+                if (!mbar_wait(bars.qfull(s), (uint32_t)(it / kStages) & 1u, abort_flag, p.dev_status)) return false;
+                // the dP buffer held dQ^T of block it-2: wait until it was drained
+                if (it >= 2 && !mbar_wait(bars.dqfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status))
+                    return false;
+                tc_fence_after();
+                const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
+                    const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
+                    mma_ss(tmem + C::kColS + b * BQ, smem_desc_sw128(sK + ko, 16, 1024),
+                           smem_desc_sw128(qb + qo, 16, 1024), idSP, ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
+                    const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
+                    mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sV + ko, 16, 1024),
+                           smem_desc_sw128(gb + qo, 16, 1024), idSP, ks > 0);
+                }
+                mma_commit(bars.sfull(b));
+                return true;
+            };
+            if (ok) ok = issue_sdp(0);
+            for (int it = 0; it < n && ok; ++it) {
+                const int s = it % kStages, b = it & 1;
+                if (it + 1 < n && !(ok = issue_sdp(it + 1))) break;
+                if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile, dsb = sDs + b * C::kDsTile;
+                // dV += P^T dO_i : A = P^T (bf16 pairs in the S buffer), B = dO_i (d contiguous)
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + ks * 8,
+                           smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV, (it > 0 || ks > 0) ? 1u : 0u);
+                // dK += dS^T Q_i : A = dS^T (K-major, 64 q per row), B = Q_i (d contiguous)
+#pragma unroll
+                for (int ks = 0; ks < BQ / 16; ++ks)
+                    mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
+                           smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV, (it > 0 || ks > 0) ? 1u : 0u);
+                // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous); into the dP buffer
+#pragma unroll
+                for (int ks = 0; ks < BKV / 16; ++ks)
+                    mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sK + ks * 2048, C::kKVSlab, 1024),
+                           smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
+                mma_commit(bars.qempty(s));
+                mma_commit(bars.dsfree(b));
+                mma_commit(bars.dqfull(b));
+            }
+            if (ok) {
+                mma_commit(bars.kvdone());
+            } else {
+                mma_commit(bars.drain());
+                mbar_wait(bars.drain(), 0, abort_flag, p.dev_status);
+            }
+        }
+    } else if (warp < kDqWarp0) {
+        // ------------------------------------------------------------ P / dS warps 0-3
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl2 = p.scale * kLog2e;
+        const uint32_t my_ds_row = (uint32_t)tid * 128u;  // byte offset of dS^T row tid in a dS tile
+        uint8_t *ds_gen = sm + C::kDsOff;
+        bool ok = true;
+        for (int it = 0; it < n; ++it) {
+            const int s = it % kStages, b = it & 1;
+            ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
+            if (ok && it >= 2)
+                ok = mbar_wait(bars.dsfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const float *lse = ld_f + s * 2 * BQ;  // LSE of the 64 queries, then D
+            const float *dvv = lse + BQ;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // two halves of 32 queries
+                uint32_t sr[32], pr[32];
+                tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
+                tmem_ld32(lane_base + C::kColDP + b * BQ + h * 32, pr);
+                tmem_wait_ld();
+                reg_fence(sr);
+                reg_fence(pr);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int q = h * 32 + 2 * t;
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -lse[q] * kLog2e));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -lse[q + 1] * kLog2e));
+                    const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
+                    const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
+                    pk[t] = pack_bf16(p0, p1);
+                    dk[t] = pack_bf16(d0, d1);
+                }
+                // P^T over the first half of the S buffer's columns (bf16 pairs)
+                tmem_st16(lane_base + C::kColS + b * BQ + h * 16, pk);
+                // dS^T row into shared memory, 128-byte swizzle: 16-byte chunk c at c ^ (row % 8)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = h * 4 + c;
+                    const uint32_t off = my_ds_row + (uint32_t)((chunk ^ (tid & 7)) * 16);
+                    *reinterpret_cast<uint4 *>(ds_gen + b * C::kDsTile + off) =
+                        make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars.pfull(b));
+        }
+        // ------------------------------------------------------------ dK, dV epilogue
+        if (ok && n > 0) {
+            ok = mbar_wait(bars.kvdone(), 0, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        const size_t grow = (size_t)kv0 + tid;
+        uint4 *dkrow = reinterpret_cast<uint4 *>(dK + grow * D);
+        uint4 *dvrow = reinterpret_cast<uint4 *>(dV + grow * D);
+        if (ok && n > 0) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t a[32], v[32];
+                tmem_ld32(lane_base + C::kColDK + c0, a);
+                tmem_ld32(lane_base + C::kColDV + c0, v);
+                tmem_wait_ld();
+                reg_fence(a);
+                reg_fence(v);
+                uint32_t pa[16], pv[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
+                    pv[t] = pack_bf16(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    dkrow[c0 / 8 + q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                    dvrow[c0 / 8 + q] = make_uint4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
+                }
+            }
+        } else if (n == 0) {
+            for (int q = 0; q < D / 8; ++q) {
+                dkrow[q] = make_uint4(0, 0, 0, 0);
+                dvrow[q] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    } else if (warp < kTmaWarp) {
+        // ------------------------------------------------------------ dQ drain warps 4-7
+        const int t = tid - kDqWarp0 * 32;  // 0..127 = d index (tensor memory lane)
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        float *dq_gen = reinterpret_cast<float *>(sm + C::kDqOff);
+        for (int it = 0; it < n; ++it) {
+            const int b = it & 1;
+            bool ok = mbar_wait(bars.dqfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(lane_base + C::kColDP + b * BQ, r0);
+            tmem_ld32(lane_base + C::kColDP + b * BQ + 32, r1);
+            tmem_wait_ld();
+            reg_fence(r0);
+            reg_fence(r1);
+            tc_fence_before();
+            mbar_arrive(bars.dqfree(b));
+            // the previous bulk reduction must have finished reading the staging tile
+            if (t == 0) bulk_wait_read_all();
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                dq_gen[q * D + t] = __uint_as_float(r0[q]);
+                dq_gen[(q + 32) * D + t] = __uint_as_float(r1[q]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (t == 0) {
+                const size_t q0 = (size_t)head * p.N + (size_t)qblock(it) * BQ;
+                bulk_reduce_add_f32(dQacc + q0 * D, sDq, C::kDqTile);
+                bulk_commit();
+            }
+        }
+        if (t == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------- 3
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__restrict__ acc,
+                                                              __nv_bfloat16 *__restrict__ dQ, float scale,
+                                                              size_t n8) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+        uint4 o;
+        o.x = pack_bf16(a.x * scale, a.y * scale);
+        o.y = pack_bf16(a.z * scale, a.w * scale);
+        o.z = pack_bf16(b.x * scale, b.y * scale);
+        o.w = pack_bf16(b.z * scale, b.w * scale);
+        reinterpret_cast<uint4 *>(dQ)[i] = o;
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const void *dO, const float *LSE,
+                     void *dQ, void *dK, void *dV, float *Dv, float *dQacc, cudaStream_t st) {
+    const size_t rows = (size_t)p.B * p.H * p.N;
+    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(O),
+                                                                   static_cast<const __nv_bfloat16 *>(dO), Dv,
+                                                                   dQacc, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    auto kern = bwd_main_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.N / BKV, p.B * p.H);
+    kern<<<grid, kThreads, BwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.dO, p, LSE, Dv, dQacc,
+                                                         static_cast<__nv_bfloat16 *>(dK),
+                                                         static_cast<__nv_bfloat16 *>(dV));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t n8 = rows * D / 8;
+    bwd_dq_convert_kernel<<<(unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16), 256, 0, st>>>(
+        dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O, const void *dO,
+                            const float *LSE, void *dQ, void *dK, void *dV, float *Dv, float *dQacc,
+                            cudaStream_t st) {
+    if (p.B * p.H > 65535) return cudaErrorNotSupported;
+    switch (p.d) {
+        case 128: return launch_d<128>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 }  // namespace attn

@@ -216,6 +216,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tmem_ld32(scol + 64, r[2]);
             tmem_ld32(scol + 96, r[3]);
             tmem_wait_ld();
+            reg_fence(r[0]);
+            reg_fence(r[1]);
+            reg_fence(r[2]);
+            reg_fence(r[3]);
             float mx = -INFINITY;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -253,6 +257,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         uint32_t o[32];
                         tmem_ld32(lane_base + kOCol + c0, o);
                         tmem_wait_ld();
+                        reg_fence(o);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
                         tmem_st32(lane_base + kOCol + c0, o);
@@ -278,6 +283,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 uint32_t o[32];
                 tmem_ld32(lane_base + kOCol + c0, o);
                 tmem_wait_ld();
+                reg_fence(o);
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t)

@@ -1,0 +1,115 @@
+"""bf16 recompute backward (tcgen05) against the oracle, through the C ABI.
+
+Tolerance: relative-L2 <= 2e-2 on dQ, dK and dV (bf16 inputs, fp32
+accumulation; the kernel rounds P and dS to bf16 before its products, the oracle
+does not).  The kernel's backward takes O and LSE from the kernel's forward; the
+oracle recomputes everything from Q, K, V and dO in double."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL_BF16_GRAD_RL2, Guarded, rel_l2
+from optimal_tiling_gb300 import attn, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+def _fwd_bwd(x, scale, mask=None, guarded=True):
+    B, H, N, d = x["q"].shape
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    dm = mask.to(DEV) if mask is not None else None
+    o, lse = attn.attn_fwd(q, k, v, scale, block_mask=dm)
+    if guarded:
+        g = [Guarded((B, H, N, d), torch.bfloat16, DEV) for _ in range(3)]
+        attn.attn_bwd(q, k, v, o, do, lse, scale, block_mask=dm, dq=g[0].t, dk=g[1].t, dv=g[2].t)
+        assert attn.attn_device_status() == attn.ATTN_OK
+        assert all(x.intact() for x in g), "write outside an output tensor"
+        outs = [x.t for x in g]
+    else:
+        outs = attn.attn_bwd(q, k, v, o, do, lse, scale, block_mask=dm)
+        assert attn.attn_device_status() == attn.ATTN_OK
+    return [t.float().cpu().numpy() for t in outs]
+
+
+def _check_full(x, scale, oracle_mod, mask=None):
+    dq, dk, dv = _fwd_bwd(x, scale, mask)
+    gQ, gK, gV, _, _ = oracle_mod.bwd_naive(x["q"], x["k"], x["v"], x["do"], scale,
+                                            None if mask is None else mask.numpy())
+    for name, got, ref in (("dQ", dq, gQ), ("dK", dk, gK), ("dV", dv, gV)):
+        assert rel_l2(got, ref) <= TOL_BF16_GRAD_RL2, name
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("N,BH", [(128, (1, 1)), (256, (1, 3)), (384, (3, 1)), (1024, (1, 2))])
+def test_small_shapes(oracle_mod, N, BH):
+    B, H = BH
+    x = inputs.make_inputs(B, H, N, 128, torch.bfloat16, seed=N + 1)
+    _check_full(x, 1.0 / math.sqrt(128), oracle_mod)
+
+
+def test_block_masks_and_empty_rows(oracle_mod):
+    N = 768
+    x = inputs.make_inputs(1, 2, N, 128, torch.bfloat16, seed=21)
+    s = 1.0 / math.sqrt(128)
+    _check_full(x, s, oracle_mod, inputs.block_diagonal_mask(N))
+    _check_full(x, s, oracle_mod, inputs.random_block_mask(N, seed=6, p=0.3))
+    m = torch.zeros((6, 6), dtype=torch.uint8)
+    m[3, 1] = 1
+    m[5, 1] = 1
+    m[5, 4] = 1
+    dq, dk, dv = _check_full(x, s, oracle_mod, m)
+    # rows of query blocks with nothing kept get no gradient; keys never kept get none
+    assert np.all(dq[:, :, 0:384] == 0) and np.all(dq[:, :, 512:640] == 0)
+    assert np.all(dk[:, :, 0:128] == 0) and np.all(dv[:, :, 256:512] == 0)
+
+
+def test_gradient_invariants():
+    """Rows of P sum to one: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i."""
+    N = 1024
+    x = inputs.make_inputs(1, 1, N, 128, torch.bfloat16, seed=22)
+    dq, dk, dv = _fwd_bwd(x, 1.0 / math.sqrt(128))
+    dO = x["do"].double().numpy()[0, 0]
+    sk = np.abs(dk[0, 0].sum(axis=0))
+    assert np.max(sk) <= 2e-2 * np.sqrt(N) * np.sqrt(np.mean(dk ** 2))
+    assert np.linalg.norm(dv[0, 0].sum(axis=0) - dO.sum(axis=0)) <= 2e-2 * np.linalg.norm(dO.sum(axis=0))
+
+
+def test_deterministic_inputs_repeat():
+    """Two calls on the same inputs agree to the rounding of fp32 additions
+    (the dQ accumulation order between key tiles is not fixed)."""
+    x = inputs.make_inputs(1, 2, 512, 128, torch.bfloat16, seed=23)
+    a = _fwd_bwd(x, 0.09, guarded=False)
+    b = _fwd_bwd(x, 0.09, guarded=False)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])   # dK, dV: fixed order
+    assert rel_l2(a[0], b[0]) <= 1e-3
+
+
+def _sample(n, N, seed):
+    r = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, N - 1], r.integers(0, N, n - 2)])).astype(np.int32)
+
+
+@pytest.mark.parametrize("name,with_kv", [("bwd_d128", True), ("sparse_16k", True), ("dense_16k", False)])
+def test_full_size_workloads_sampled(oracle_mod, name, with_kv):
+    """Full-size workloads in the bench's launch configuration; the oracle computes
+    sampled gradient rows of two heads (dQ rows need one query row each; dK and dV
+    rows need every row's LSE and D, so they are checked where that stays cheap)."""
+    w = inputs.WORKLOADS[name]
+    x, mask = inputs.workload_inputs(w)
+    dq, dk, dv = _fwd_bwd(x, w.scale, mask, guarded=False)
+    B, H, N, d = w.shape
+    m = None if mask is None else mask.numpy()
+    for head in (0, B * H - 1):
+        b, h = divmod(head, H)
+        qr = _sample(24, N, head)
+        kr = _sample(16, N, head + 100) if with_kv else np.zeros(0, np.int32)
+        gQ, gK, gV = oracle_mod.bwd_rows(x["q"][b, h], x["k"][b, h], x["v"][b, h], x["do"][b, h], w.scale,
+                                         qr, kr, m)
+        assert rel_l2(dq[b, h][qr], gQ) <= TOL_BF16_GRAD_RL2
+        if with_kv:
+            assert rel_l2(dk[b, h][kr], gK) <= TOL_BF16_GRAD_RL2
+            assert rel_l2(dv[b, h][kr], gV) <= TOL_BF16_GRAD_RL2
+    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
