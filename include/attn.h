@@ -126,6 +126,21 @@ ATTN_API attn_status attn_fwd_materialized(const void *Q, const void *K, const v
  */
 ATTN_API attn_status attn_device_status(void *stream);
 
+/*
+ * Launch timing, for measurement tools.  While enabled, every kernel launch of
+ * this library is bracketed by a pair of CUDA events recorded on the stream the
+ * kernel is launched on (the events are created and owned by the library).
+ * attn_profile_query synchronises on the recorded events and returns, for the
+ * kernel family `index` (0 <= index < attn_profile_count()), its name, the
+ * number of launches and their summed duration in milliseconds.
+ * attn_profile_reset drops every record.  Host-side only; off by default.
+ */
+ATTN_API void attn_profile_enable(int on);
+ATTN_API int attn_profile_count(void);
+ATTN_API attn_status attn_profile_query(int index, char *name, int name_capacity, int *launches,
+                                        double *total_ms);
+ATTN_API void attn_profile_reset(void);
+
 /* Static description of a status code (never NULL). */
 ATTN_API const char *attn_status_string(attn_status status);
 

@@ -7,6 +7,9 @@
 #include <mutex>
 #include <stdint.h>
 #include <string.h>
+#include <string>
+#include <utility>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "internal.h"
@@ -91,9 +94,89 @@ attn_status launch_status(cudaError_t e) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// ---- launch timing ---------------------------------------------------------
+struct ProfFamily {
+    std::string name;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+};
+bool g_prof_on = false;
+std::vector<ProfFamily> g_prof;
+std::mutex g_prof_mu;
+
 }  // namespace
 
+namespace attn {
+
+ProfScope::ProfScope(const char *kernel, cudaStream_t st) : slot_(-1), idx_(0), st_(st) {
+    if (!g_prof_on) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    int fam = -1;
+    for (size_t i = 0; i < g_prof.size(); ++i)
+        if (g_prof[i].name == kernel) fam = (int)i;
+    if (fam < 0) {
+        g_prof.push_back(ProfFamily{kernel, {}});
+        fam = (int)g_prof.size() - 1;
+    }
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+        cudaEventDestroy(a);
+        return;
+    }
+    cudaEventRecord(a, st);
+    g_prof[fam].ev.emplace_back(a, b);
+    slot_ = fam;
+    idx_ = g_prof[fam].ev.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+    if (slot_ < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if ((size_t)slot_ < g_prof.size() && idx_ < g_prof[slot_].ev.size())
+        cudaEventRecord(g_prof[slot_].ev[idx_].second, st_);
+}
+
+}  // namespace attn
+
 extern "C" {
+
+void attn_profile_enable(int on) { g_prof_on = on != 0; }
+
+int attn_profile_count(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    return (int)g_prof.size();
+}
+
+attn_status attn_profile_query(int index, char *name, int name_capacity, int *launches, double *total_ms) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (index < 0 || index >= (int)g_prof.size()) return ATTN_ERR_INVALID_ARG;
+    const ProfFamily &f = g_prof[index];
+    if (name && name_capacity > 0) {
+        strncpy(name, f.name.c_str(), (size_t)name_capacity - 1);
+        name[name_capacity - 1] = 0;
+    }
+    double tot = 0.0;
+    for (const auto &e : f.ev) {
+        if (cudaEventSynchronize(e.second) != cudaSuccess) return ATTN_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, e.first, e.second) != cudaSuccess) return ATTN_ERR_CUDA;
+        tot += ms;
+    }
+    if (launches) *launches = (int)f.ev.size();
+    if (total_ms) *total_ms = tot;
+    return ATTN_OK;
+}
+
+void attn_profile_reset(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto &f : g_prof)
+        for (auto &e : f.ev) {
+            cudaEventDestroy(e.first);
+            cudaEventDestroy(e.second);
+        }
+    g_prof.clear();
+}
+
 
 const char *attn_status_string(attn_status s) {
     switch (s) {

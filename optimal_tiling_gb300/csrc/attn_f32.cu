@@ -266,7 +266,10 @@ cudaError_t launch_fwd_f32(const Problem &p, const float *Q, const float *K, con
                                          (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.N + kWarps - 1) / kWarps, p.B * p.H);
-    fwd_f32_kernel<<<grid, kWarps * 32, smem, st>>>(p, Q, K, V, O, LSE);
+    {
+        ProfScope prof_("fwd_f32", st);
+        fwd_f32_kernel<<<grid, kWarps * 32, smem, st>>>(p, Q, K, V, O, LSE);
+    }
     return cudaGetLastError();
 }
 
@@ -274,19 +277,28 @@ cudaError_t launch_bwd_f32(const Problem &p, const float *Q, const float *K, con
                            const float *O, const float *dO, const float *LSE, float *dQ,
                            float *dK, float *dV, float *D, cudaStream_t st) {
     dim3 grid((p.N + kWarps - 1) / kWarps, p.B * p.H);
-    bwd_f32_rowdot_kernel<<<grid, kWarps * 32, 0, st>>>(p, O, dO, D);
+    {
+        ProfScope prof_("bwd_f32_rowdot", st);
+        bwd_f32_rowdot_kernel<<<grid, kWarps * 32, 0, st>>>(p, O, dO, D);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem_q = (size_t)(2 * kChunk * (p.d + 1) + 2 * kWarps * p.d) * sizeof(float);
     e = cudaFuncSetAttribute(bwd_f32_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q);
     if (e != cudaSuccess) return e;
-    bwd_f32_dq_kernel<<<grid, kWarps * 32, smem_q, st>>>(p, Q, K, V, dO, LSE, D, dQ);
+    {
+        ProfScope prof_("bwd_f32_dq", st);
+        bwd_f32_dq_kernel<<<grid, kWarps * 32, smem_q, st>>>(p, Q, K, V, dO, LSE, D, dQ);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem_k = (size_t)(2 * kChunk * (p.d + 1) + 2 * kWarps * p.d + 2 * kChunk) * sizeof(float);
     e = cudaFuncSetAttribute(bwd_f32_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_k);
     if (e != cudaSuccess) return e;
-    bwd_f32_dkv_kernel<<<grid, kWarps * 32, smem_k, st>>>(p, Q, K, V, dO, LSE, D, dK, dV);
+    {
+        ProfScope prof_("bwd_f32_dkv", st);
+        bwd_f32_dkv_kernel<<<grid, kWarps * 32, smem_k, st>>>(p, Q, K, V, dO, LSE, D, dK, dV);
+    }
     return cudaGetLastError();
 }
 

@@ -431,23 +431,32 @@ template <int D>
 cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const void *dO, const float *LSE,
                      void *dQ, void *dK, void *dV, float *Dv, float *dQacc, cudaStream_t st) {
     const size_t rows = (size_t)p.B * p.H * p.N;
-    bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(O),
-                                                                   static_cast<const __nv_bfloat16 *>(dO), Dv,
-                                                                   dQacc, rows);
+    {
+        ProfScope prof_("bwd_pre", st);
+        bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(O),
+                                                                       static_cast<const __nv_bfloat16 *>(dO), Dv,
+                                                                       dQacc, rows);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kern = bwd_main_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.N / BKV, p.B * p.H);
-    kern<<<grid, kThreads, BwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.dO, p, LSE, Dv, dQacc,
-                                                         static_cast<__nv_bfloat16 *>(dK),
-                                                         static_cast<__nv_bfloat16 *>(dV));
+    {
+        ProfScope prof_("bwd_main", st);
+        kern<<<grid, kThreads, BwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.dO, p, LSE, Dv, dQacc,
+                                                             static_cast<__nv_bfloat16 *>(dK),
+                                                             static_cast<__nv_bfloat16 *>(dV));
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t n8 = rows * D / 8;
-    bwd_dq_convert_kernel<<<(unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16), 256, 0, st>>>(
-        dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8);
+    {
+        ProfScope prof_("bwd_dq_convert", st);
+        bwd_dq_convert_kernel<<<(unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16), 256, 0, st>>>(
+            dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8);
+    }
     return cudaGetLastError();
 }
 

@@ -314,7 +314,10 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.N / BM, p.B * p.H);
-    kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, p, static_cast<__nv_bfloat16 *>(O), LSE);
+    {
+        ProfScope prof_("fwd_bf16", st);
+        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, p, static_cast<__nv_bfloat16 *>(O), LSE);
+    }
     return cudaGetLastError();
 }
 

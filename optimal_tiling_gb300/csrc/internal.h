@@ -15,6 +15,20 @@ enum : int {
     kDevTimeout = 1,
 };
 
+// Opt-in launch timing (attn_profile_* in the C ABI).  A ProfScope placed around
+// a kernel launch records a CUDA event pair on the launching stream when
+// profiling is enabled, and does nothing otherwise.
+class ProfScope {
+  public:
+    ProfScope(const char *kernel, cudaStream_t st);
+    ~ProfScope();
+
+  private:
+    int slot_;
+    size_t idx_;
+    cudaStream_t st_;
+};
+
 // Problem description shared by every launcher.
 struct Problem {
     int B, H, N, d;

@@ -1,7 +1,369 @@
+// Materialising two-GEMM attention forward for sm_103a: the comparison point.
+//
+// Method: "The I/O Complexity of Attention" exposition (blog.aeilot.top,
+// attention-io-complexity), section "Small caches: when storing an intermediate
+// matrix helps": the exponentiated score matrix (N^2 elements per head) is
+// written to slow memory, then multiplied by V.  The page's schedule targets a
+// cache with M < d^2; every supported d has d^2 below a GB300 SM's shared
+// memory, so this variant shows the cost of the extra N^2 traffic that the fused
+// kernel avoids.  The page leaves the exponent unstabilised; here each row i is
+// shifted by c_i = s |q_i| max_j |k_j|, an upper bound of every score in the
+// row (Cauchy-Schwarz), so E never overflows and the result is the same
+// function:  E = exp(s Q K^T - c),  l = rowsum E,  O = E V / l,  LSE = c + ln l.
+//
+// Kernels (caller's stream): mat_init (zero l and the per-head key-norm max),
+// mat_norms (|q_i| and the per-head max |k_j|), mat_scores (tcgen05 S tile ->
+// E tile, bf16, TMA-stored; row sums of the stored values added into l),
+// mat_output (tcgen05 O = E V over the kept key blocks, O / l and LSE).
+// Key blocks removed by the block mask are neither written nor read.
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "sm103_ptx.cuh"
+
 namespace attn {
-cudaError_t launch_fwd_materialized_bf16(const Problem &, const MatMaps &, const void *, const void *, void *,
-                                         float *, float *, float *, void *, float *, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+using namespace ptx;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int BT = 128;  // tile rows / columns
+
+__global__ void mat_init_kernel(float *__restrict__ rowl, float *__restrict__ kmax, size_t rows, int heads) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += (size_t)gridDim.x * blockDim.x)
+        rowl[i] = 0.f;
+    if (blockIdx.x == 0)
+        for (int h = threadIdx.x; h < heads; h += blockDim.x) kmax[h] = 0.f;
 }
+
+// One warp per row: |q_row| into qnorm, max over the head's |k_row| into kmax.
+template <int D>
+__global__ void __launch_bounds__(256) mat_norms_kernel(const __nv_bfloat16 *__restrict__ Q,
+                                                        const __nv_bfloat16 *__restrict__ K,
+                                                        float *__restrict__ qnorm, float *__restrict__ kmax,
+                                                        size_t rows, int N) {
+    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float aq = 0.f, ak = 0.f;
+    for (int c = lane * 2; c < D; c += 64) {
+        const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(Q + row * D + c));
+        const float2 k = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(K + row * D + c));
+        aq = fmaf(q.x, q.x, fmaf(q.y, q.y, aq));
+        ak = fmaf(k.x, k.x, fmaf(k.y, k.y, ak));
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+        aq += __shfl_xor_sync(0xffffffffu, aq, off);
+        ak += __shfl_xor_sync(0xffffffffu, ak, off);
+    }
+    if (lane == 0) {
+        qnorm[row] = sqrtf(aq);
+        // norms are non-negative, so their bit patterns order like the values
+        atomicMax(reinterpret_cast<int *>(kmax) + row / N, __float_as_int(sqrtf(ak)));
+    }
+}
+
+template <int D>
+struct ScoreCfg {
+    static constexpr int kTile = BT * D * 2;       // Q or K tile
+    static constexpr int kSlab = BT * 128;
+    static constexpr int kQOff = 0, kKOff = kTile, kBarOff = 2 * kTile;
+    // at most four CTAs per SM, so that their 128 tensor-memory columns always fit
+    static constexpr int kSmemBytes = (2 * kTile + 64 + 1024) > 59 * 1024 ? (2 * kTile + 64 + 1024) : 59 * 1024;
+};
+
+// One CTA per (key tile, query tile, head): S = Q K^T on tcgen05, then
+// E = exp(s S - c) as bf16 through shared memory to HBM with a TMA store.
+template <int D>
+__global__ void __launch_bounds__(128) mat_scores_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                         const __grid_constant__ CUtensorMap tmK,
+                                                         const __grid_constant__ CUtensorMap tmE, const Problem p,
+                                                         const float *__restrict__ qnorm,
+                                                         const float *__restrict__ kmax, float *__restrict__ rowl) {
+    using C = ScoreCfg<D>;
+    const int kt = blockIdx.x, qt = blockIdx.y, head = blockIdx.z;
+    const int nb = p.N / BT;
+    if (p.mask && p.mask[(size_t)qt * nb + kt] == 0) return;  // removed block: never written, never read
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t bar_ld = smem_addr(sm + C::kBarOff), bar_mma = bar_ld + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kBarOff + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kBarOff + 24);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff);
+    const int q0 = head * p.N + qt * BT, k0 = head * p.N + kt * BT;
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tmem_slot), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_ld, 2 * C::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(sQ + c * C::kSlab, &tmQ, c * 64, q0, bar_ld);
+            tma_load_2d(sK + c * C::kSlab, &tmK, c * 64, k0, bar_ld);
+        }
+    }
+    bool ok = mbar_wait(bar_ld, 0, abort_flag, p.dev_status);
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16_f32(BT, BT, false, false);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kSlab + (ks & 3) * 32;
+            mma_ss(tmem, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), id, ks > 0);
+        }
+        mma_commit(bar_mma);
+    }
+    ok = ok && mbar_wait(bar_mma, 0, abort_flag, p.dev_status);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (ok) {
+        const float sl2 = p.scale * kLog2e;
+        const float c2 = p.scale * qnorm[q0 + tid] * kmax[head] * kLog2e;  // row bound, log2 domain
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        uint8_t *stage = sm + C::kQOff;  // the Q tile is no longer read: stage E there (two 64-column slabs)
+        float rs = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BT; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + c0, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                pk[t] = pack_bf16(ex2(fmaf(__uint_as_float(r[2 * t]), sl2, -c2)),
+                                  ex2(fmaf(__uint_as_float(r[2 * t + 1]), sl2, -c2)));
+                const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[t]));
+                rs += back.x + back.y;  // the row sum of the values actually stored
+            }
+            const int slab = c0 / 64;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int chunk = ((c0 % 64) / 8) + v;  // 16-byte chunk within the 128-byte row
+                const uint32_t off = slab * C::kSlab + tid * 128 + ((chunk ^ (tid & 7)) * 16);
+                *reinterpret_cast<uint4 *>(stage + off) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+        atomicAdd(rowl + q0 + tid, rs);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tma_store_2d(&tmE, kt * BT, q0, sQ);
+        tma_store_2d(&tmE, kt * BT + 64, q0, sQ + C::kSlab);
+        bulk_commit();
+        bulk_wait_all();
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+template <int D>
+struct OutCfg {
+    static constexpr int kETile = BT * BT * 2;     // 32 KB
+    static constexpr int kVTile = BT * D * 2;
+    static constexpr int kSlab = BT * 128;
+    static constexpr int kStages = D == 64 ? 4 : (D == 128 ? 3 : 2);
+    static constexpr int kEOff = 0;
+    static constexpr int kVOff = kStages * kETile;
+    static constexpr int kBarOff = kVOff + kStages * kVTile;
+    static constexpr int kNumBars = 2 * kStages + 1 + 1;  // full[S], empty[S], done, drain
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+    static constexpr uint32_t kTmemCols = D < 32 ? 32 : D;
+};
+
+// One CTA per 128-row query tile: O = E V over the kept key blocks, then O / l and LSE.
+template <int D>
+__global__ void __launch_bounds__(192, 1) mat_output_kernel(const __grid_constant__ CUtensorMap tmE,
+                                                            const __grid_constant__ CUtensorMap tmV, const Problem p,
+                                                            const float *__restrict__ qnorm,
+                                                            const float *__restrict__ kmax,
+                                                            const float *__restrict__ rowl,
+                                                            __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
+    using C = OutCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t bar0 = smem_addr(sm + C::kBarOff);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    const uint32_t bar_done = bar0 + 8u * (2 * S), bar_drain = bar0 + 8u * (2 * S + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qt = blockIdx.x, head = blockIdx.y;
+    const int nb = p.N / BT;
+    const uint8_t *mrow = p.mask ? p.mask + (size_t)qt * nb : nullptr;
+    int n = 0;
+    for (int j = 0; j < nb; ++j) n += (mrow == nullptr || mrow[j]) ? 1 : 0;
+    const int q0 = head * p.N + qt * BT;
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(bar_done, 1);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sE = smem_addr(sm + C::kEOff), sV = smem_addr(sm + C::kVOff);
+    if (warp == 4) {
+        if (lane == 0 && n > 0) {
+            int it = 0;
+            for (int j = 0; j < nb; ++j) {
+                if (mrow && !mrow[j]) continue;
+                const int s = it % S;
+                if (it >= S &&
+                    !mbar_wait(empty(s), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, p.dev_status))
+                    break;
+                mbar_arrive_expect_tx(full(s), C::kETile + C::kVTile);
+                tma_load_2d(sE + s * C::kETile, &tmE, j * BT, q0, full(s));
+                tma_load_2d(sE + s * C::kETile + C::kSlab, &tmE, j * BT + 64, q0, full(s));
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d(sV + s * C::kVTile + c * C::kSlab, &tmV, c * 64, head * p.N + j * BT, full(s));
+                ++it;
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
+            bool ok = true;
+            for (int it = 0; it < n; ++it) {
+                const int s = it % S;
+                if (!(ok = mbar_wait(full(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                const uint32_t eb = sE + s * C::kETile, vb = sV + s * C::kVTile;
+#pragma unroll
+                for (int ks = 0; ks < BT / 16; ++ks)
+                    mma_ss(tmem, smem_desc_sw128(eb + (ks >> 2) * C::kSlab + (ks & 3) * 32, 16, 1024),
+                           smem_desc_sw128(vb + ks * 2048, C::kSlab, 1024), id, (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(empty(s));
+            }
+            if (ok) {
+                mma_commit(bar_done);
+            } else {
+                mma_commit(bar_drain);
+                mbar_wait(bar_drain, 0, abort_flag, p.dev_status);
+            }
+        }
+    } else {
+        bool ok = true;
+        if (n > 0) {
+            ok = mbar_wait(bar_done, 0, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        const size_t grow = (size_t)q0 + tid;
+        uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
+        if (ok && n > 0) {
+            const float l = rowl[grow];
+            const float inv = 1.f / l;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(lane_base + c0, r);
+                tmem_wait_ld();
+                reg_fence(r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    pk[t] = pack_bf16(__uint_as_float(r[2 * t]) * inv, __uint_as_float(r[2 * t + 1]) * inv);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+            LSE[grow] = p.scale * qnorm[grow] * kmax[head] + __log2f(l) * kLn2;
+        } else if (n == 0) {
+            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
+            LSE[grow] = -INFINITY;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const Problem &p, const MatMaps &m, const void *Q, const void *K, float *qnorm, float *rowl,
+                     float *kmax, void *O, float *LSE, cudaStream_t st) {
+    const size_t rows = (size_t)p.B * p.H * p.N;
+    const int heads = p.B * p.H;
+    {
+        ProfScope prof_("mat_init", st);
+        mat_init_kernel<<<152 * 4, 256, 0, st>>>(rowl, kmax, rows, heads);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    {
+        ProfScope prof_("mat_norms", st);
+        mat_norms_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(Q),
+                                                                         static_cast<const __nv_bfloat16 *>(K), qnorm,
+                                                                         kmax, rows, p.N);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto ks = mat_scores_kernel<D>;
+    if ((e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, ScoreCfg<D>::kSmemBytes)) !=
+        cudaSuccess)
+        return e;
+    {
+        ProfScope prof_("mat_scores", st);
+        ks<<<dim3(p.N / BT, p.N / BT, heads), 128, ScoreCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.e, p, qnorm, kmax, rowl);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto ko = mat_output_kernel<D>;
+    if ((e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, OutCfg<D>::kSmemBytes)) !=
+        cudaSuccess)
+        return e;
+    {
+        ProfScope prof_("mat_output", st);
+        ko<<<dim3(p.N / BT, heads), 192, OutCfg<D>::kSmemBytes, st>>>(m.e, m.v, p, qnorm, kmax, rowl,
+                                                                      static_cast<__nv_bfloat16 *>(O), LSE);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_materialized_bf16(const Problem &p, const MatMaps &maps, const void *Q, const void *K,
+                                         void *E, float *rowc, float *rowl, float *kmax, void *O, float *LSE,
+                                         cudaStream_t st) {
+    (void)E;
+    if (p.B * p.H > 65535 || p.N / BT > 65535) return cudaErrorNotSupported;
+    switch (p.d) {
+        case 64: return launch_d<64>(p, maps, Q, K, rowc, rowl, kmax, O, LSE, st);
+        case 128: return launch_d<128>(p, maps, Q, K, rowc, rowl, kmax, O, LSE, st);
+        case 256: return launch_d<256>(p, maps, Q, K, rowc, rowl, kmax, O, LSE, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 }  // namespace attn
