@@ -277,7 +277,7 @@ def run_cuda(args):
                      else "fallback 1.9 PFLOP/s bf16",
                      "frac_of_sustained": round(achieved / peak_sus, 4),
                      "flops_per_launch": dom_flops / max(1, 1)},
-        "io_model": _io_model(iomodel, N, d, heads, kept),
+        "io_model": _io_model(iomodel, N, d, heads, kept, peaks),
         "kernel_ms_per_step": {kname: round(t / args.steps, 4) for kname, (n, t) in prof.items()},
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
@@ -294,21 +294,43 @@ def run_cuda(args):
         dist.destroy_process_group()
 
 
+KERNEL_SOURCES = {"bwd_main": "bwd_sm103.cu", "bwd_pre": "bwd_sm103.cu", "bwd_dq_convert": "bwd_sm103.cu",
+                  "fwd_bf16": "fwd_sm103.cu"}
+
+
+def _source_hash(kernel):
+    import hashlib
+    csrc = os.path.join(ROOT, "optimal_tiling_gb300", "csrc")
+    m = hashlib.sha256()
+    for f in (KERNEL_SOURCES.get(kernel, ""), "sm103_ptx.cuh", "internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
 def _recorded_traffic(workload, kernel):
-    """DRAM bytes per launch from the committed ncu summary for this kernel and workload, if any."""
+    """DRAM bytes per launch from the committed ncu capture of this kernel on this
+    workload; None when there is none or the kernel source changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)
-        return t.get(workload, {}).get(kernel)
+            rec = json.load(f).get(workload, {}).get(kernel)
+        if rec and rec.get("source_sha256") == _source_hash(kernel):
+            return rec["dram_bytes"]
     except Exception:
-        return None
+        pass
+    return None
 
 
-def _io_model(iomodel, N, d, heads, kept):
+def _io_model(iomodel, N, d, heads, kept, peaks):
     """The pages' leading terms, at the kernels' actual tiles (bf16, w = 2 bytes)."""
     M_smem = 228 * 1024 / 2  # one SM's shared memory in bf16 elements (the pages' M)
+    rep = iomodel.report(N, d, heads, 2, M_smem, float(peaks["hbm_gbs"]) * 1e9, float(peaks["bf16_tflops"]) * 1e12,
+                         kept)
     return {
+        "fwd_time_lower_bound_ms": round(rep["fwd_time_lower_bound_s"] * 1e3, 4),
+        "bwd_time_lower_bound_ms": round(rep["bwd_time_lower_bound_s"] * 1e3, 4),
+        **({"sparse_bound_elements": rep["sparse_bound_elements"]} if "sparse_bound_elements" in rep else {}),
         "M_elements_smem": M_smem,
         "large_cache_regime": iomodel.is_large_cache(M_smem, d),
         "fwd_compulsory_dram_bytes": iomodel.fwd_dram_compulsory_bytes(N, d, heads, 2),
@@ -398,7 +420,7 @@ def _comparison(attn, torch, dev, stream, inputs, iomodel, peaks):
 
 # ------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(w, budget_s: float = 10.0, seed: int = 0):
+def cpu_baseline(w, budget_s: float = 10.0, seed: int = 0, data=None):
     """The oracle (as it stands) on a bounded sample of the workload: R query rows
     of head 0 -- forward (O, LSE) and backward dQ for those rows -- credited with
     R / (B H N) of the step's algorithmic FLOPs."""
@@ -407,7 +429,7 @@ def cpu_baseline(w, budget_s: float = 10.0, seed: int = 0):
 
     oracle.build()
     B, H, N, d = w.shape
-    x, mask = inputs.workload_inputs(w, seed=seed)
+    x, mask = data if data is not None else inputs.workload_inputs(w, seed=seed)
     qh, kh, vh, doh = (x[n][0, 0] for n in ("q", "k", "v", "do"))
     m = None if mask is None else mask.numpy()
     kept = float(mask.float().mean()) if mask is not None else 1.0
@@ -442,9 +464,10 @@ def run_reference(args):
     from optimal_tiling_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    data = inputs.workload_inputs(w, seed=0)
     for _ in range(args.warmup):
-        cpu_baseline(w, budget_s=min(per_step, 4.0))
-    vals = [cpu_baseline(w, budget_s=min(per_step, 8.0)) for _ in range(args.steps)]
+        cpu_baseline(w, budget_s=min(per_step, 4.0), data=data)
+    vals = [cpu_baseline(w, budget_s=min(per_step, 8.0), data=data) for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
     B, H, N, d = w.shape
     out = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "impl": "reference", "n_gpus": 1,

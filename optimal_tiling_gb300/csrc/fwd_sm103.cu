@@ -49,6 +49,12 @@ template <int D>
 struct FwdCfg {
     static constexpr int kChunks = D / 64;                     // 64-element (128 B) swizzle atoms per row
     static constexpr int kStages = D == 64 ? 4 : (D == 128 ? 2 : 1);
+    // exps per 8 pairs evaluated by the FMA-pipe polynomial instead of MUFU
+#ifdef ATTN_FWD_POLY_PAIRS
+    static constexpr int kPolyPairs = ATTN_FWD_POLY_PAIRS;
+#else
+    static constexpr int kPolyPairs = 0;  // measured: every split above 0 is slower on GB300
+#endif
     static constexpr int kTileBytes = BM * D * 2;              // Q tile == K tile == V tile bytes
     static constexpr int kChunkBytes = BM * 128;               // one 64-column slab of a tile
     static constexpr int kQOff = 0;
@@ -224,26 +230,44 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(r[q][t]));
+                for (int t = 0; t < 16; ++t)
+                    mx = fmax3(mx, __uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1]));
             const float m_new = fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
             if (m_new > m_used + kRescaleThreshold) {
                 alpha = ex2(m_used - m_new);
                 m_used = m_new;
             }
-            float rs = 0.f;
+            // p = 2^(s log2e S - m): pairs on the packed FMA path; kPolyPairs of every 8
+            // pairs take the FMA-pipe polynomial, the rest the MUFU ex2.
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m_used, -m_used);
+            uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const float p0 = ex2(fmaf(__uint_as_float(r[q][2 * t]), sl2, -m_used));
-                    const float p1 = ex2(fmaf(__uint_as_float(r[q][2 * t + 1]), sl2, -m_used));
-                    rs += p0 + p1;
-                    pk[t] = pack_bf16(p0, p1);
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1])),
+                                               sl2x2, negm2);
+                    uint64_t y2;
+                    if ((t & 7) < C::kPolyPairs) {
+                        y2 = exp2_poly_pair(x2);
+                    } else {
+                        float x0, x1;
+                        f2_unpack(x2, x0, x1);
+                        y2 = f2_pack(ex2(x0), ex2(x1));
+                    }
+                    sum2 = f2_add(sum2, y2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
+                    pk[t] = pack_bf16(y0, y1);
                 }
                 tmem_st16(scol + q * 16, pk);
             }
+            float rs0, rs1;
+            f2_unpack(sum2, rs0, rs1);
+            const float rs = rs0 + rs1;
             l = l * alpha + rs;
             tmem_wait_st();
             if (it > 0) {

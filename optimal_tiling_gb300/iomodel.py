@@ -128,3 +128,37 @@ def fwd_kv_rescan_bytes(N: int, d: int, heads: int, w: int, rows_per_query_tile:
 def materialized_extra_bytes(N: int, heads: int, w: int) -> float:
     """The stored exp-score matrix: N^2 elements written and read back once."""
     return heads * 2.0 * N * N * w
+
+
+def report(N: int, d: int, heads: int, elem_bytes: int, M: float, hbm_bytes_per_s: float,
+           flops_per_s: float, kept_fraction: float = 1.0) -> dict:
+    """The pages' bounds for one workload, per GPU, as a flat dict.
+
+    M is the fast-memory capacity in elements (the pages' model); the leading
+    terms are per head and multiplied by the head count.  For a block-sparse
+    workload the sparse bound of Theorem 4.5 is evaluated with Z_input = 2 N d
+    (the non-zeros of Q and K, the operands of QK^T) and Z_QK = kept * N^2; the
+    dense forms are scaled by the kept-block fraction.  Time bounds use
+    T >= max(w L / beta, F / P) with L the compulsory elements plus the leading
+    term (ideal overlap; no constant is known for the Theta forms).
+    """
+    fwd_lead = fused_stream_io(N, d, M) if is_large_cache(M, d) else square_tile_io(N, d, M)
+    bwd_lead = bwd_io_bound(N, d, M)
+    out = {
+        "M_elements": M,
+        "large_cache_regime": is_large_cache(M, d),
+        "fwd_leading_elements": heads * fwd_lead * kept_fraction,
+        "fwd_bound_elements": heads * (fwd_lead * kept_fraction + compulsory_io(N, d)),
+        "bwd_leading_elements": heads * bwd_lead * kept_fraction,
+        "fwd_flops": fwd_flops(N, d, heads) * kept_fraction,
+        "bwd_flops": bwd_flops(N, d, heads) * kept_fraction,
+    }
+    out["fwd_time_lower_bound_s"] = time_lower_bound(out["fwd_bound_elements"], elem_bytes, hbm_bytes_per_s,
+                                                     out["fwd_flops"], flops_per_s)
+    out["bwd_time_lower_bound_s"] = time_lower_bound(out["bwd_leading_elements"] + heads * 2 * compulsory_io(N, d),
+                                                     elem_bytes, hbm_bytes_per_s, out["bwd_flops"], flops_per_s)
+    if kept_fraction < 1.0:
+        z_in, z_qk = 2.0 * N * d, kept_fraction * N * N
+        out["sparse_bound_elements"] = heads * sparse_io_bound(z_in, z_qk, M)
+        out["sparse_regime_split_M"] = sparse_regime_split(z_in, z_qk)
+    return out

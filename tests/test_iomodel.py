@@ -62,3 +62,13 @@ def test_time_bound_is_max_of_memory_and_compute():
     t = iomodel.time_lower_bound(1e9, 2, 1e12, 1e12, 1e15)
     assert t == max(2e9 / 1e12, 1e12 / 1e15)
     assert iomodel.elements_in_fast_memory(65536 * 2, 2) == 65536
+
+
+def test_report_at_teaching_example():
+    r = iomodel.report(4096, 64, 1, 2, 65536, 1e12, 1e15)
+    assert r["large_cache_regime"] and r["fwd_leading_elements"] == G["fused_stream_io"]
+    assert r["fwd_bound_elements"] == G["fused_stream_io"] + G["compulsory_io"]
+    assert r["bwd_leading_elements"] == G["bwd_io_large"]
+    assert r["fwd_time_lower_bound_s"] == max(2 * r["fwd_bound_elements"] / 1e12, G["fwd_flops"] / 1e15)
+    s = iomodel.report(4096, 64, 1, 2, 65536, 1e12, 1e15, kept_fraction=0.25)
+    assert s["sparse_bound_elements"] == iomodel.sparse_io_bound(2 * 4096 * 64, 0.25 * 4096 ** 2, 65536)
