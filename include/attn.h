@@ -103,6 +103,30 @@ ATTN_API attn_status attn_bwd(const void *Q, const void *K, const void *V, const
                      const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
                      void *stream);
 
+/*
+ * attn_bwd_static_workspace — attn_bwd for callers that cannot allocate device
+ * memory (the pages have no counterpart: this is a deployment convenience).
+ * Some callers cannot call cudaMalloc: code inside a host framework that owns
+ * every device allocation through its own pool, or a latency-critical path that
+ * must not allocate after start-up (an allocation can synchronise the device).
+ * Same arguments and results as attn_bwd, without the workspace: the scratch
+ * comes from a fixed 64 MiB array compiled into the library, held in device
+ * memory of every GPU that loads the library until the process exits.
+ *   - Shapes whose attn_bwd_workspace_size exceeds 64 MiB return
+ *     ATTN_ERR_WORKSPACE and launch nothing (bf16, d = 128: B*H*N up to
+ *     about 129,000 rows; fp32: B*H*N up to 16 million rows).
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.  No call allocates.
+ *   - Every call on a device shares the array, which keeps the last call's
+ *     contents; the kernels rewrite D and zero the dQ accumulator before use.
+ *     Calls whose work overlaps on the GPU (e.g. unordered streams) race.
+ */
+ATTN_API attn_status attn_bwd_static_workspace(const void *Q, const void *K, const void *V, const void *O,
+                                               const void *dO, const float *LSE, void *dQ, void *dK,
+                                               void *dV, int B, int H, int N, int d, float scale,
+                                               attn_dtype dtype, const uint8_t *block_mask, void *stream);
+
 /* Bytes of scratch attn_fwd_materialized needs (the N x N exp-score matrix and row terms). */
 ATTN_API size_t attn_fwd_materialized_workspace_size(int B, int H, int N, int d, attn_dtype dtype);
 

@@ -65,6 +65,9 @@ def load():
             lib.attn_fwd_materialized.restype = _i
             lib.attn_fwd_materialized_workspace_size.argtypes = [_i, _i, _i, _i, _i]
             lib.attn_fwd_materialized_workspace_size.restype = _sz
+            lib.attn_bwd_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                                      _i, _f, _i, _vp, _vp]
+            lib.attn_bwd_static_workspace.restype = _i
             lib.attn_device_status.argtypes = [_vp]
             lib.attn_device_status.restype = _i
             lib.attn_status_string.argtypes = [_i]
@@ -156,6 +159,23 @@ def attn_bwd(q, k, v, o, do, lse, scale: float, block_mask=None, dq=None, dk=Non
                       B, H, N, d, float(scale), code, _ptr(block_mask), _ptr(workspace),
                       workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_static_workspace(q, k, v, o, do, lse, scale: float, block_mask=None, dq=None, dk=None, dv=None,
+                              stream=None):
+    """attn_bwd without a workspace argument: the scratch is the library's fixed
+    64 MiB device array (for callers that cannot allocate device memory)."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _check(q, k, v, o, do, lse, dq, dk, dv, block_mask)
+    st = lib.attn_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), B, H, N, d, float(scale), _dtype_code(q),
+                                       _ptr(block_mask), _stream(stream))
+    _raise(st, "attn_bwd_static_workspace")
     return dq, dk, dv
 
 
