@@ -46,7 +46,7 @@ constexpr int kThreads = 320;
 constexpr int kDqWarp0 = 4;     // warps 4-7 drain dQ
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStages = 2;      // Q/dO/LSE/D ring depth
+constexpr int kStages = 3;      // Q/dO/LSE/D ring depth (loads run two blocks ahead of the MMAs)
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
@@ -70,6 +70,7 @@ struct BwdCfg {
     static constexpr int kNumBars = 1 + 2 * kStages + 2 * 5 + 2;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
     // tensor memory columns
     static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 2 * BQ;
     static_assert(kColDP + 2 * BQ <= kTmemCols, "tensor memory budget");
@@ -367,38 +368,46 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     } else if (warp < kTmaWarp) {
         // ------------------------------------------------------------ dQ drain warps 4-7
+        // Every drain thread runs the same sequence of named barriers whatever happens:
+        // after a failed (timed-out) wait the work is skipped but the barriers are kept,
+        // and the CTA abort flag makes every later wait return at once.
         const int t = tid - kDqWarp0 * 32;  // 0..127 = d index (tensor memory lane)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         float *dq_gen = reinterpret_cast<float *>(sm + C::kDqOff);
+        bool alive = true;
         for (int it = 0; it < n; ++it) {
             const int b = it & 1;
-            bool ok = mbar_wait(bars.dqfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
+            bool ok = alive && mbar_wait(bars.dqfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
             uint32_t r0[32], r1[32];
-            tmem_ld32(lane_base + C::kColDP + b * BQ, r0);
-            tmem_ld32(lane_base + C::kColDP + b * BQ + 32, r1);
-            tmem_wait_ld();
-            reg_fence(r0);
-            reg_fence(r1);
-            tc_fence_before();
-            mbar_arrive(bars.dqfree(b));
+            if (ok) {
+                tc_fence_after();
+                tmem_ld32(lane_base + C::kColDP + b * BQ, r0);
+                tmem_ld32(lane_base + C::kColDP + b * BQ + 32, r1);
+                tmem_wait_ld();
+                reg_fence(r0);
+                reg_fence(r1);
+                tc_fence_before();
+                mbar_arrive(bars.dqfree(b));
+            }
             // the previous bulk reduction must have finished reading the staging tile
             if (t == 0) bulk_wait_read_all();
             named_bar_sync(1, 128);
+            if (ok) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                dq_gen[q * D + t] = __uint_as_float(r0[q]);
-                dq_gen[(q + 32) * D + t] = __uint_as_float(r1[q]);
+                for (int q = 0; q < 32; ++q) {
+                    dq_gen[q * D + t] = __uint_as_float(r0[q]);
+                    dq_gen[(q + 32) * D + t] = __uint_as_float(r1[q]);
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             named_bar_sync(1, 128);
-            if (t == 0) {
+            if (t == 0 && ok) {
                 const size_t q0 = (size_t)head * p.N + (size_t)qblock(it) * BQ;
                 bulk_reduce_add_f32(dQacc + q0 * D, sDq, C::kDqTile);
                 bulk_commit();
             }
+            alive = alive && ok;
         }
         if (t == 0) bulk_wait_all();
     }

@@ -226,12 +226,16 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             reg_fence(r[1]);
             reg_fence(r[2]);
             reg_fence(r[3]);
-            float mx = -INFINITY;
+            // row max: four independent chains (one per 32-column chunk), then combined
+            float mxq[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q) {
+                mxq[q] = fmaxf(__uint_as_float(r[q][0]), __uint_as_float(r[q][1]));
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    mx = fmax3(mx, __uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1]));
+                for (int t = 1; t < 16; ++t)
+                    mxq[q] = fmax3(mxq[q], __uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1]));
+            }
+            const float mx = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]);
             const float m_new = fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
             if (m_new > m_used + kRescaleThreshold) {
@@ -242,9 +246,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // pairs take the FMA-pipe polynomial, the rest the MUFU ex2.
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t negm2 = f2_pack(-m_used, -m_used);
-            uint64_t sum2 = f2_pack(0.f, 0.f);
+            uint64_t sumq[4];  // four independent row-sum chains
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                sumq[q] = f2_pack(0.f, 0.f);
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
@@ -258,7 +263,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         f2_unpack(x2, x0, x1);
                         y2 = f2_pack(ex2(x0), ex2(x1));
                     }
-                    sum2 = f2_add(sum2, y2);
+                    sumq[q] = f2_add(sumq[q], y2);
                     float y0, y1;
                     f2_unpack(y2, y0, y1);
                     pk[t] = pack_bf16(y0, y1);
@@ -266,7 +271,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tmem_st16(scol + q * 16, pk);
             }
             float rs0, rs1;
-            f2_unpack(sum2, rs0, rs1);
+            f2_unpack(f2_add(f2_add(sumq[0], sumq[1]), f2_add(sumq[2], sumq[3])), rs0, rs1);
             const float rs = rs0 + rs1;
             l = l * alpha + rs;
             tmem_wait_st();
@@ -332,6 +337,307 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA ("ping-pong"): 256 query rows, two softmax
+// warpgroups (warps 0-3: tile A, warps 4-7: tile B), TMA warp 8, MMA warp 9.
+// Tensor memory: S_A, S_B (128 columns each; P overwrites its own S), O_A, O_B
+// (d columns each).  MMA order per key block j:
+//     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+// so the tensor core works on one tile while the other tile's softmax runs, and,
+// because tcgen05 MMAs of one thread complete in issue order, "S_X(j+1) done"
+// also means "PV_X(j) done": the softmax may rescale O_X as soon as it sees
+// S_X(j+1).  Used without a block mask (both tiles visit every key block).
+constexpr int kPPThreads = 320;
+constexpr int kPPTmaWarp = 8;
+constexpr int kPPMmaWarp = 9;
+
+template <int D>
+struct PPCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kTileBytes = BM * D * 2;
+    static constexpr int kChunkBytes = BM * 128;
+    static constexpr int kQOff = 0;                                // Q_A, Q_B
+    static constexpr int kKOff = 2 * kTileBytes;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone[2], drain
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+    static constexpr uint32_t kOCol0 = 256;
+    static __device__ __forceinline__ uint32_t scol(int x) { return x ? 128u : 0u; }
+    static_assert(kOCol0 + 2 * D <= kTmemCols, "tensor memory budget");
+};
+
+struct PPBars {
+    uint32_t base;
+    int stages;
+    __device__ uint32_t q() const { return base; }
+    __device__ uint32_t kfull(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t kempty(int s) const { return base + 8u * (1 + stages + s); }
+    __device__ uint32_t vfull(int s) const { return base + 8u * (1 + 2 * stages + s); }
+    __device__ uint32_t vempty(int s) const { return base + 8u * (1 + 3 * stages + s); }
+    __device__ uint32_t sfull(int x) const { return base + 8u * (1 + 4 * stages + x); }
+    __device__ uint32_t pfull(int x) const { return base + 8u * (3 + 4 * stages + x); }
+    __device__ uint32_t odone(int x) const { return base + 8u * (5 + 4 * stages + x); }
+    __device__ uint32_t drain() const { return base + 8u * (7 + 4 * stages); }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPPThreads, 1)
+fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Problem p, __nv_bfloat16 *__restrict__ O,
+                   float *__restrict__ LSE) {
+    using C = PPCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const PPBars bars{smem_addr(sm + C::kBarOff), S};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int head = blockIdx.y;
+    const int n = p.N / BN;                        // key blocks (no mask on this path)
+    const int row0 = head * p.N + blockIdx.x * 2 * BM;  // first row of tile A; tile B follows
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bars.q(), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bars.kfull(s), 1);
+            mbar_init(bars.kempty(s), 1);
+            mbar_init(bars.vfull(s), 1);
+            mbar_init(bars.vempty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bars.sfull(x), 1);
+            mbar_init(bars.pfull(x), 128);
+            mbar_init(bars.odone(x), 1);
+        }
+        mbar_init(bars.drain(), 1);
+        fence_barrier_init();
+    }
+    if (warp == kPPMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+
+    if (warp == kPPTmaWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(bars.q(), 2 * C::kTileBytes);
+            for (int x = 0; x < 2; ++x)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sQ + x * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * 64, row0 + x * BM, bars.q());
+            for (int j = 0; j < n; ++j) {
+                const int s = j % S;
+                const uint32_t ph = (uint32_t)(j / S) & 1u;
+                const int krow = head * p.N + j * BN;
+                if (j >= S && !mbar_wait(bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(bars.kfull(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sK + s * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(s));
+                if (j >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
+            }
+        }
+    } else if (warp == kPPMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+            auto mma_s = [&](int x, int j) {
+                const uint32_t kb = sK + (j % S) * C::kTileBytes, qb = sQ + x * C::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                    mma_ss(tmem + C::scol(x), smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                           idS, ks > 0);
+                }
+                mma_commit(bars.sfull(x));
+            };
+            auto mma_pv = [&](int x, int j) {
+                const uint32_t vb = sV + (j % S) * C::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ts(tmem + C::kOCol0 + x * D, tmem + C::scol(x) + ks * 8,
+                           smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO, (j > 0 || ks > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status) &&
+                      mbar_wait(bars.kfull(0), 0, abort_flag, p.dev_status);
+            if (ok) {
+                tc_fence_after();
+                mma_s(0, 0);
+                mma_s(1, 0);
+                mma_commit(bars.kempty(0));
+            }
+            for (int j = 0; j < n && ok; ++j) {
+                const int s = j % S;
+                const bool more = j + 1 < n;
+                const uint32_t ph = (uint32_t)j & 1u;
+                if (!(ok = mbar_wait(bars.pfull(0), ph, abort_flag, p.dev_status))) break;
+                if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(j / S) & 1u, abort_flag, p.dev_status))) break;
+                if (more && !(ok = mbar_wait(bars.kfull((j + 1) % S), (uint32_t)((j + 1) / S) & 1u, abort_flag,
+                                             p.dev_status)))
+                    break;
+                tc_fence_after();
+                mma_pv(0, j);
+                if (more) mma_s(0, j + 1);
+                else mma_commit(bars.odone(0));
+                if (!(ok = mbar_wait(bars.pfull(1), ph, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                mma_pv(1, j);
+                mma_commit(bars.vempty(s));
+                if (more) {
+                    mma_s(1, j + 1);
+                    mma_commit(bars.kempty((j + 1) % S));
+                } else {
+                    mma_commit(bars.odone(1));
+                }
+            }
+            if (!ok) {
+                mma_commit(bars.drain());
+                mbar_wait(bars.drain(), 0, abort_flag, p.dev_status);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax, one tile per warpgroup
+        const int x = warp >> 2;  // 0: tile A, 1: tile B
+        const int r = tid & 127;  // row within the tile == tensor memory lane
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t scol = lane_base + C::scol(x);
+        const uint32_t ocol = lane_base + C::kOCol0 + x * D;
+        const float sl2 = p.scale * kLog2e;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = mbar_wait(bars.sfull(x), (uint32_t)j & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t rr[4][32];
+            tmem_ld32(scol + 0, rr[0]);
+            tmem_ld32(scol + 32, rr[1]);
+            tmem_ld32(scol + 64, rr[2]);
+            tmem_ld32(scol + 96, rr[3]);
+            tmem_wait_ld();
+            reg_fence(rr[0]);
+            reg_fence(rr[1]);
+            reg_fence(rr[2]);
+            reg_fence(rr[3]);
+            float mxq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                mxq[q] = fmaxf(__uint_as_float(rr[q][0]), __uint_as_float(rr[q][1]));
+#pragma unroll
+                for (int t = 1; t < 16; ++t)
+                    mxq[q] = fmax3(mxq[q], __uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1]));
+            }
+            const float mx = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]);
+            const float m_new = fmaxf(m_used, mx * sl2);
+            float alpha = 1.f;
+            if (m_new > m_used + kRescaleThreshold) {
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+            }
+            // O_X is complete up to block j-1 (S_X(j) was issued after PV_X(j-1)), and
+            // PV_X(j) waits for this warpgroup: rescale it here when a row's max moved.
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(ocol + c0, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    tmem_st32(ocol + c0, o);
+                }
+            }
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m_used, -m_used);
+            uint64_t sumq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                sumq[q] = f2_pack(0.f, 0.f);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1])),
+                                               sl2x2, negm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[q] = f2_add(sumq[q], f2_pack(y0, y1));
+                    pk[t] = pack_bf16(y0, y1);
+                }
+                tmem_st16(scol + q * 16, pk);
+            }
+            float rs0, rs1;
+            f2_unpack(f2_add(f2_add(sumq[0], sumq[1]), f2_add(sumq[2], sumq[3])), rs0, rs1);
+            l = l * alpha + (rs0 + rs1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bars.pfull(x));
+        }
+        if (ok) {
+            ok = mbar_wait(bars.odone(x), 0, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        if (ok) {
+            const size_t grow = (size_t)row0 + x * BM + r;
+            uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(ocol + c0, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+            LSE[grow] = (m_used + __log2f(l)) * kLn2;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kPPMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_pp(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
+    auto kern = fwd_bf16_pp_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PPCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.N / (2 * BM), p.B * p.H);
+    {
+        ProfScope prof_("fwd_bf16", st);
+        kern<<<grid, kPPThreads, PPCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, p, static_cast<__nv_bfloat16 *>(O), LSE);
+    }
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
     auto kern = fwd_bf16_kernel<D>;
@@ -349,6 +655,13 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
 
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
+#ifndef ATTN_FWD_NO_PINGPONG
+    // two query tiles per CTA when both tiles visit every key block
+    if (p.mask == nullptr && p.N % (2 * BM) == 0) {
+        if (p.d == 64) return launch_pp<64>(p, maps, O, LSE, st);
+        if (p.d == 128) return launch_pp<128>(p, maps, O, LSE, st);
+    }
+#endif
     switch (p.d) {
         case 64: return launch_d<64>(p, maps, O, LSE, st);
         case 128: return launch_d<128>(p, maps, O, LSE, st);
