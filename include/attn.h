@@ -39,8 +39,9 @@
  *               that attn_device_status() reports as ATTN_ERR_TIMEOUT.
  *   Shapes      fp32: any N >= 1, 1 <= d <= 256 (SIMT kernels).
  *               bf16: N a multiple of 128; forward d in {64, 128, 256};
- *               backward d in {64, 128}; materialising forward d in
- *               {64, 128, 256}.  Anything else returns ATTN_ERR_UNSUPPORTED.
+ *               backward d = 128; materialising forward d in {64, 128, 256};
+ *               materialising backward d in {64, 128}.  Anything else returns
+ *               ATTN_ERR_UNSUPPORTED.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -141,6 +142,26 @@ ATTN_API attn_status attn_fwd_materialized(const void *Q, const void *K, const v
                                   float *LSE, int B, int H, int N, int d, float scale,
                                   attn_dtype dtype, const uint8_t *block_mask,
                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of scratch attn_bwd_materialized needs (P and dS, N x N bf16 per head, and D). */
+ATTN_API size_t attn_bwd_materialized_workspace_size(int B, int H, int N, int d, attn_dtype dtype);
+
+/*
+ * attn_bwd_materialized — the small-cache backward schedule of "On Fine-Grained
+ * I/O Complexity of Attention Backward Passes" (gist.science 2410.09397,
+ * "Algorithm 6": the n x n attention matrices are written to slow memory and
+ * read back), as the comparison point for attn_bwd:
+ *   D = rowsum(dO o O);  P = exp(s Q K^T - LSE) and dS = P o (dO V^T - D) are
+ *   stored in the workspace (bf16, N x N per head);  dV = P^T dO,
+ *   dK = s dS^T Q, dQ = s dS K are three GEMMs over them.
+ * Same inputs and outputs as attn_bwd; bf16, N % 128 == 0, d in {64, 128}.
+ * workspace: at least attn_bwd_materialized_workspace_size() bytes.
+ */
+ATTN_API attn_status attn_bwd_materialized(const void *Q, const void *K, const void *V, const void *O,
+                                           const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                                           int B, int H, int N, int d, float scale, attn_dtype dtype,
+                                           const uint8_t *block_mask, void *workspace,
+                                           size_t workspace_bytes, void *stream);
 
 /*
  * attn_device_status — synchronise `stream`, then read and clear the device

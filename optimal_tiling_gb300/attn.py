@@ -68,6 +68,11 @@ def load():
             lib.attn_bwd_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i,
                                                       _i, _f, _i, _vp, _vp]
             lib.attn_bwd_static_workspace.restype = _i
+            lib.attn_bwd_materialized.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
+                                                  _i, _vp, _vp, _sz, _vp]
+            lib.attn_bwd_materialized.restype = _i
+            lib.attn_bwd_materialized_workspace_size.argtypes = [_i, _i, _i, _i, _i]
+            lib.attn_bwd_materialized_workspace_size.restype = _sz
             lib.attn_device_status.argtypes = [_vp]
             lib.attn_device_status.restype = _i
             lib.attn_status_string.argtypes = [_i]
@@ -198,6 +203,30 @@ def attn_fwd_materialized(q, k, v, scale: float, block_mask=None, out=None, lse=
                                    workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(st, "attn_fwd_materialized")
     return out, lse
+
+
+def attn_bwd_materialized_workspace_size(B, H, N, d, dtype_code) -> int:
+    return int(load().attn_bwd_materialized_workspace_size(B, H, N, d, dtype_code))
+
+
+def attn_bwd_materialized(q, k, v, o, do, lse, scale: float, block_mask=None, dq=None, dk=None, dv=None,
+                          workspace=None, stream=None):
+    """dQ, dK, dV through the materialising schedule (P and dS stored in HBM), bf16."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    code = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = attn_bwd_materialized_workspace_size(B, H, N, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    _check(q, k, v, o, do, lse, dq, dk, dv, workspace, block_mask)
+    st = lib.attn_bwd_materialized(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, H, N, d, float(scale), code, _ptr(block_mask), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(st, "attn_bwd_materialized")
+    return dq, dk, dv
 
 
 def attn_device_status(stream=None) -> int:

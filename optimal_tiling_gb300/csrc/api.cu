@@ -81,7 +81,8 @@ attn_status check_common(int B, int H, int N, int d, attn_dtype dt) {
 }
 
 bool bf16_fwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128 || d == 256); }
-bool bf16_bwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
+bool bf16_bwd_shape_ok(int N, int d) { return N % 128 == 0 && d == 128; }
+bool bf16_matbwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
 
 attn_status launch_status(cudaError_t e) {
     if (e == cudaSuccess) return ATTN_OK;
@@ -298,6 +299,46 @@ attn_status attn_fwd_materialized(const void *Q, const void *K, const void *V, v
         !make_map_bf16(&maps.e, E, N, heads * N, 128) || !make_map_bf16(&maps.v, V, d, rows, 128))
         return ATTN_ERR_CUDA;
     return launch_status(attn::launch_fwd_materialized_bf16(p, maps, Q, K, E, rowc, rowl, kmax, O, LSE,
+                                                            static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_bwd_materialized_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
+    if (check_common(B, H, N, d, dtype) != ATTN_OK || dtype != ATTN_DTYPE_BF16) return 0;
+    const size_t heads = (size_t)B * H, rows = heads * N;
+    return 2 * align_up(heads * (size_t)N * N * 2, 256)   // P and dS, bf16
+           + align_up(rows * sizeof(float), 256);          // D
+}
+
+attn_status attn_bwd_materialized(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                  const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d,
+                                  float scale, attn_dtype dtype, const uint8_t *block_mask, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    attn_status s = check_common(B, H, N, d, dtype);
+    if (s != ATTN_OK) return s;
+    if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    const void *ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_BF16 || !bf16_matbwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_bwd_materialized_workspace_size(B, H, N, d, dtype);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    attn::Problem p{B, H, N, d, scale, block_mask, status};
+    const size_t heads = (size_t)B * H, rows = heads * N;
+    char *w = static_cast<char *>(workspace);
+    void *P = w;
+    w += align_up(heads * (size_t)N * N * 2, 256);
+    void *dS = w;
+    w += align_up(heads * (size_t)N * N * 2, 256);
+    float *Dv = reinterpret_cast<float *>(w);
+    attn::MatBwdMaps maps;
+    if (!make_map_bf16(&maps.q, Q, d, rows, 128) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
+        !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.dO, dO, d, rows, 128) ||
+        !make_map_bf16(&maps.p, P, N, rows, 128) || !make_map_bf16(&maps.ds, dS, N, rows, 128))
+        return ATTN_ERR_CUDA;
+    return launch_status(attn::launch_bwd_materialized_bf16(p, maps, O, dO, LSE, Dv, dQ, dK, dV,
                                                             static_cast<cudaStream_t>(stream)));
 }
 

@@ -228,17 +228,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     return false;
                 tc_fence_after();
                 const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile;
+                // S^T and dP^T accumulate into different tensor-memory columns: alternate
+                // their k-steps so that the two dependent chains overlap in the tensor pipe
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
                     const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
                     mma_ss(tmem + C::kColS + b * BQ, smem_desc_sw128(sK + ko, 16, 1024),
                            smem_desc_sw128(qb + qo, 16, 1024), idSP, ks > 0);
-                }
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
-                    const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
                     mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sV + ko, 16, 1024),
                            smem_desc_sw128(gb + qo, 16, 1024), idSP, ks > 0);
                 }
@@ -252,21 +249,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
                 tc_fence_after();
                 const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile, dsb = sDs + b * C::kDsTile;
-                // dV += P^T dO_i : A = P^T (bf16 pairs in the S buffer), B = dO_i (d contiguous)
+                // Three independent accumulators, k-steps interleaved:
+                //   dV += P^T dO_i : A = P^T (bf16 pairs in the S buffer), B = dO_i (d contiguous)
+                //   dK += dS^T Q_i : A = dS^T (K-major, 64 q per row),      B = Q_i (d contiguous)
+                //   dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous); into the dP buffer
 #pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
+                for (int ks = 0; ks < BQ / 16; ++ks) {
                     mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + ks * 8,
                            smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV, (it > 0 || ks > 0) ? 1u : 0u);
-                // dK += dS^T Q_i : A = dS^T (K-major, 64 q per row), B = Q_i (d contiguous)
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks)
                     mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
                            smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV, (it > 0 || ks > 0) ? 1u : 0u);
-                // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous); into the dP buffer
 #pragma unroll
-                for (int ks = 0; ks < BKV / 16; ++ks)
-                    mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sK + ks * 2048, C::kKVSlab, 1024),
-                           smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
+                    for (int kq = 2 * ks; kq < 2 * ks + 2; ++kq)
+                        mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sK + kq * 2048, C::kKVSlab, 1024),
+                               smem_desc_sw128(dsb + kq * 2048, C::kDsTile, 1024), idQ, kq > 0);
+                }
                 mma_commit(bars.qempty(s));
                 mma_commit(bars.dsfree(b));
                 mma_commit(bars.dqfull(b));

@@ -66,4 +66,11 @@ cudaError_t launch_fwd_materialized_bf16(const Problem &p, const MatMaps &maps, 
                                          const void *K, void *E, float *rowc, float *rowl,
                                          float *kmax, void *O, float *LSE, cudaStream_t st);
 
+// Materialising backward: Q, K, V, dO with 128-row boxes; P and dS over [B*H*N, N].
+struct MatBwdMaps {
+    CUtensorMap q, k, v, dO, p, ds;
+};
+cudaError_t launch_bwd_materialized_bf16(const Problem &p, const MatBwdMaps &maps, const void *O, const void *dO,
+                                         const float *LSE, float *Dv, void *dQ, void *dK, void *dV, cudaStream_t st);
+
 }  // namespace attn
