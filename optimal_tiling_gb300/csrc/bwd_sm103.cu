@@ -20,6 +20,12 @@
 //                     dK  += dS^T Q_i        (A = dS^T from shared memory)
 //                     dQ_i^T = K^T dS_i^T    (M = d: into the dP buffer, which the
 //                                             softmax warps have already read)
+//                   The MMAs come from three warps, because one thread issues a
+//                   tcgen05.mma only every ~100 cycles while the tensor core takes
+//                   them several times faster: warp 9 issues S^T then dV (so that
+//                   S^T of block i+2 follows, in one thread's issue order, the dV
+//                   that read P of block i from the same columns), warp 10 dP^T then
+//                   dK, warp 11 dQ^T.
 //                   dQ_i^T is drained by its own warpgroup into shared memory as
 //                   [q][d] fp32 and added into the accumulator with one bulk
 //                   reduction (cp.reduce.async.bulk .add.f32).  S/dP are double
@@ -42,10 +48,10 @@ using namespace ptx;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int BKV = 128;   // key/value rows per CTA
 constexpr int BQ = 64;     // query rows per inner block
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kDqWarp0 = 4;     // warps 4-7 drain dQ
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;     // warps 9, 10, 11 issue MMAs (see the kernel comment)
 constexpr int kStages = 3;      // Q/dO/LSE/D ring depth (loads run two blocks ahead of the MMAs)
 constexpr uint32_t kTmemCols = 512;
 
@@ -66,8 +72,8 @@ struct BwdCfg {
     static constexpr int kDqOff = kDsOff + 2 * kDsTile;
     static constexpr int kLdOff = kDqOff + kDqTile;      // per stage: LSE[64], D[64]
     static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
-    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull[2], dqfree[2], kvdone, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 5 + 2;
+    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull[2], dqfree[2], kvdone, drain[3]
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 5 + 1 + 3;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -87,7 +93,7 @@ struct BwdBars {
     __device__ uint32_t dqfull(int b) const { return base + 8u * (7 + 2 * kStages + b); }
     __device__ uint32_t dqfree(int b) const { return base + 8u * (9 + 2 * kStages + b); }
     __device__ uint32_t kvdone() const { return base + 8u * (11 + 2 * kStages); }
-    __device__ uint32_t drain() const { return base + 8u * (12 + 2 * kStages); }
+    __device__ uint32_t drain(int role) const { return base + 8u * (12 + 2 * kStages + role); }
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -158,17 +164,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bars.kv(), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bars.qfull(s), 1);
-            mbar_init(bars.qempty(s), 1);
+            mbar_init(bars.qempty(s), 2);   // dV (warp 9) and dK (warp 10) are the last readers
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bars.sfull(b), 1);
+            mbar_init(bars.sfull(b), 2);    // S^T (warp 9) and dP^T (warp 10)
             mbar_init(bars.pfull(b), 128);
-            mbar_init(bars.dsfree(b), 1);
+            mbar_init(bars.dsfree(b), 2);   // dK (warp 10) and dQ^T (warp 11) read dS
             mbar_init(bars.dqfull(b), 1);
             mbar_init(bars.dqfree(b), 128);
         }
-        mbar_init(bars.kvdone(), 1);
-        mbar_init(bars.drain(), 1);
+        mbar_init(bars.kvdone(), 2);        // dV and dK complete
+        for (int r = 0; r < 3; ++r) mbar_init(bars.drain(r), 1);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -212,67 +218,84 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 bulk_load(sLd + s * 2 * BQ * 4 + BQ * 4, Dv + q0, BQ * 4, bars.qfull(s));
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp >= kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        const int role = warp - kMmaWarp;  // 0: S^T then dV, 1: dP^T then dK, 2: dQ^T
         if (lane == 0 && n > 0) {
             constexpr uint32_t idSP = idesc_bf16_f32(BKV, BQ, false, false);  // S^T, dP^T
             constexpr uint32_t idKV = idesc_bf16_f32(BKV, D, false, true);    // dV, dK
             constexpr uint32_t idQ = idesc_bf16_f32(D, BQ, true, true);       // dQ^T
             bool ok = mbar_wait(bars.kv(), 0, abort_flag, p.dev_status);
-            // S^T_it and dP^T_it into buffer it & 1
-            auto issue_sdp = [&](int it) -> bool {
-                const int s = it % kStages, b = it & 1;
-                if (!mbar_wait(bars.qfull(s), (uint32_t)(it / kStages) & 1u, abort_flag, p.dev_status)) return false;
-                // the dP buffer held dQ^T of block it-2: wait until it was drained
-                if (it >= 2 && !mbar_wait(bars.dqfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status))
-                    return false;
-                tc_fence_after();
-                const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile;
-                // S^T and dP^T accumulate into different tensor-memory columns: alternate
-                // their k-steps so that the two dependent chains overlap in the tensor pipe
+            if (role < 2) {
+                // S^T_it (role 0) or dP^T_it (role 1) into buffer it & 1
+                auto issue_first = [&](int it) -> bool {
+                    const int s = it % kStages, b = it & 1;
+                    if (!mbar_wait(bars.qfull(s), (uint32_t)(it / kStages) & 1u, abort_flag, p.dev_status))
+                        return false;
+                    // the dP buffer held dQ^T of block it-2: wait until it was drained
+                    if (role == 1 && it >= 2 &&
+                        !mbar_wait(bars.dqfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t xb = (role == 0 ? sQ : sdO) + s * C::kQTile;
+                    const uint32_t kb = role == 0 ? sK : sV;
+                    const uint32_t dcol = tmem + (role == 0 ? C::kColS : C::kColDP) + b * BQ;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
-                    const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
-                    mma_ss(tmem + C::kColS + b * BQ, smem_desc_sw128(sK + ko, 16, 1024),
-                           smem_desc_sw128(qb + qo, 16, 1024), idSP, ks > 0);
-                    mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sV + ko, 16, 1024),
-                           smem_desc_sw128(gb + qo, 16, 1024), idSP, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
+                        const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
+                        mma_ss(dcol, smem_desc_sw128(kb + ko, 16, 1024), smem_desc_sw128(xb + qo, 16, 1024), idSP,
+                               ks > 0);
+                    }
+                    mma_commit(bars.sfull(b));
+                    return true;
+                };
+                if (ok) ok = issue_first(0);
+                for (int it = 0; it < n && ok; ++it) {
+                    const int s = it % kStages, b = it & 1;
+                    if (it + 1 < n && !(ok = issue_first(it + 1))) break;
+                    if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                    tc_fence_after();
+                    const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile, dsb = sDs + b * C::kDsTile;
+                    if (role == 0) {
+                        // dV += P^T dO_i : A = P^T (bf16 pairs in the S buffer), B = dO_i (d contiguous)
+#pragma unroll
+                        for (int ks = 0; ks < BQ / 16; ++ks)
+                            mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + ks * 8,
+                                   smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV,
+                                   (it > 0 || ks > 0) ? 1u : 0u);
+                    } else {
+                        // dK += dS^T Q_i : A = dS^T (K-major, 64 q per row), B = Q_i (d contiguous)
+#pragma unroll
+                        for (int ks = 0; ks < BQ / 16; ++ks)
+                            mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
+                                   smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV,
+                                   (it > 0 || ks > 0) ? 1u : 0u);
+                        mma_commit(bars.dsfree(b));
+                    }
+                    mma_commit(bars.qempty(s));
                 }
-                mma_commit(bars.sfull(b));
-                return true;
-            };
-            if (ok) ok = issue_sdp(0);
-            for (int it = 0; it < n && ok; ++it) {
-                const int s = it % kStages, b = it & 1;
-                if (it + 1 < n && !(ok = issue_sdp(it + 1))) break;
-                if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
-                tc_fence_after();
-                const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile, dsb = sDs + b * C::kDsTile;
-                // Three independent accumulators, k-steps interleaved:
-                //   dV += P^T dO_i : A = P^T (bf16 pairs in the S buffer), B = dO_i (d contiguous)
-                //   dK += dS^T Q_i : A = dS^T (K-major, 64 q per row),      B = Q_i (d contiguous)
-                //   dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous); into the dP buffer
-#pragma unroll
-                for (int ks = 0; ks < BQ / 16; ++ks) {
-                    mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + ks * 8,
-                           smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV, (it > 0 || ks > 0) ? 1u : 0u);
-                    mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
-                           smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV, (it > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kq = 2 * ks; kq < 2 * ks + 2; ++kq)
-                        mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sK + kq * 2048, C::kKVSlab, 1024),
-                               smem_desc_sw128(dsb + kq * 2048, C::kDsTile, 1024), idQ, kq > 0);
-                }
-                mma_commit(bars.qempty(s));
-                mma_commit(bars.dsfree(b));
-                mma_commit(bars.dqfull(b));
-            }
-            if (ok) {
-                mma_commit(bars.kvdone());
+                if (ok) mma_commit(bars.kvdone());
             } else {
-                mma_commit(bars.drain());
-                mbar_wait(bars.drain(), 0, abort_flag, p.dev_status);
+                for (int it = 0; it < n && ok; ++it) {
+                    const int b = it & 1;
+                    if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                    tc_fence_after();
+                    const uint32_t dsb = sDs + b * C::kDsTile;
+                    // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous); into the dP
+                    // buffer, whose dP^T the softmax warps have read (pfull)
+#pragma unroll
+                    for (int ks = 0; ks < BKV / 16; ++ks)
+                        mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sK + ks * 2048, C::kKVSlab, 1024),
+                               smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
+                    mma_commit(bars.dsfree(b));
+                    mma_commit(bars.dqfull(b));
+                }
+            }
+            if (!ok) {
+                // let every MMA this thread issued finish before tensor memory is released
+                mma_commit(bars.drain(role));
+                mbar_wait(bars.drain(role), 0, abort_flag, p.dev_status);
             }
         }
     } else if (warp < kDqWarp0) {

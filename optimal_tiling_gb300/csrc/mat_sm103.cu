@@ -14,10 +14,12 @@
 // Kernels (caller's stream): mat_init (zero l and the per-head key-norm max),
 // mat_norms (|q_i| and the per-head max |k_j|), mat_scores (tcgen05 S tile ->
 // E tile, bf16, TMA-stored; row sums of the stored values added into l),
-// mat_output (tcgen05 O = E V over the kept key blocks, O / l and LSE).
+// mat_output (the shared block GEMM of gemm_sm103.cuh: O = E V over the kept
+// key blocks, then O / l and LSE).
 // Key blocks removed by the block mask are neither written nor read.
 #include <cuda_bf16.h>
 
+#include "gemm_sm103.cuh"
 #include "internal.h"
 #include "sm103_ptx.cuh"
 
@@ -173,144 +175,26 @@ __global__ void __launch_bounds__(128) mat_scores_kernel(const __grid_constant__
     }
 }
 
+// O = E V / l and LSE = c + ln l, as the epilogue of the shared block GEMM
+// (one CTA per 128-row query tile, E blocks in K-major orientation).
 template <int D>
-struct OutCfg {
-    static constexpr int kETile = BT * BT * 2;     // 32 KB
-    static constexpr int kVTile = BT * D * 2;
-    static constexpr int kSlab = BT * 128;
-    static constexpr int kStages = D == 64 ? 4 : (D == 128 ? 3 : 2);
-    static constexpr int kEOff = 0;
-    static constexpr int kVOff = kStages * kETile;
-    static constexpr int kBarOff = kVOff + kStages * kVTile;
-    static constexpr int kNumBars = 2 * kStages + 1 + 1;  // full[S], empty[S], done, drain
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
-    static constexpr uint32_t kTmemCols = D < 32 ? 32 : D;
+struct MatOutEpi {
+    __nv_bfloat16 *O;
+    float *LSE;
+    const float *rowl, *qnorm, *kmax;
+    float scale;
+    int N;
+    __device__ void operator()(size_t grow, const uint32_t (&r)[32], int c0) const {
+        gemm::store_row_chunk<D>(O, grow, r, c0, 1.f / rowl[grow]);
+    }
+    __device__ void finish(size_t grow) const {
+        LSE[grow] = scale * qnorm[grow] * kmax[grow / N] + __log2f(rowl[grow]) * kLn2;
+    }
+    __device__ void empty(size_t grow) const {
+        gemm::zero_row<D>(O, grow);
+        LSE[grow] = -INFINITY;
+    }
 };
-
-// One CTA per 128-row query tile: O = E V over the kept key blocks, then O / l and LSE.
-template <int D>
-__global__ void __launch_bounds__(192, 1) mat_output_kernel(const __grid_constant__ CUtensorMap tmE,
-                                                            const __grid_constant__ CUtensorMap tmV, const Problem p,
-                                                            const float *__restrict__ qnorm,
-                                                            const float *__restrict__ kmax,
-                                                            const float *__restrict__ rowl,
-                                                            __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
-    using C = OutCfg<D>;
-    constexpr int S = C::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t bar0 = smem_addr(sm + C::kBarOff);
-    auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
-    const uint32_t bar_done = bar0 + 8u * (2 * S), bar_drain = bar0 + 8u * (2 * S + 1);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qt = blockIdx.x, head = blockIdx.y;
-    const int nb = p.N / BT;
-    const uint8_t *mrow = p.mask ? p.mask + (size_t)qt * nb : nullptr;
-    int n = 0;
-    for (int j = 0; j < nb; ++j) n += (mrow == nullptr || mrow[j]) ? 1 : 0;
-    const int q0 = head * p.N + qt * BT;
-    if (tid == 0) {
-        *abort_flag = 0;
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
-        }
-        mbar_init(bar_done, 1);
-        mbar_init(bar_drain, 1);
-        fence_barrier_init();
-    }
-    if (warp == 5) {
-        tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t sE = smem_addr(sm + C::kEOff), sV = smem_addr(sm + C::kVOff);
-    if (warp == 4) {
-        if (lane == 0 && n > 0) {
-            int it = 0;
-            for (int j = 0; j < nb; ++j) {
-                if (mrow && !mrow[j]) continue;
-                const int s = it % S;
-                if (it >= S &&
-                    !mbar_wait(empty(s), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, p.dev_status))
-                    break;
-                mbar_arrive_expect_tx(full(s), C::kETile + C::kVTile);
-                tma_load_2d(sE + s * C::kETile, &tmE, j * BT, q0, full(s));
-                tma_load_2d(sE + s * C::kETile + C::kSlab, &tmE, j * BT + 64, q0, full(s));
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_2d(sV + s * C::kVTile + c * C::kSlab, &tmV, c * 64, head * p.N + j * BT, full(s));
-                ++it;
-            }
-        }
-    } else if (warp == 5) {
-        if (lane == 0 && n > 0) {
-            constexpr uint32_t id = idesc_bf16_f32(BT, D, false, true);
-            bool ok = true;
-            for (int it = 0; it < n; ++it) {
-                const int s = it % S;
-                if (!(ok = mbar_wait(full(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
-                tc_fence_after();
-                const uint32_t eb = sE + s * C::kETile, vb = sV + s * C::kVTile;
-#pragma unroll
-                for (int ks = 0; ks < BT / 16; ++ks)
-                    mma_ss(tmem, smem_desc_sw128(eb + (ks >> 2) * C::kSlab + (ks & 3) * 32, 16, 1024),
-                           smem_desc_sw128(vb + ks * 2048, C::kSlab, 1024), id, (it > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(empty(s));
-            }
-            if (ok) {
-                mma_commit(bar_done);
-            } else {
-                mma_commit(bar_drain);
-                mbar_wait(bar_drain, 0, abort_flag, p.dev_status);
-            }
-        }
-    } else {
-        bool ok = true;
-        if (n > 0) {
-            ok = mbar_wait(bar_done, 0, abort_flag, p.dev_status);
-            ok = __all_sync(0xffffffffu, ok);
-            tc_fence_after();
-        }
-        const size_t grow = (size_t)q0 + tid;
-        uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
-        if (ok && n > 0) {
-            const float l = rowl[grow];
-            const float inv = 1.f / l;
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(lane_base + c0, r);
-                tmem_wait_ld();
-                reg_fence(r);
-                uint32_t pk[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    pk[t] = pack_bf16(__uint_as_float(r[2 * t]) * inv, __uint_as_float(r[2 * t + 1]) * inv);
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
-            LSE[grow] = p.scale * qnorm[grow] * kmax[head] + __log2f(l) * kLn2;
-        } else if (n == 0) {
-            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
-            LSE[grow] = -INFINITY;
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::kTmemCols);
-    }
-}
 
 template <int D>
 cudaError_t launch_d(const Problem &p, const MatMaps &m, const void *Q, const void *K, float *qnorm, float *rowl,
@@ -339,16 +223,9 @@ cudaError_t launch_d(const Problem &p, const MatMaps &m, const void *Q, const vo
         ks<<<dim3(p.N / BT, p.N / BT, heads), 128, ScoreCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.e, p, qnorm, kmax, rowl);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    auto ko = mat_output_kernel<D>;
-    if ((e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, OutCfg<D>::kSmemBytes)) !=
-        cudaSuccess)
-        return e;
-    {
-        ProfScope prof_("mat_output", st);
-        ko<<<dim3(p.N / BT, heads), 192, OutCfg<D>::kSmemBytes, st>>>(m.e, m.v, p, qnorm, kmax, rowl,
-                                                                      static_cast<__nv_bfloat16 *>(O), LSE);
-    }
-    return cudaGetLastError();
+    return gemm::launch_block_gemm<D, false>(
+        "mat_output", p, m.e, m.v,
+        MatOutEpi<D>{static_cast<__nv_bfloat16 *>(O), LSE, rowl, qnorm, kmax, p.scale, p.N}, st);
 }
 
 }  // namespace
