@@ -70,6 +70,8 @@ def _bind(lib):
     lib.oracle_bwd_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, _u8p,
                                     _dp, _dp, _dp, _dp, ctypes.c_int, _ip, _dp,
                                     ctypes.c_int, _ip, _dp, _dp]
+    lib.oracle_fwd_rect.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                    _dp, _dp, _dp, _dp, _dp]
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
 
@@ -241,3 +243,17 @@ def bwd_rows(q, k, v, do, scale: float, qrows, krows, mask=None, _oracle=None):
                         int(qr.size), qr.ctypes.data_as(_ip), _ptr(dQ),
                         int(kr.size), kr.ctypes.data_as(_ip), _ptr(dK), _ptr(dV))
     return dQ, dK, dV
+
+
+def fwd_rect(q, k, v, scale: float, _oracle=None):
+    """Rectangular forward: q [..., Nq, d] against k, v [..., Nk, d] (no mask)."""
+    lib = _oracle.lib if _oracle is not None else _load()
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    if K.shape != V.shape or Q.shape[:-2] != K.shape[:-2] or Q.shape[-1] != K.shape[-1]:
+        raise ValueError("q [..., Nq, d], k and v [..., Nk, d] with the same leading dims and d")
+    nh, Nq, d = _heads(Q)
+    Nk = K.shape[-2]
+    O = np.empty_like(Q)
+    LSE = np.empty(Q.shape[:-1], dtype=np.float64)
+    lib.oracle_fwd_rect(nh, Nq, Nk, d, float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE))
+    return O, LSE

@@ -374,6 +374,46 @@ void oracle_bwd_rows(int N, int d, double s, const uint8_t *mask,
     free(Lall);
 }
 
+/*
+ * Rectangular forward: Nq queries against Nk keys per head, no mask
+ * ("The I/O Complexity of Attention" exposition, end of "From a movement lower
+ * bound to a performance upper bound": single-token decoding has query length
+ * one and needs a rectangular account).  Same definition as the square case:
+ * S_i. = s q_i K^T over the Nk keys, LSE_i = log sum_j e^{S_ij} with the exact
+ * row max, o_i = sum_j e^{S_ij - LSE_i} v_j.
+ * Q, O: [nh][Nq][d]; K, V: [nh][Nk][d]; LSE: [nh][Nq].
+ */
+void oracle_fwd_rect(int nh, int Nq, int Nk, int d, double s,
+                     const double *Q, const double *K, const double *V,
+                     double *O, double *LSE)
+{
+#pragma omp parallel
+    {
+        double *srow = (double *)malloc((size_t)Nk * sizeof(double));
+#pragma omp for collapse(2) schedule(dynamic, 1)
+        for (int h = 0; h < nh; ++h)
+            for (int i = 0; i < Nq; ++i) {
+                const double *q = Q + ((size_t)h * Nq + i) * d;
+                const double *Kh = K + (size_t)h * Nk * d, *Vh = V + (size_t)h * Nk * d;
+                double *o = O + ((size_t)h * Nq + i) * d;
+                double mx = -INFINITY;
+                for (int j = 0; j < Nk; ++j) {
+                    srow[j] = s * dot(q, Kh + (size_t)j * d, d);
+                    if (srow[j] > mx) mx = srow[j];
+                }
+                double L = row_lse(srow, Nk, mx);
+                LSE[(size_t)h * Nq + i] = L;
+                for (int t = 0; t < d; ++t) o[t] = 0.0;
+                for (int j = 0; j < Nk; ++j) {
+                    double p = exp(srow[j] - L);
+                    const double *vj = Vh + (size_t)j * d;
+                    for (int t = 0; t < d; ++t) o[t] += p * vj[t];
+                }
+            }
+        free(srow);
+    }
+}
+
 /* Number of OpenMP threads the oracle runs with (for reporting). */
 int oracle_num_threads(void)
 {

@@ -249,6 +249,34 @@ def test_fwd_rows_matches_full(oracle_mod):
         assert np.array_equal(Or[n], O[h, i]) and Lr[n] == L[h, i]
 
 
+# --------------------------------------------------------------------------- rectangular (decode)
+
+def test_rect_matches_library_and_square_rows(oracle_mod):
+    """Nq queries against Nk keys: equals the library evaluation, and each query
+    row equals the same row of a square problem that shares the keys."""
+    Nq, Nk, d = 5, 300, 16
+    Q, K, V = _rand((2, Nq, d), 90), _rand((2, Nk, d), 91), _rand((2, Nk, d), 92)
+    O, L = oracle_mod.fwd_rect(Q, K, V, 0.3)
+    Or, Lr = _torch_attention(Q, K, V, 0.3)
+    assert np.max(np.abs(O - Or)) < 1e-12 and np.max(np.abs(L - Lr)) < 1e-12
+    Qsq = _rand((2, Nk, d), 93)
+    Qsq[:, 17:17 + Nq] = Q
+    Osq, Lsq = oracle_mod.fwd_naive(Qsq, K, V, 0.3)
+    assert np.max(np.abs(O - Osq[:, 17:17 + Nq])) < 1e-13 and np.max(np.abs(L - Lsq[:, 17:17 + Nq])) < 1e-13
+
+
+def test_rect_single_key_and_zero_query(oracle_mod):
+    """Nk = 1 gives O = v and LSE = s q.k; q = 0 gives the column mean and ln Nk."""
+    q, k, v = _rand((3, 2, 6), 94), _rand((3, 1, 6), 95), _rand((3, 1, 6), 96)
+    O, L = oracle_mod.fwd_rect(q, k, v, 0.7)
+    assert np.max(np.abs(O - v)) < 1e-15
+    assert np.max(np.abs(L - 0.7 * np.einsum("hqd,hkd->hq", q, k))) < 1e-14
+    K, V = _rand((1, 77, 4), 97), _rand((1, 77, 4), 98)
+    O, L = oracle_mod.fwd_rect(np.zeros((1, 3, 4)), K, V, 1.0)
+    assert np.max(np.abs(O - V.mean(axis=1, keepdims=True))) < 1e-14
+    assert np.max(np.abs(L - math.log(77))) < 1e-14
+
+
 # --------------------------------------------------------------------------- backward
 
 def _loss(oracle_mod, Q, K, V, G, s, mask):
@@ -351,6 +379,12 @@ MUTATIONS = [
     ("dV takes dS instead of P",
      "dv[t] += P * doi[t];",
      "dv[t] += dS * doi[t];"),
+    ("rectangular: scale dropped",
+     "srow[j] = s * dot(q, Kh + (size_t)j * d, d);",
+     "srow[j] = dot(q, Kh + (size_t)j * d, d);"),
+    ("rectangular: weights not normalised",
+     "double p = exp(srow[j] - L);\n                    const double *vj = Vh",
+     "double p = exp(srow[j] - mx);\n                    const double *vj = Vh"),
 ]
 
 
@@ -365,6 +399,11 @@ def _pins_pass(oracle_mod, handle) -> bool:
         return False
     O2, L2 = oracle_mod.fwd_stream(Q, K, V, s, [17, 64, 130], _oracle=handle)
     if not (np.max(np.abs(O - O2)) < 1e-12):
+        return False
+    Qr, Kr, Vr = _rand((3, d), 88), _rand((N, d), 86), _rand((N, d), 87)
+    Orr, Lrr = oracle_mod.fwd_rect(Qr[None], Kr[None], Vr[None], s, _oracle=handle)
+    Ort, Lrt = _torch_attention(Qr, Kr, Vr, s)
+    if not (np.max(np.abs(Orr[0] - Ort)) < 1e-12 and np.max(np.abs(Lrr[0] - Lrt)) < 1e-12):
         return False
     dQ, dK, dV, _, _ = oracle_mod.bwd_naive(Q, K, V, dO, s, _oracle=handle)
     Qt, Kt, Vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
