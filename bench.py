@@ -78,25 +78,33 @@ def _sum_over_ranks(dist, value: float, device=None) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """nvidia-smi clock / throttle samples; only samples stamped inside the timed
+    region (between mark_start() and mark_end(), host wall clock) are kept."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.5)  # let nvidia-smi start sampling before the timed region
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         self.lines = []
@@ -110,25 +118,40 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text.strip(), fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, n_all = [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
+                continue
+            n_all += 1
+            ts = self._stamp(f[0])
+            if ts is None or self.t0 is None or not (self.t0 <= ts <= self.t1):
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                sm.append(float(f[2]))
+                mx = float(f[3])
             except ValueError:
                 continue
-            for nm, val in zip(names, f[5:9]):
+            for nm, val in zip(names, f[6:10]):
                 if val.lower() == "active":
                     reasons.add(nm)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples in the timed region"],
+                    "samples_total": n_all}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm)}
 
 
 def _profile_kernels(lib):
@@ -205,11 +228,13 @@ def run_cuda(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.mark_start()
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark_end()
     if dist is not None:
         dist.barrier()
     lib.attn_profile_enable(0)
@@ -302,7 +327,7 @@ def _source_hash(kernel):
     import hashlib
     csrc = os.path.join(ROOT, "optimal_tiling_gb300", "csrc")
     m = hashlib.sha256()
-    for f in (KERNEL_SOURCES.get(kernel, ""), "sm103_ptx.cuh", "internal.h"):
+    for f in (KERNEL_SOURCES.get(kernel, ""), "sm103_ptx.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:16]
@@ -484,7 +509,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="dense_16k")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
