@@ -73,6 +73,10 @@ def load():
             lib.attn_bwd_materialized.restype = _i
             lib.attn_bwd_materialized_workspace_size.argtypes = [_i, _i, _i, _i, _i]
             lib.attn_bwd_materialized_workspace_size.restype = _sz
+            lib.attn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]
+            lib.attn_decode.restype = _i
+            lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+            lib.attn_decode_workspace_size.restype = _sz
             lib.attn_device_status.argtypes = [_vp]
             lib.attn_device_status.restype = _i
             lib.attn_status_string.argtypes = [_i]
@@ -227,6 +231,32 @@ def attn_bwd_materialized(q, k, v, o, do, lse, scale: float, block_mask=None, dq
                                    workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(st, "attn_bwd_materialized")
     return dq, dk, dv
+
+
+def attn_decode_workspace_size(B, H, Nq, Nk, d, dtype_code) -> int:
+    return int(load().attn_decode_workspace_size(B, H, Nq, Nk, d, dtype_code))
+
+
+def attn_decode(q, k, v, scale: float, out=None, lse=None, workspace=None, stream=None):
+    """Decode-shaped attention: q [B, H, Nq, d] against k, v [B, H, Nk, d] (bf16)."""
+    lib = load()
+    B, H, Nq, d = _shape(q)
+    Nk = int(k.shape[2])
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    need = attn_decode_workspace_size(B, H, Nq, Nk, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    _check(q, k, v, out, lse, workspace)
+    st = lib.attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, float(scale), code,
+                         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(st, "attn_decode")
+    return out, lse
 
 
 def attn_device_status(stream=None) -> int:

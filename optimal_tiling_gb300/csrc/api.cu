@@ -342,6 +342,37 @@ attn_status attn_bwd_materialized(const void *Q, const void *K, const void *V, c
                                                             static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+attn_status check_decode(int B, int H, int Nq, int Nk, int d, attn_dtype dtype) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_DTYPE_BF16 || Nq > 16 || !(d == 64 || d == 128 || d == 256)) return ATTN_ERR_UNSUPPORTED;
+    if ((uint64_t)B * H > 65535 || (uint64_t)B * H * Nk > (1ull << 31)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+}  // namespace
+
+size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d, attn_dtype dtype) {
+    if (check_decode(B, H, Nq, Nk, d, dtype) != ATTN_OK) return 0;
+    return attn::decode_workspace_bytes(attn::decode_shape(B, H, Nq, Nk, d, 1.f));
+}
+
+attn_status attn_decode(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int Nq,
+                        int Nk, int d, float scale, attn_dtype dtype, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    attn_status s = check_decode(B, H, Nq, Nk, d, dtype);
+    if (s != ATTN_OK) return s;
+    if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+        return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    const attn::DecodeShape sh = attn::decode_shape(B, H, Nq, Nk, d, scale);
+    if (workspace == nullptr || workspace_bytes < attn::decode_workspace_bytes(sh) || !aligned16(workspace))
+        return ATTN_ERR_WORKSPACE;
+    return launch_status(attn::launch_decode_bf16(sh, Q, K, V, O, LSE, static_cast<float *>(workspace),
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 attn_status attn_device_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     int *status = device_status_ptr();

@@ -73,4 +73,15 @@ struct MatBwdMaps {
 cudaError_t launch_bwd_materialized_bf16(const Problem &p, const MatBwdMaps &maps, const void *O, const void *dO,
                                          const float *LSE, float *Dv, void *dQ, void *dK, void *dV, cudaStream_t st);
 
+// Decode-shaped attention (Nq <= 16 queries against Nk keys, split over keys).
+struct DecodeShape {
+    int B, H, Nq, Nk, d;
+    float scale;
+    int splits, keys_per_split;
+};
+DecodeShape decode_shape(int B, int H, int Nq, int Nk, int d, float scale);
+size_t decode_workspace_bytes(const DecodeShape &sh);
+cudaError_t launch_decode_bf16(const DecodeShape &sh, const void *Q, const void *K, const void *V, void *O,
+                               float *LSE, float *part, cudaStream_t st);
+
 }  // namespace attn

@@ -80,6 +80,21 @@ def make_inputs(B: int, H: int, N: int, d: int, dtype=torch.bfloat16, seed: int 
     return out
 
 
+def make_decode_inputs(B: int, H: int, Nq: int, Nk: int, d: int, dtype=torch.bfloat16, seed: int = 0):
+    """Rectangular (decode-shaped) inputs: Q [B, H, Nq, d], then K and V [B, H, Nk, d],
+    drawn in that order from one seeded CPU generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = {"q": torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32)}
+    for nm in ("k", "v"):
+        out[nm] = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    return {k: (v.to(dtype) if dtype != torch.float32 else v) for k, v in out.items()}
+
+
+# Decode workload: one new query per head against a 32k-token K/V cache held in HBM.
+DECODE_WORKLOAD = {"name": "decode_32k", "B": 8, "H": 32, "Nq": 1, "Nk": 32768, "d": 128}
+
+
 def num_mask_blocks(N: int) -> int:
     return (N + MASK_BLOCK - 1) // MASK_BLOCK
 
