@@ -310,6 +310,7 @@ def run_cuda(args):
     }
     if not args.no_comparison and rank == 0:
         result["comparison"] = _comparison(attn, torch, dev, stream, inputs, iomodel, peaks)
+        result["decode"] = _decode(attn, torch, dev, stream, inputs, peaks)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -367,44 +368,78 @@ def _io_model(iomodel, N, d, heads, kept, peaks):
 
 
 def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist):
-    """Same metric through the public API with host buffers: pinned H2D of the
-    step's inputs, fwd + bwd, D2H of every result, all inside the timed region."""
+    """Same metric through the public API with host buffers.  Every step copies its
+    inputs (Q, K, V, dO) host -> device from pinned memory, runs fwd + bwd, and
+    copies every result (O, LSE, dQ, dK, dV) device -> host, all inside the timed
+    region.  Steps are pipelined the way a training loop would run them: the
+    inputs of step i+1 are copied on a second stream while step i computes, and
+    step i's results are copied back on a third stream while step i+1 computes
+    (two device buffer sets, ordered with CUDA events)."""
     B, H, N, d = w.shape
-    hq, hk, hv, hdo = (x[n].contiguous().pin_memory() for n in ("q", "k", "v", "do"))
-    outs_h = [torch.empty(x["q"].shape, dtype=x["q"].dtype).pin_memory() for _ in range(4)]
-    lse_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    dq_, dk_, dv_ = (torch.empty_like(x["q"], device=dev) for _ in range(3))
-    q_, k_, v_, do_ = (torch.empty_like(x["q"], device=dev) for _ in range(4))
+    names = ("q", "k", "v", "do")
+    host_in = [{n: x[n].contiguous().pin_memory() for n in names} for _ in range(2)]
+    host_out = [[torch.empty(x["q"].shape, dtype=x["q"].dtype).pin_memory() for _ in range(4)] +
+                [torch.empty((B, H, N), dtype=torch.float32).pin_memory()] for _ in range(2)]
+    dev_in = [{n: torch.empty_like(x[n], device=dev) for n in names} for _ in range(2)]
+    dev_out = [[torch.empty_like(x["q"], device=dev) for _ in range(4)] +
+               [torch.empty((B, H, N), device=dev, dtype=torch.float32)] for _ in range(2)]
     ws_bytes = attn.attn_bwd_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16)
     wsp = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
+    s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer b are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # compute on buffer b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # results of buffer b are on the host
 
-    def one():
-        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
-            dst.copy_(src, non_blocking=True)
-        o_, l_ = attn.attn_fwd(q_, k_, v_, w.scale, block_mask=dmask, stream=stream)
-        attn.attn_bwd(q_, k_, v_, o_, do_, l_, w.scale, block_mask=dmask, dq=dq_, dk=dk_, dv=dv_, workspace=wsp,
-                      stream=stream)
-        for dst, src in zip(outs_h, (o_, dq_, dk_, dv_)):
-            dst.copy_(src, non_blocking=True)
-        lse_h.copy_(l_, non_blocking=True)
+    def h2d(b):
+        s_h2d.wait_event(ev_done[b])     # the previous compute on this buffer set has read it
+        with torch.cuda.stream(s_h2d):
+            for n in names:
+                dev_in[b][n].copy_(host_in[b][n], non_blocking=True)
+        ev_in[b].record(s_h2d)
 
-    for _ in range(max(1, args.warmup)):
-        one()
-    torch.cuda.synchronize(dev)
+    def compute(b):
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])     # the previous results of this set were copied out
+        di, do_ = dev_in[b], dev_out[b]
+        attn.attn_fwd(di["q"], di["k"], di["v"], w.scale, block_mask=dmask, out=do_[0], lse=do_[4], stream=stream)
+        attn.attn_bwd(di["q"], di["k"], di["v"], do_[0], di["do"], do_[4], w.scale, block_mask=dmask,
+                      dq=do_[1], dk=do_[2], dv=do_[3], workspace=wsp, stream=stream)
+        ev_done[b].record(stream)
+
+    def d2h(b):
+        s_d2h.wait_event(ev_done[b])
+        with torch.cuda.stream(s_d2h):
+            for hdst, dsrc in zip(host_out[b], dev_out[b]):
+                hdst.copy_(dsrc, non_blocking=True)
+        ev_out[b].record(s_d2h)
+
+    def run(nsteps):
+        for b in range(2):
+            ev_done[b].record(stream)
+            ev_out[b].record(s_d2h)
+        h2d(0)
+        for i in range(nsteps):
+            b = i & 1
+            if i + 1 < nsteps:
+                h2d(1 - b)
+            compute(b)
+            d2h(b)
+        torch.cuda.synchronize(dev)
+
+    run(max(2, args.warmup))
     if dist is not None:
         dist.barrier()
-    steps = max(1, min(args.steps, 5))
+    steps = max(2, min(args.steps, 20))
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
-    torch.cuda.synchronize(dev)
+    run(steps)
     el = (time.perf_counter() - t0) / steps
     el = _max_over_ranks(dist, el, dev)
     total = _sum_over_ranks(dist, step_flops, dev)
-    h2d = 4 * x["q"].numel() * x["q"].element_size()
-    d2h = 4 * x["q"].numel() * x["q"].element_size() + B * H * N * 4
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host_in[0].values())
+    d2h_bytes = sum(t.numel() * t.element_size() for t in host_out[0])
     return {"value": round(total / el / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(el * 1e3, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": steps,
+            "pipelining": "inputs of step i+1 copied and results of step i-1 read back while step i computes"}
 
 
 def _comparison(attn, torch, dev, stream, inputs, iomodel, peaks):
@@ -441,6 +476,40 @@ def _comparison(attn, torch, dev, stream, inputs, iomodel, peaks):
         (iomodel.materialized_extra_bytes(N, B * H, 2) + iomodel.fwd_dram_compulsory_bytes(N, d, B * H, 2))
         / (float(peaks["hbm_gbs"]) * 1e9) * 1e3, 4)
     return res
+
+
+def _decode(attn, torch, dev, stream, inputs, peaks):
+    """Decode-shaped attention (one query per head against a 32k-token K/V cache):
+    HBM-bound, so reported as bytes moved per second against the measured copy
+    bandwidth.  Bytes = K and V read once + Q read + O and LSE written."""
+    w = inputs.DECODE_WORKLOAD
+    B, H, Nq, Nk, d = w["B"], w["H"], w["Nq"], w["Nk"], w["d"]
+    g = torch.Generator(device="cpu")
+    g.manual_seed(0)
+    q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    l = torch.empty((B, H, Nq), device=dev, dtype=torch.float32)
+    wsp = torch.empty(max(16, attn.attn_decode_workspace_size(B, H, Nq, Nk, d, attn.ATTN_DTYPE_BF16)), device=dev,
+                      dtype=torch.uint8)
+    fn = lambda: attn.attn_decode(q, k, v, 1.0 / math.sqrt(d), out=o, lse=l, workspace=wsp, stream=stream)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    iters = 20
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / iters
+    nbytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2 + B * H * Nq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"{w['name']}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} bf16 (K/V cache {2 * B * H * Nk * d * 2 / 2**30:.1f} GiB > L2)",
+            "ms": round(ms, 4), "bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": float(peaks["hbm_gbs"]),
+            "frac": round(gbs / float(peaks["hbm_gbs"]), 4), "bound": "hbm"}
 
 
 # ------------------------------------------------------------------------- CPU oracle

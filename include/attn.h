@@ -205,6 +205,16 @@ ATTN_API attn_status attn_profile_query(int index, char *name, int name_capacity
                                         double *total_ms);
 ATTN_API void attn_profile_reset(void);
 
+/*
+ * attn_selftest_timeout — check of the failure path (no counterpart in the
+ * pages).  Enqueues a one-CTA kernel that waits, with the library's bounded
+ * wait, on an mbarrier nothing completes; after limit_us microseconds (1 to
+ * 10,000,000) the wait records a timeout in the device status word and the
+ * kernel exits normally.  A following attn_device_status() on the same stream
+ * returns ATTN_ERR_TIMEOUT; the CUDA context stays usable.
+ */
+ATTN_API attn_status attn_selftest_timeout(unsigned int limit_us, void *stream);
+
 /* Static description of a status code (never NULL). */
 ATTN_API const char *attn_status_string(attn_status status);
 

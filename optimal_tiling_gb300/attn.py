@@ -77,6 +77,8 @@ def load():
             lib.attn_decode.restype = _i
             lib.attn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
             lib.attn_decode_workspace_size.restype = _sz
+            lib.attn_selftest_timeout.argtypes = [ctypes.c_uint, _vp]
+            lib.attn_selftest_timeout.restype = _i
             lib.attn_device_status.argtypes = [_vp]
             lib.attn_device_status.restype = _i
             lib.attn_status_string.argtypes = [_i]
@@ -257,6 +259,11 @@ def attn_decode(q, k, v, scale: float, out=None, lse=None, workspace=None, strea
                          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(st, "attn_decode")
     return out, lse
+
+
+def attn_selftest_timeout(limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that nothing completes)."""
+    _raise(load().attn_selftest_timeout(int(limit_us), _stream(stream)), "attn_selftest_timeout")
 
 
 def attn_device_status(stream=None) -> int:

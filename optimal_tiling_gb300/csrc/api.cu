@@ -369,8 +369,21 @@ attn_status attn_decode(const void *Q, const void *K, const void *V, void *O, fl
     const attn::DecodeShape sh = attn::decode_shape(B, H, Nq, Nk, d, scale);
     if (workspace == nullptr || workspace_bytes < attn::decode_workspace_bytes(sh) || !aligned16(workspace))
         return ATTN_ERR_WORKSPACE;
-    return launch_status(attn::launch_decode_bf16(sh, Q, K, V, O, LSE, static_cast<float *>(workspace),
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    const uint64_t krows = (uint64_t)B * H * Nk;
+    attn::DecodeMaps maps;
+    if (!make_map_bf16(&maps.k, K, d, krows, 32) || !make_map_bf16(&maps.v, V, d, krows, 32)) return ATTN_ERR_CUDA;
+    return launch_status(attn::launch_decode_bf16(sh, maps, Q, O, LSE, static_cast<float *>(workspace), status,
                                                   static_cast<cudaStream_t>(stream)));
+}
+
+attn_status attn_selftest_timeout(unsigned int limit_us, void *stream) {
+    if (limit_us == 0 || limit_us > 10000000u) return ATTN_ERR_INVALID_ARG;
+    int *status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    return launch_status(
+        attn::launch_selftest_wait(status, 1000ull * limit_us, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status attn_device_status(void *stream) {

@@ -10,14 +10,18 @@
 // it runs on the CUDA cores, not the tensor cores.
 //
 // Two kernels:
-//   decode_split: the key range of each head is cut into splits (enough CTAs to
-//     fill the GPU); a CTA streams its split in groups of 32 keys per warp, each
-//     lane scoring one key against all queries (q pre-scaled by s log2 e, fp32
-//     accumulation), and keeps per query the running max m, sum l and
-//     unnormalised output u (lane t owns output columns t, t+32, ...) -- the
-//     online update of the page's section "Softmax without storing the score
-//     matrix".  The four warps' states are merged in shared memory and the
-//     CTA writes (u, m, l) of its split.
+//   decode_split: the key range of each head is cut into splits (about four
+//     waves of CTAs, one CTA per SM at a time).  A producer warp streams the
+//     split's K and V rows with TMA, 32-key step by 32-key step, into a ring of
+//     shared-memory stages per consumer warp (~190 KB in flight per SM, which is
+//     what keeps HBM busy).  Each consumer warp scores its step with one lane per
+//     key against all queries (q pre-scaled by s log2 e, fp32 accumulation) and
+//     keeps per query the running max m, sum l and unnormalised output u (lane t
+//     owns output columns [t*d/32, (t+1)*d/32)) -- the online update of the
+//     page's section "Softmax without storing the score matrix".  The 128-byte
+//     TMA swizzle makes both the per-key row reads and the per-column V reads
+//     conflict-free.  The warps' states are merged in shared memory and the CTA
+//     writes (u, m, l) of its split.
 //   decode_merge: for each (head, query) the splits are merged with the same
 //     rule (m' = max m_s, l' = sum e^{m_s - m'} l_s, u' likewise), o = u'/l',
 //     LSE = (m' + log2 l') ln 2.
@@ -35,7 +39,6 @@ using namespace ptx;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kWarps = 4;
 constexpr int kGroup = 32;  // keys per warp step (one per lane)
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -53,52 +56,114 @@ __device__ __forceinline__ size_t part_index(int head, int split, int q, int spl
     return (((size_t)head * splits + split) * nq + q) * (D + 2);
 }
 
+// Shared-memory plan of decode_split: per consumer warp a ring of NS stages, each
+// stage one 32-key step: the K rows and V rows of the step as 64-column slabs of
+// 32 rows x 128 bytes in the 128-byte-swizzled TMA layout (16-byte chunk c of row
+// r at chunk c ^ (r % 8)), then q (fp32, pre-scaled), the warps' final states and
+// the barriers.
 template <int D, int NQ>
-__global__ void __launch_bounds__(kWarps * 32)
-decode_split_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__restrict__ K,
-                    const __nv_bfloat16 *__restrict__ V, float *__restrict__ part, int Nq, int Nk, float scale,
-                    int keys_per_split, int splits) {
-    constexpr int DPL = D / 32;  // output columns per lane
-    extern __shared__ float dsm[];
-    float(*qs)[D] = reinterpret_cast<float(*)[D]>(dsm);                      // [NQ][D]
-    float(*st_u)[NQ][D] = reinterpret_cast<float(*)[NQ][D]>(dsm + NQ * D);   // [kWarps][NQ][D]
-    float(*st_m)[NQ] = reinterpret_cast<float(*)[NQ]>(dsm + (1 + kWarps) * NQ * D);
-    float(*st_l)[NQ] = reinterpret_cast<float(*)[NQ]>(dsm + (1 + kWarps) * NQ * D + kWarps * NQ);
+struct DecCfg {
+    static constexpr int kConsumers = D == 256 ? 2 : 4;              // consumer warps
+    static constexpr int kSlab = kGroup * 128;                        // 4 KB: 32 rows x 64 columns
+    static constexpr int kTile = kGroup * D * 2;                      // K (or V) rows of one step
+    static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kRest = NQ * D * 4 + kConsumers * NQ * (D + 2) * 4 + 4096;  // q, states, barriers
+    static constexpr int kRingBudget = 220 * 1024 - kRest;
+    static constexpr int kStages = kRingBudget / (kConsumers * kStageBytes) > 6 ? 6
+                                                                                : kRingBudget / (kConsumers * kStageBytes);
+    static constexpr int kRingOff = 0;
+    static constexpr int kQOff = kConsumers * kStages * kStageBytes;
+    static constexpr int kStOff = kQOff + NQ * D * 4;                 // [warps][NQ][D] u, then m, l
+    static constexpr int kBarOff = kStOff + (kConsumers * NQ * (D + 2)) * 4;
+    static constexpr int kBarBytes = 2 * kConsumers * kStages * 8;
+    static constexpr int kSmemBytes = ((kBarOff + kBarBytes + 64) + 1023) / 1024 * 1024 + 1024;
+    static constexpr int kThreads = (kConsumers + 1) * 32;            // + one producer warp
+    static_assert(kStages >= 2, "at least double buffering");
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+};
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1)
+decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __nv_bfloat16 *__restrict__ Q, float *__restrict__ part, int Nq, int Nk, float scale,
+                    int keys_per_split, int splits, int *dev_status) {
+    using C = DecCfg<D, NQ>;
+    constexpr int W = C::kConsumers, NS = C::kStages;
+    constexpr int DPL = D / 32;  // output columns per lane: lane owns [lane*DPL, lane*DPL + DPL)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float(*qs)[D] = reinterpret_cast<float(*)[D]>(sm + C::kQOff);
+    float *st = reinterpret_cast<float *>(sm + C::kStOff);
+    const uint32_t bar0 = smem_addr(sm + C::kBarOff);
+    auto full = [&](int w, int s) { return bar0 + 8u * (w * NS + s); };
+    auto empty = [&](int w, int s) { return bar0 + 8u * (W * NS + w * NS + s); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kBarOff + C::kBarBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, head = blockIdx.y;
     const float sl2 = scale * kLog2e;
+    const int k_begin = split * keys_per_split;
+    const int k_end = min(Nk, k_begin + keys_per_split);
+    const int nsteps = (k_end - k_begin + kGroup - 1) / kGroup;  // 32-key steps of this split
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int i = 0; i < W * NS; ++i) {
+            mbar_init(bar0 + 8u * i, 1);             // full: the producer's expect_tx
+            mbar_init(bar0 + 8u * (W * NS + i), 1);  // empty: lane 0 of the consumer warp
+        }
+        fence_barrier_init();
+    }
     for (int t = threadIdx.x; t < NQ * D; t += blockDim.x) {
         const int q = t / D, c = t % D;
         qs[q][c] = q < Nq ? __bfloat162float(Q[((size_t)head * Nq + q) * D + c]) * sl2 : 0.f;
     }
     __syncthreads();
 
-    float m[NQ], l[NQ], u[NQ][DPL];
+    if (warp == W) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            for (int t = 0; t < nsteps; ++t) {
+                const int w = t % W, s = (t / W) % NS, use = t / (W * NS);
+                if (use > 0 && !mbar_wait(empty(w, s), (uint32_t)(use - 1) & 1u, abort_flag, dev_status)) break;
+                const uint32_t kb = smem_addr(sm + C::kRingOff) + (uint32_t)((w * NS + s) * C::kStageBytes);
+                const int row = head * Nk + k_begin + t * kGroup;
+                mbar_arrive_expect_tx(full(w, s), C::kStageBytes);
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        m[q] = -INFINITY;
-        l[q] = 0.f;
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_2d(kb + c * C::kSlab, &tmK, c * 64, row, full(w, s));
+                    tma_load_2d(kb + C::kTile + c * C::kSlab, &tmV, c * 64, row, full(w, s));
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        float m[NQ], l[NQ], u[NQ][DPL];
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) u[q][c] = 0.f;
-    }
-    const int k_begin = split * keys_per_split;
-    const int k_end = min(Nk, k_begin + keys_per_split);
-    const __nv_bfloat16 *Kh = K + (size_t)head * Nk * D;
-    const __nv_bfloat16 *Vh = V + (size_t)head * Nk * D;
-    for (int g0 = k_begin + warp * kGroup; g0 < k_end; g0 += kWarps * kGroup) {
-        const int j = g0 + lane;
-        const bool valid = j < k_end;
-        // scores of key j against every query, 8 columns (16 bytes) at a time
-        float sc[NQ];
+        for (int q = 0; q < NQ; ++q) {
+            m[q] = -INFINITY;
+            l[q] = 0.f;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) sc[q] = 0.f;
-        if (valid) {
-            const uint4 *krow = reinterpret_cast<const uint4 *>(Kh + (size_t)j * D);
-#pragma unroll 4
+            for (int c = 0; c < DPL; ++c) u[q][c] = 0.f;
+        }
+        for (int t = warp; t < nsteps; t += W) {
+            const int s = (t / W) % NS, use = t / (W * NS);
+            bool ok = mbar_wait(full(warp, s), (uint32_t)use & 1u, abort_flag, dev_status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const uint8_t *kt = sm + C::kRingOff + (warp * NS + s) * C::kStageBytes;
+            const uint8_t *vt = kt + C::kTile;
+            const int g0 = k_begin + t * kGroup;
+            const bool valid = g0 + lane < k_end;
+            // scores: lane = key (row `lane` of the step); q columns are a broadcast
+            float sc[NQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) sc[q] = 0.f;
+#pragma unroll 2
             for (int c8 = 0; c8 < D / 8; ++c8) {
-                // every lane reads the same q columns (a shared-memory broadcast) and its own
-                // key row; the row's remaining bytes are L1 hits for the next column blocks
-                const uint4 kv = __ldg(krow + c8);
+                const int slab = c8 >> 3, chunk = c8 & 7;
+                const uint4 kv = *reinterpret_cast<const uint4 *>(kt + slab * C::kSlab + lane * 128 +
+                                                                  ((chunk ^ (lane & 7)) << 4));
                 const __nv_bfloat162 *kp = reinterpret_cast<const __nv_bfloat162 *>(&kv);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -108,42 +173,64 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__
                         sc[q] = fmaf(qs[q][c8 * 8 + 2 * e], kf.x, fmaf(qs[q][c8 * 8 + 2 * e + 1], kf.y, sc[q]));
                 }
             }
-        }
-        float pj[NQ];
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            const float s = valid ? sc[q] : -INFINITY;
-            const float m_new = fmaxf(m[q], warp_max(s));  // finite: the group has at least one valid key
-            const float alpha = ex2(m[q] - m_new);         // 0 while m was -inf
-            pj[q] = valid ? ex2(s - m_new) : 0.f;
-            l[q] = l[q] * alpha + warp_sum(pj[q]);
-#pragma unroll
-            for (int c = 0; c < DPL; ++c) u[q][c] *= alpha;
-            m[q] = m_new;
-        }
-        // u_q += sum over the group's keys of p_qj v_j (lane owns columns lane, lane+32, ...)
-        const int nvalid = min(kGroup, k_end - g0);
-        for (int jj = 0; jj < nvalid; ++jj) {
-            const __nv_bfloat16 *vrow = Vh + (size_t)(g0 + jj) * D;
-            float vv[DPL];
-#pragma unroll
-            for (int c = 0; c < DPL; ++c) vv[c] = __bfloat162float(vrow[lane + 32 * c]);
+            float pj[NQ];
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
-                const float w = __shfl_sync(0xffffffffu, pj[q], jj);
+                const float sv = valid ? sc[q] : -INFINITY;
+                const float m_new = fmaxf(m[q], warp_max(sv));  // finite: the step holds a valid key
+                const float alpha = ex2(m[q] - m_new);
+                pj[q] = valid ? ex2(sv - m_new) : 0.f;
+                l[q] = l[q] * alpha + warp_sum(pj[q]);
 #pragma unroll
-                for (int c = 0; c < DPL; ++c) u[q][c] = fmaf(w, vv[c], u[q][c]);
+                for (int c = 0; c < DPL; ++c) u[q][c] *= alpha;
+                m[q] = m_new;
             }
+            // u_q += sum_j p_qj v_j: lane reads its DPL columns of row j (2*DPL bytes)
+            const int nvalid = min(kGroup, k_end - g0);
+            const int byte0 = lane * DPL * 2;                 // byte offset of the lane's columns in a row
+            const int vslab = byte0 >> 7, vin = byte0 & 127;  // 64-column slab, offset inside its 128 B
+            for (int jj = 0; jj < nvalid; ++jj) {
+                const int pos = (((vin >> 4) ^ (jj & 7)) << 4) | (vin & 15);
+                const uint8_t *vp = vt + vslab * C::kSlab + jj * 128 + pos;
+                float vv[DPL];
+                if constexpr (DPL == 2) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(vp));
+                    vv[0] = f.x;
+                    vv[1] = f.y;
+                } else if constexpr (DPL == 4) {
+                    const uint2 r = *reinterpret_cast<const uint2 *>(vp);
+                    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+                    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+                    vv[0] = a.x; vv[1] = a.y; vv[2] = b.x; vv[3] = b.y;
+                } else {
+                    const uint4 r = *reinterpret_cast<const uint4 *>(vp);
+                    const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                        vv[2 * e] = a.x;
+                        vv[2 * e + 1] = a.y;
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const float w = __shfl_sync(0xffffffffu, pj[q], jj);
+#pragma unroll
+                    for (int c = 0; c < DPL; ++c) u[q][c] = fmaf(w, vv[c], u[q][c]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(warp, s));
         }
-    }
-    // merge the four warps' states
+        // this warp's state for the merge: u at [warp][q][D], then m, l at [W][NQ][D] + ...
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
+        for (int q = 0; q < NQ; ++q) {
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) st_u[warp][q][lane + 32 * c] = u[q][c];
-        if (lane == 0) {
-            st_m[warp][q] = m[q];
-            st_l[warp][q] = l[q];
+            for (int c = 0; c < DPL; ++c) st[((size_t)warp * NQ + q) * D + lane * DPL + c] = u[q][c];
+            if (lane == 0) {
+                st[(size_t)W * NQ * D + warp * NQ + q] = m[q];
+                st[(size_t)W * NQ * D + W * NQ + warp * NQ + q] = l[q];
+            }
         }
     }
     __syncthreads();
@@ -152,14 +239,14 @@ decode_split_kernel(const __nv_bfloat16 *__restrict__ Q, const __nv_bfloat16 *__
         if (q >= Nq) continue;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, st_m[w][q]);
+        for (int w = 0; w < W; ++w) M = fmaxf(M, st[(size_t)W * NQ * D + w * NQ + q]);
         float uu = 0.f, ll = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float a = ex2(st_m[w][q] - M);
-                uu = fmaf(a, st_u[w][q][c], uu);
-                ll = fmaf(a, st_l[w][q], ll);
+            for (int w = 0; w < W; ++w) {
+                const float a = ex2(st[(size_t)W * NQ * D + w * NQ + q] - M);
+                uu = fmaf(a, st[((size_t)w * NQ + q) * D + c], uu);
+                ll = fmaf(a, st[(size_t)W * NQ * D + W * NQ + w * NQ + q], ll);
             }
         }
         float *dst = part + part_index<D>(head, split, q, splits, Nq);
@@ -201,21 +288,20 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restri
 }
 
 template <int D, int NQ>
-cudaError_t launch_dq(const DecodeShape &sh, const void *Q, const void *K, const void *V, void *O, float *LSE,
-                      float *part, cudaStream_t st) {
+cudaError_t launch_dq(const DecodeShape &sh, const DecodeMaps &maps, const void *Q, void *O, float *LSE, float *part,
+                      int *dev_status, cudaStream_t st) {
+    using C = DecCfg<D, NQ>;
     const int heads = sh.B * sh.H;
-    const size_t smem = ((size_t)(1 + kWarps) * NQ * D + 2 * kWarps * NQ) * sizeof(float);
     auto kern = decode_split_kernel<D, NQ>;
-    cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e0 != cudaSuccess) return e0;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
     {
         ProfScope prof_("decode_split", st);
-        kern<<<dim3(sh.splits, heads), kWarps * 32, smem, st>>>(
-            static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(K),
-            static_cast<const __nv_bfloat16 *>(V), part, sh.Nq, sh.Nk, sh.scale, sh.keys_per_split, sh.splits);
+        kern<<<dim3(sh.splits, heads), C::kThreads, C::kSmemBytes, st>>>(
+            maps.k, maps.v, static_cast<const __nv_bfloat16 *>(Q), part, sh.Nq, sh.Nk, sh.scale, sh.keys_per_split,
+            sh.splits, dev_status);
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
         ProfScope prof_("decode_merge", st);
         decode_merge_kernel<D><<<(heads * sh.Nq + 3) / 4, 128, 0, st>>>(part, static_cast<__nv_bfloat16 *>(O), LSE,
@@ -225,13 +311,13 @@ cudaError_t launch_dq(const DecodeShape &sh, const void *Q, const void *K, const
 }
 
 template <int D>
-cudaError_t launch_d(const DecodeShape &sh, const void *Q, const void *K, const void *V, void *O, float *LSE,
-                     float *part, cudaStream_t st) {
-    if (sh.Nq <= 1) return launch_dq<D, 1>(sh, Q, K, V, O, LSE, part, st);
-    if (sh.Nq <= 2) return launch_dq<D, 2>(sh, Q, K, V, O, LSE, part, st);
-    if (sh.Nq <= 4) return launch_dq<D, 4>(sh, Q, K, V, O, LSE, part, st);
-    if (sh.Nq <= 8) return launch_dq<D, 8>(sh, Q, K, V, O, LSE, part, st);
-    return launch_dq<D, 16>(sh, Q, K, V, O, LSE, part, st);
+cudaError_t launch_d(const DecodeShape &sh, const DecodeMaps &m, const void *Q, void *O, float *LSE, float *part,
+                     int *dev_status, cudaStream_t st) {
+    if (sh.Nq <= 1) return launch_dq<D, 1>(sh, m, Q, O, LSE, part, dev_status, st);
+    if (sh.Nq <= 2) return launch_dq<D, 2>(sh, m, Q, O, LSE, part, dev_status, st);
+    if (sh.Nq <= 4) return launch_dq<D, 4>(sh, m, Q, O, LSE, part, dev_status, st);
+    if (sh.Nq <= 8) return launch_dq<D, 8>(sh, m, Q, O, LSE, part, dev_status, st);
+    return launch_dq<D, 16>(sh, m, Q, O, LSE, part, dev_status, st);
 }
 
 }  // namespace
@@ -239,9 +325,10 @@ cudaError_t launch_d(const DecodeShape &sh, const void *Q, const void *K, const 
 DecodeShape decode_shape(int B, int H, int Nq, int Nk, int d, float scale) {
     DecodeShape sh{B, H, Nq, Nk, d, scale, 1, Nk};
     const int heads = B * H;
-    // enough CTAs to fill the GPU four times over, each split at least one group per warp
+    // one CTA per SM at a time (a deep TMA ring each): enough splits for about four
+    // waves, each split at least one 32-key step per consumer warp
     const int want = std::max(1, (4 * 152 + heads - 1) / heads);
-    const int max_splits = std::max(1, (Nk + kWarps * kGroup - 1) / (kWarps * kGroup));
+    const int max_splits = std::max(1, (Nk + 4 * kGroup - 1) / (4 * kGroup));
     sh.splits = std::min(want, max_splits);
     const int per = (Nk + sh.splits - 1) / sh.splits;
     sh.keys_per_split = (per + kGroup - 1) / kGroup * kGroup;
@@ -253,12 +340,12 @@ size_t decode_workspace_bytes(const DecodeShape &sh) {
     return (size_t)sh.B * sh.H * sh.splits * sh.Nq * (sh.d + 2) * sizeof(float);
 }
 
-cudaError_t launch_decode_bf16(const DecodeShape &sh, const void *Q, const void *K, const void *V, void *O,
-                               float *LSE, float *part, cudaStream_t st) {
+cudaError_t launch_decode_bf16(const DecodeShape &sh, const DecodeMaps &maps, const void *Q, void *O, float *LSE,
+                               float *part, int *dev_status, cudaStream_t st) {
     switch (sh.d) {
-        case 64: return launch_d<64>(sh, Q, K, V, O, LSE, part, st);
-        case 128: return launch_d<128>(sh, Q, K, V, O, LSE, part, st);
-        case 256: return launch_d<256>(sh, Q, K, V, O, LSE, part, st);
+        case 64: return launch_d<64>(sh, maps, Q, O, LSE, part, dev_status, st);
+        case 128: return launch_d<128>(sh, maps, Q, O, LSE, part, dev_status, st);
+        case 256: return launch_d<256>(sh, maps, Q, O, LSE, part, dev_status, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -79,9 +79,15 @@ struct DecodeShape {
     float scale;
     int splits, keys_per_split;
 };
+struct DecodeMaps {
+    CUtensorMap k, v;  // [B*H*Nk, d] bf16, boxes of 32 rows x 64 columns, 128-byte swizzle
+};
 DecodeShape decode_shape(int B, int H, int Nq, int Nk, int d, float scale);
 size_t decode_workspace_bytes(const DecodeShape &sh);
-cudaError_t launch_decode_bf16(const DecodeShape &sh, const void *Q, const void *K, const void *V, void *O,
-                               float *LSE, float *part, cudaStream_t st);
+cudaError_t launch_decode_bf16(const DecodeShape &sh, const DecodeMaps &maps, const void *Q, void *O, float *LSE,
+                               float *part, int *dev_status, cudaStream_t st);
+
+// One-CTA kernel whose bounded mbarrier wait expires after limit_ns (self-test).
+cudaError_t launch_selftest_wait(int *status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace attn

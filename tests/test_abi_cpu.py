@@ -89,3 +89,22 @@ def test_materialized_argument_checks(lib):
     r = lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 256, 64, 0.1, attn.ATTN_DTYPE_F32,
                                   None, FAKE, need, None)
     assert r == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.attn_selftest_timeout(0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_timeout(10000001, None) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_decode_argument_checks(lib):
+    def dec(Nq=1, Nk=100, d=128, dt=attn.ATTN_DTYPE_BF16, ws=FAKE, wsz=1 << 30, q=FAKE):
+        return lib.attn_decode(q, FAKE, FAKE, FAKE, FAKE, 2, 3, Nq, Nk, d, 0.1, dt, ws, wsz, None)
+    assert dec(Nq=0) == attn.ATTN_ERR_INVALID_ARG
+    assert dec(Nq=17) == attn.ATTN_ERR_UNSUPPORTED
+    assert dec(d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert dec(dt=attn.ATTN_DTYPE_F32) == attn.ATTN_ERR_UNSUPPORTED
+    assert dec(q=MIS) == attn.ATTN_ERR_INVALID_ARG
+    assert dec(ws=None) == attn.ATTN_ERR_WORKSPACE
+    need = lib.attn_decode_workspace_size(2, 3, 4, 1000, 128, attn.ATTN_DTYPE_BF16)
+    assert need >= 2 * 3 * 4 * 130 * 4
+    assert dec(Nq=4, Nk=1000, wsz=need - 4) == attn.ATTN_ERR_WORKSPACE
