@@ -72,6 +72,10 @@ def _bind(lib):
                                     ctypes.c_int, _ip, _dp, _dp]
     lib.oracle_fwd_rect.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                     _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_fwd_naive_m.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, _u8p,
+                                       ctypes.c_int, ctypes.c_longlong, _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_bwd_naive_m.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, _u8p,
+                                       ctypes.c_int, ctypes.c_longlong, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
     lib.oracle_num_threads.restype = ctypes.c_int
     return lib
 
@@ -257,3 +261,44 @@ def fwd_rect(q, k, v, scale: float, _oracle=None):
     LSE = np.empty(Q.shape[:-1], dtype=np.float64)
     lib.oracle_fwd_rect(nh, Nq, Nk, d, float(scale), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE))
     return O, LSE
+
+
+def _mask_general(mask, N: int, block: int, nh: int):
+    """Block mask of side `block`: [nb, nb] shared by all heads, or [nh, nb, nb] per head."""
+    if mask is None:
+        return None, None, 0
+    m = mask.detach().cpu().numpy() if hasattr(mask, "detach") else np.asarray(mask)
+    m = np.ascontiguousarray(m.astype(np.uint8))
+    nb = (N + block - 1) // block
+    if m.shape == (nb, nb):
+        return m, m.ctypes.data_as(_u8p), 0
+    if m.shape == (nh, nb, nb):
+        return m, m.ctypes.data_as(_u8p), nb * nb
+    raise ValueError(f"mask must be [{nb},{nb}] or [{nh},{nb},{nb}], got {m.shape}")
+
+
+def fwd_naive_m(q, k, v, scale: float, mask=None, block: int = 128, _oracle=None):
+    """Forward with a general block mask: side `block`; [nb, nb] or per head [heads, nb, nb]."""
+    lib = _oracle.lib if _oracle is not None else _load()
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    _same_shape(Q, K, V)
+    nh, N, d = _heads(Q)
+    m, mp, stride = _mask_general(mask, N, block, nh)
+    O = np.empty_like(Q)
+    LSE = np.empty(Q.shape[:-1], dtype=np.float64)
+    lib.oracle_fwd_naive_m(nh, N, d, float(scale), mp, int(block), int(stride), _ptr(Q), _ptr(K), _ptr(V),
+                           _ptr(O), _ptr(LSE))
+    return O, LSE
+
+
+def bwd_naive_m(q, k, v, do, scale: float, mask=None, block: int = 128, _oracle=None):
+    """Backward with a general block mask (as fwd_naive_m).  Returns (dQ, dK, dV)."""
+    lib = _oracle.lib if _oracle is not None else _load()
+    Q, K, V, dO = _f64(q), _f64(k), _f64(v), _f64(do)
+    _same_shape(Q, K, V, dO)
+    nh, N, d = _heads(Q)
+    m, mp, stride = _mask_general(mask, N, block, nh)
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(Q), np.empty_like(Q)
+    lib.oracle_bwd_naive_m(nh, N, d, float(scale), mp, int(block), int(stride), _ptr(Q), _ptr(K), _ptr(V),
+                           _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV))
+    return dQ, dK, dV

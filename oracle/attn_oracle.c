@@ -45,6 +45,33 @@
 
 #define ORACLE_MASK_BLOCK 128
 
+/*
+ * Block mask of one head: score (i, j) is kept when mask[i/block][j/block] != 0
+ * (an nb x nb byte array, nb = ceil(N/block)).  The plain entry points use
+ * block 128 and one mask for every head; the *_m entry points take the block
+ * side and the byte distance between consecutive heads' masks (0 = shared).
+ */
+typedef struct {
+    const uint8_t *mask;  /* NULL: keep everything */
+    int block;
+    int nb;
+} mask_view;
+
+static int keep_v(const mask_view *mv, int i, int j)
+{
+    if (mv->mask == NULL) return 1;
+    return mv->mask[(size_t)(i / mv->block) * mv->nb + (j / mv->block)] != 0;
+}
+
+static mask_view head_mask(const uint8_t *mask, int block, long long head_stride, int h, int N)
+{
+    mask_view mv;
+    mv.block = block;
+    mv.nb = (N + block - 1) / block;
+    mv.mask = mask ? mask + (size_t)h * (size_t)head_stride : NULL;
+    return mv;
+}
+
 static int keep(const uint8_t *mask, int nb, int i, int j)
 {
     if (mask == NULL) return 1;
@@ -412,6 +439,117 @@ void oracle_fwd_rect(int nh, int Nq, int Nk, int d, double s,
             }
         free(srow);
     }
+}
+
+/*
+ * Forward and backward with a general block mask (block side `block`, per-head
+ * masks `head_stride` bytes apart).  Same definitions as oracle_fwd_naive and
+ * oracle_bwd_naive; only the lookup of removed scores differs.
+ */
+static double score_row_m(const double *Q, const double *K, int N, int d, double s, const mask_view *mv, int i,
+                          double *srow)
+{
+    double mx = -INFINITY;
+    for (int j = 0; j < N; ++j) {
+        if (keep_v(mv, i, j)) {
+            srow[j] = s * dot(Q + (size_t)i * d, K + (size_t)j * d, d);
+            if (srow[j] > mx) mx = srow[j];
+        } else {
+            srow[j] = -INFINITY;
+        }
+    }
+    return mx;
+}
+
+void oracle_fwd_naive_m(int nh, int N, int d, double s, const uint8_t *mask, int block, long long head_stride,
+                        const double *Q, const double *K, const double *V, double *O, double *LSE)
+{
+#pragma omp parallel
+    {
+        double *srow = (double *)malloc((size_t)N * sizeof(double));
+#pragma omp for collapse(2) schedule(dynamic, 16)
+        for (int h = 0; h < nh; ++h)
+            for (int i = 0; i < N; ++i) {
+                size_t hb = (size_t)h * N * d;
+                mask_view mv = head_mask(mask, block, head_stride, h, N);
+                double mx = score_row_m(Q + hb, K + hb, N, d, s, &mv, i, srow);
+                double L = row_lse(srow, N, mx);
+                double *o = O + hb + (size_t)i * d;
+                for (int t = 0; t < d; ++t) o[t] = 0.0;
+                LSE[(size_t)h * N + i] = L;
+                if (L == -INFINITY) continue;
+                for (int j = 0; j < N; ++j) {
+                    if (srow[j] == -INFINITY) continue;
+                    double p = exp(srow[j] - L);
+                    const double *vj = V + hb + (size_t)j * d;
+                    for (int t = 0; t < d; ++t) o[t] += p * vj[t];
+                }
+            }
+        free(srow);
+    }
+}
+
+void oracle_bwd_naive_m(int nh, int N, int d, double s, const uint8_t *mask, int block, long long head_stride,
+                        const double *Q, const double *K, const double *V, const double *dO,
+                        double *dQ, double *dK, double *dV)
+{
+    double *Dall = (double *)malloc((size_t)nh * N * sizeof(double));
+    double *Lall = (double *)malloc((size_t)nh * N * sizeof(double));
+#pragma omp parallel
+    {
+        double *prow = (double *)malloc((size_t)N * sizeof(double));
+#pragma omp for collapse(2) schedule(dynamic, 16)
+        for (int h = 0; h < nh; ++h)
+            for (int i = 0; i < N; ++i) {
+                size_t hb = (size_t)h * N * d;
+                const double *Qh = Q + hb, *Kh = K + hb, *Vh = V + hb, *dOh = dO + hb;
+                mask_view mv = head_mask(mask, block, head_stride, h, N);
+                double mx = score_row_m(Qh, Kh, N, d, s, &mv, i, prow);
+                double L = row_lse(prow, N, mx);
+                double D = 0.0;
+                double *dq = dQ + hb + (size_t)i * d;
+                for (int t = 0; t < d; ++t) dq[t] = 0.0;
+                Lall[(size_t)h * N + i] = L;
+                if (L == -INFINITY) {
+                    Dall[(size_t)h * N + i] = 0.0;
+                    continue;
+                }
+                /* D_i = sum_j P_ij dP_ij */
+                for (int j = 0; j < N; ++j) {
+                    if (prow[j] == -INFINITY) continue;
+                    D += exp(prow[j] - L) * dot(dOh + (size_t)i * d, Vh + (size_t)j * d, d);
+                }
+                Dall[(size_t)h * N + i] = D;
+                for (int j = 0; j < N; ++j) {
+                    if (prow[j] == -INFINITY) continue;
+                    double P = exp(prow[j] - L);
+                    double dS = P * (dot(dOh + (size_t)i * d, Vh + (size_t)j * d, d) - D);
+                    for (int t = 0; t < d; ++t) dq[t] += s * dS * Kh[(size_t)j * d + t];
+                }
+            }
+#pragma omp for collapse(2) schedule(dynamic, 16)
+        for (int h = 0; h < nh; ++h)
+            for (int j = 0; j < N; ++j) {
+                size_t hb = (size_t)h * N * d;
+                const double *Qh = Q + hb, *Kh = K + hb, *Vh = V + hb, *dOh = dO + hb;
+                mask_view mv = head_mask(mask, block, head_stride, h, N);
+                double *dk = dK + hb + (size_t)j * d, *dv = dV + hb + (size_t)j * d;
+                for (int t = 0; t < d; ++t) { dk[t] = 0.0; dv[t] = 0.0; }
+                for (int i = 0; i < N; ++i) {
+                    double L = Lall[(size_t)h * N + i];
+                    if (L == -INFINITY || !keep_v(&mv, i, j)) continue;
+                    double P = exp(s * dot(Qh + (size_t)i * d, Kh + (size_t)j * d, d) - L);
+                    double dS = P * (dot(dOh + (size_t)i * d, Vh + (size_t)j * d, d) - Dall[(size_t)h * N + i]);
+                    for (int t = 0; t < d; ++t) {
+                        dv[t] += P * dOh[(size_t)i * d + t];
+                        dk[t] += s * dS * Qh[(size_t)i * d + t];
+                    }
+                }
+            }
+        free(prow);
+    }
+    free(Dall);
+    free(Lall);
 }
 
 /* Number of OpenMP threads the oracle runs with (for reporting). */

@@ -37,6 +37,14 @@ def _torch_attention(Q, K, V, s, mask=None):
     return (P @ Vt).numpy(), torch.logsumexp(S, dim=-1).numpy()
 
 
+def _torch_attention_block(Q, K, V, s, mask, block):
+    Qt, Kt, Vt = (torch.tensor(x, dtype=torch.float64) for x in (Q, K, V))
+    N = Q.shape[-2]
+    keep = torch.tensor(np.kron(mask, np.ones((block, block)))[:N, :N] > 0)
+    S = (s * (Qt @ Kt.transpose(-1, -2))).masked_fill(~keep, float("-inf"))
+    return (torch.softmax(S, dim=-1) @ Vt).numpy(), torch.logsumexp(S, dim=-1).numpy()
+
+
 # --------------------------------------------------------------------------- forward
 
 @pytest.mark.parametrize("N,d", [(7, 3), (130, 16), (300, 8)])
@@ -249,6 +257,57 @@ def test_fwd_rows_matches_full(oracle_mod):
         assert np.array_equal(Or[n], O[h, i]) and Lr[n] == L[h, i]
 
 
+# --------------------------------------------------------------------------- general block masks
+
+def _kron_mask(mask, block, N):
+    return np.kron(mask, np.ones((block, block)))[:N, :N] > 0
+
+
+def test_general_mask_against_library(oracle_mod):
+    """64-granular per-head masks: forward and backward equal torch float64
+    autograd of softmax attention with the expanded element mask."""
+    N, d, s = 256, 8, 0.4
+    Q, K, V, dO = (_rand((3, N, d), 300 + i) for i in range(4))
+    r = np.random.default_rng(301)
+    masks = (r.random((3, 4, 4)) < 0.5).astype(np.uint8)
+    masks[:, np.arange(4), np.arange(4)] = 1          # every query row keeps its diagonal block
+    O, L = oracle_mod.fwd_naive_m(Q, K, V, s, masks, block=64)
+    dQ, dK, dV = oracle_mod.bwd_naive_m(Q, K, V, dO, s, masks, block=64)
+    Qt, Kt, Vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
+    keep = torch.tensor(np.stack([_kron_mask(m, 64, N) for m in masks]))
+    S = (s * Qt @ Kt.transpose(-1, -2)).masked_fill(~keep, float("-inf"))
+    Ot = torch.softmax(S, dim=-1) @ Vt
+    Ot.backward(torch.tensor(dO))
+    assert np.max(np.abs(O - Ot.detach().numpy())) < 1e-12
+    assert np.max(np.abs(L - torch.logsumexp(S, dim=-1).detach().numpy())) < 1e-12
+    for got, t in ((dQ, Qt), (dK, Kt), (dV, Vt)):
+        assert np.max(np.abs(got - t.grad.numpy())) < 1e-12
+
+
+def test_general_mask_special_cases(oracle_mod):
+    """A 64-granular refinement of a 128 mask equals the 128 mask; shared masks
+    equal per-head copies; a 64-block-diagonal mask splits into 64-row attentions."""
+    N, d = 384, 4
+    Q, K, V, dO = (_rand((2, N, d), 310 + i) for i in range(4))
+    m128 = inputs.random_block_mask(N, seed=11, p=0.5).numpy()
+    m64 = np.kron(m128, np.ones((2, 2), np.uint8))
+    O1, L1 = oracle_mod.fwd_naive(Q, K, V, 0.7, m128)
+    O2, L2 = oracle_mod.fwd_naive_m(Q, K, V, 0.7, m64, block=64)
+    O3, L3 = oracle_mod.fwd_naive_m(Q, K, V, 0.7, np.stack([m64, m64]), block=64)
+    assert np.max(np.abs(O1 - O2)) < 1e-13 and np.max(np.abs(O1 - O3)) < 1e-13
+    assert np.array_equal(np.isneginf(L1), np.isneginf(L2))
+    g1 = oracle_mod.bwd_naive(Q, K, V, dO, 0.7, m128)[:3]
+    g2 = oracle_mod.bwd_naive_m(Q, K, V, dO, 0.7, m64, block=64)
+    for a, b in zip(g1, g2):
+        assert np.max(np.abs(a - b)) < 1e-12
+    eye = np.eye(N // 64, dtype=np.uint8)
+    Ob, Lb = oracle_mod.fwd_naive_m(Q, K, V, 0.7, eye, block=64)
+    for t in range(N // 64):
+        sl = slice(64 * t, 64 * (t + 1))
+        Ot, Lt = oracle_mod.fwd_naive(Q[:, sl], K[:, sl], V[:, sl], 0.7)
+        assert np.max(np.abs(Ob[:, sl] - Ot)) < 1e-13 and np.max(np.abs(Lb[:, sl] - Lt)) < 1e-13
+
+
 # --------------------------------------------------------------------------- rectangular (decode)
 
 def test_rect_matches_library_and_square_rows(oracle_mod):
@@ -379,6 +438,9 @@ MUTATIONS = [
     ("dV takes dS instead of P",
      "dv[t] += P * doi[t];",
      "dv[t] += dS * doi[t];"),
+    ("general mask: row and column block swapped",
+     "return mv->mask[(size_t)(i / mv->block) * mv->nb + (j / mv->block)] != 0;",
+     "return mv->mask[(size_t)(j / mv->block) * mv->nb + (i / mv->block)] != 0;"),
     ("rectangular: scale dropped",
      "srow[j] = s * dot(q, Kh + (size_t)j * d, d);",
      "srow[j] = dot(q, Kh + (size_t)j * d, d);"),
@@ -404,6 +466,12 @@ def _pins_pass(oracle_mod, handle) -> bool:
     Orr, Lrr = oracle_mod.fwd_rect(Qr[None], Kr[None], Vr[None], s, _oracle=handle)
     Ort, Lrt = _torch_attention(Qr, Kr, Vr, s)
     if not (np.max(np.abs(Orr[0] - Ort)) < 1e-12 and np.max(np.abs(Lrr[0] - Lrt)) < 1e-12):
+        return False
+    mg = np.array([[1, 0, 0], [1, 1, 0], [1, 1, 1]], dtype=np.uint8)   # not symmetric
+    Om, _ = oracle_mod.fwd_naive_m(_rand((192, 4), 89), _rand((192, 4), 90), _rand((192, 4), 91), s, mg,
+                                   block=64, _oracle=handle)
+    Omr, _ = _torch_attention_block(_rand((192, 4), 89), _rand((192, 4), 90), _rand((192, 4), 91), s, mg, 64)
+    if not np.max(np.abs(Om - Omr)) < 1e-12:
         return False
     dQ, dK, dV, _, _ = oracle_mod.bwd_naive(Q, K, V, dO, s, _oracle=handle)
     Qt, Kt, Vt = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V))
