@@ -189,7 +189,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
             const int nvalid = min(kGroup, k_end - g0);
             const int byte0 = lane * DPL * 2;                 // byte offset of the lane's columns in a row
             const int vslab = byte0 >> 7, vin = byte0 & 127;  // 64-column slab, offset inside its 128 B
-            for (int jj = 0; jj < nvalid; ++jj) {
+            auto accumulate_row = [&](int jj) {
                 const int pos = (((vin >> 4) ^ (jj & 7)) << 4) | (vin & 15);
                 const uint8_t *vp = vt + vslab * C::kSlab + jj * 128 + pos;
                 float vv[DPL];
@@ -218,6 +218,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 #pragma unroll
                     for (int c = 0; c < DPL; ++c) u[q][c] = fmaf(w, vv[c], u[q][c]);
                 }
+            };
+            if (nvalid == kGroup) {
+#pragma unroll 8
+                for (int jj = 0; jj < kGroup; ++jj) accumulate_row(jj);
+            } else {
+                for (int jj = 0; jj < nvalid; ++jj) accumulate_row(jj);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(warp, s));
