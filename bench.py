@@ -311,6 +311,7 @@ def run_cuda(args):
     if not args.no_comparison and rank == 0:
         result["comparison"] = _comparison(attn, torch, dev, stream, inputs, iomodel, peaks)
         result["decode"] = _decode(attn, torch, dev, stream, inputs, peaks)
+        result["workloads"] = _workloads(attn, torch, dev, stream, inputs, iomodel, peaks)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -476,6 +477,64 @@ def _comparison(attn, torch, dev, stream, inputs, iomodel, peaks):
         (iomodel.materialized_extra_bytes(N, B * H, 2) + iomodel.fwd_dram_compulsory_bytes(N, d, B * H, 2))
         / (float(peaks["hbm_gbs"]) * 1e9) * 1e3, 4)
     return res
+
+
+def _time(fn, torch, dev, stream, iters=10):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / iters
+
+
+def _workloads(attn, torch, dev, stream, inputs, iomodel, peaks):
+    """Every named workload, device-timed: the fused forward, the backward where
+    the workload has one, the materialising forward for the d-sweep.  FLOPs count
+    kept blocks only (the block-sparse workload)."""
+    peak = float(peaks["bf16_tflops"])
+    out = {}
+    for name in ("teaching", "dsweep_d64", "dsweep_d128", "dsweep_d256", "bwd_d128", "sparse_16k"):
+        w = inputs.WORKLOADS[name]
+        B, H, N, d = w.shape
+        x, mask = inputs.workload_inputs(w, with_do="bwd" in w.passes)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        dm = mask.to(dev) if mask is not None else None
+        kept = float(mask.float().mean()) if mask is not None else 1.0
+        o = torch.empty_like(q)
+        l = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        ff = iomodel.fwd_flops(N, d, B * H) * kept
+        ms = _time(lambda: attn.attn_fwd(q, k, v, w.scale, block_mask=dm, out=o, lse=l, stream=stream), torch, dev,
+                   stream)
+        r = {"shape": [B, H, N, d], "kept_block_fraction": round(kept, 4), "fwd_ms": round(ms, 4),
+             "fwd_tflops": round(ff / ms / 1e9, 1), "fwd_frac": round(ff / ms / 1e9 / peak, 4)}
+        if "bwd" in w.passes:
+            do = x["do"].to(dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            wsp = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16), device=dev,
+                              dtype=torch.uint8)
+            bf = iomodel.bwd_flops(N, d, B * H) * kept
+            ms = _time(lambda: attn.attn_bwd(q, k, v, o, do, l, w.scale, block_mask=dm, dq=dq, dk=dk, dv=dv,
+                                             workspace=wsp, stream=stream), torch, dev, stream)
+            r.update({"bwd_ms": round(ms, 4), "bwd_tflops": round(bf / ms / 1e9, 1),
+                      "bwd_frac": round(bf / ms / 1e9 / peak, 4)})
+            del do, dq, dk, dv, wsp
+        if "mat" in w.passes:
+            wsp = torch.empty(attn.attn_fwd_materialized_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16),
+                              device=dev, dtype=torch.uint8)
+            ms = _time(lambda: attn.attn_fwd_materialized(q, k, v, w.scale, out=o, lse=l, workspace=wsp,
+                                                          stream=stream), torch, dev, stream)
+            r.update({"materialized_fwd_ms": round(ms, 4), "materialized_fwd_tflops": round(ff / ms / 1e9, 1),
+                      "materialized_extra_hbm_bytes": iomodel.materialized_extra_bytes(N, B * H, 2)})
+            del wsp
+        out[name] = r
+        del q, k, v, o, l
+        torch.cuda.empty_cache()
+    return out
 
 
 def _decode(attn, torch, dev, stream, inputs, peaks):

@@ -42,6 +42,9 @@
  *               backward d = 128; materialising forward d in {64, 128, 256};
  *               materialising backward d in {64, 128}.  Anything else returns
  *               ATTN_ERR_UNSUPPORTED.
+ *   Scale       Any finite s.  The bf16 forwards (fused and materialising)
+ *               take the row maximum of the raw products and so need s >= 0;
+ *               they return ATTN_ERR_UNSUPPORTED for s < 0.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -74,6 +77,26 @@ typedef enum {
 } attn_dtype;
 
 /*
+ * A general block mask, the generalisation of the 128 x 128 block mask that
+ * "On Fine-Grained I/O Complexity of Attention Backward Passes" (gist.science
+ * 2410.09397, Theorem 4.5, sparse attention stored by non-zero blocks) studies:
+ *   blocks       device array; for each (b, h) an nb x nb row-major byte matrix,
+ *                nb = ceil(N / block); blocks[i][j] == 0 removes every score
+ *                (q, k) with q / block == i and k / block == j.  NULL: no mask.
+ *   block        side of a block: 64 or 128 (anything else: ATTN_ERR_INVALID_ARG).
+ *   head_stride  bytes between the matrices of consecutive (b, h), index
+ *                b * H + h; 0 means one matrix shared by every head; negative
+ *                is ATTN_ERR_INVALID_ARG.
+ * The struct itself is read on the host during the call; `blocks` is read by
+ * the kernels and must stay valid until the call's work on the stream ends.
+ */
+typedef struct {
+    const uint8_t *blocks;
+    int block;
+    long long head_stride;
+} attn_block_mask;
+
+/*
  * attn_fwd — fused streaming forward.
  * In:  Q, K, V [B,H,N,d] (dtype), block_mask (nullable, see above), scale s.
  * Out: O [B,H,N,d] (dtype) = softmax(s Q K^T) V; LSE [B,H,N] fp32.
@@ -83,6 +106,17 @@ typedef enum {
 ATTN_API attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE,
                      int B, int H, int N, int d, float scale, attn_dtype dtype,
                      const uint8_t *block_mask, void *stream);
+
+/*
+ * attn_fwd_masked — attn_fwd with a general block mask (64- or 128-blocks,
+ * shared or per head); `mask` NULL, or mask->blocks NULL, means no mask.  A
+ * query row whose every score is removed gets O = 0 and LSE = -inf.  The bf16
+ * path visits a 128-key block when any mask entry covering it and the 128-row
+ * query tile is kept, and drops the removed 64-key halves inside the softmax.
+ */
+ATTN_API attn_status attn_fwd_masked(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                     int B, int H, int N, int d, float scale, attn_dtype dtype,
+                                     const attn_block_mask *mask, void *stream);
 
 /* Bytes of scratch attn_bwd needs for this shape (0 is a valid answer). */
 ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype);
@@ -103,6 +137,17 @@ ATTN_API attn_status attn_bwd(const void *Q, const void *K, const void *V, const
                      int B, int H, int N, int d, float scale, attn_dtype dtype,
                      const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
                      void *stream);
+
+/*
+ * attn_bwd_masked — attn_bwd with a general block mask (see attn_block_mask);
+ * pass the mask the forward that produced O and LSE used.  Rows and columns
+ * with no kept score get zero gradients.  workspace as attn_bwd.
+ */
+ATTN_API attn_status attn_bwd_masked(const void *Q, const void *K, const void *V, const void *O,
+                                     const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
+                                     int B, int H, int N, int d, float scale, attn_dtype dtype,
+                                     const attn_block_mask *mask, void *workspace, size_t workspace_bytes,
+                                     void *stream);
 
 /*
  * attn_bwd_static_workspace — attn_bwd for callers that cannot allocate device

@@ -34,6 +34,11 @@ _f = ctypes.c_float
 _sz = ctypes.c_size_t
 
 
+class BlockMask(ctypes.Structure):
+    """attn_block_mask: device mask pointer, block side (64 or 128), bytes between heads' masks."""
+    _fields_ = [("blocks", _vp), ("block", _i), ("head_stride", ctypes.c_longlong)]
+
+
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -58,6 +63,12 @@ def load():
             lib.attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
                                      _vp, _vp, _sz, _vp]
             lib.attn_bwd.restype = _i
+            _bm = ctypes.POINTER(BlockMask)
+            lib.attn_fwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _bm, _vp]
+            lib.attn_fwd_masked.restype = _i
+            lib.attn_bwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
+                                            _bm, _vp, _sz, _vp]
+            lib.attn_bwd_masked.restype = _i
             lib.attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i]
             lib.attn_bwd_workspace_size.restype = _sz
             lib.attn_fwd_materialized.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
@@ -151,6 +162,62 @@ def attn_fwd(q, k, v, scale: float, block_mask=None, out=None, lse=None, stream=
                       _dtype_code(q), _ptr(block_mask), _stream(stream))
     _raise(st, "attn_fwd")
     return out, lse
+
+
+def _block_mask(mask, block: int, B: int, H: int, N: int):
+    """attn_block_mask for a uint8 mask tensor: [nb, nb] shared by every head, or
+    [B*H, nb, nb] / [B, H, nb, nb] one per head (nb = ceil(N / block))."""
+    if mask is None:
+        return BlockMask(None, int(block), 0)
+    nb = (N + block - 1) // block
+    if mask.dtype != torch.uint8 or not mask.is_contiguous():
+        raise ValueError("block mask must be a contiguous uint8 tensor")
+    if tuple(mask.shape[-2:]) != (nb, nb):
+        raise ValueError(f"block mask must end in [{nb}, {nb}] for N={N}, block={block}")
+    if mask.dim() == 2:
+        stride = 0
+    elif mask.numel() == B * H * nb * nb and mask.dim() in (3, 4):
+        stride = nb * nb
+    else:
+        raise ValueError("block mask must be [nb, nb], [B*H, nb, nb] or [B, H, nb, nb]")
+    return BlockMask(ctypes.c_void_p(mask.data_ptr()), int(block), stride)
+
+
+def attn_fwd_masked(q, k, v, scale: float, mask=None, block: int = 128, out=None, lse=None, stream=None):
+    """attn_fwd with a general block mask: 64- or 128-blocks, shared or one per head."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    _check(q, k, v, out, lse, mask)
+    bm = _block_mask(mask, block, B, H, N)
+    st = lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                             _dtype_code(q), ctypes.byref(bm), _stream(stream))
+    _raise(st, "attn_fwd_masked")
+    return out, lse
+
+
+def attn_bwd_masked(q, k, v, o, do, lse, scale: float, mask=None, block: int = 128, dq=None, dk=None, dv=None,
+                    workspace=None, stream=None):
+    """attn_bwd with a general block mask (the one the forward used)."""
+    lib = load()
+    B, H, N, d = _shape(q)
+    code = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = attn_bwd_workspace_size(B, H, N, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    _check(q, k, v, o, do, lse, dq, dk, dv, workspace, mask)
+    bm = _block_mask(mask, block, B, H, N)
+    st = lib.attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                             B, H, N, d, float(scale), code, ctypes.byref(bm), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(st, "attn_bwd_masked")
+    return dq, dk, dv
 
 
 def attn_bwd(q, k, v, o, do, lse, scale: float, block_mask=None, dq=None, dk=None, dv=None,

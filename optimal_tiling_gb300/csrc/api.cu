@@ -191,8 +191,16 @@ const char *attn_status_string(attn_status s) {
     return "unknown status";
 }
 
-attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
-                     int d, float scale, attn_dtype dtype, const uint8_t *block_mask, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Block mask fields: side 64 or 128, head stride >= 0 (0: one mask for every head).
+bool mask_ok(int block, long long head_stride) { return (block == 64 || block == 128) && head_stride >= 0; }
+
+attn_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N, int d,
+                     float scale, attn_dtype dtype, const uint8_t *mask, int mblock, long long mstride,
+                     void *stream) {
     attn_status s = check_common(B, H, N, d, dtype);
     if (s != ATTN_OK) return s;
     if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
@@ -200,10 +208,10 @@ attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float
         return ATTN_ERR_INVALID_ARG;
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
-    if (dtype == ATTN_DTYPE_BF16 && !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_DTYPE_BF16 && (!bf16_fwd_shape_ok(N, d) || scale < 0.f)) return ATTN_ERR_UNSUPPORTED;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
-    attn::Problem p{B, H, N, d, scale, block_mask, status};
+    attn::Problem p{B, H, N, d, scale, mask, status, mblock, mask ? mstride : 0};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == ATTN_DTYPE_F32) {
         return launch_status(attn::launch_fwd_f32(p, static_cast<const float *>(Q), static_cast<const float *>(K),
@@ -217,6 +225,24 @@ attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float
     return launch_status(attn::launch_fwd_bf16(p, maps, O, LSE, st));
 }
 
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                     int d, float scale, attn_dtype dtype, const uint8_t *block_mask, void *stream) {
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, block_mask, 128, 0, stream);
+}
+
+attn_status attn_fwd_masked(const void *Q, const void *K, const void *V, void *O, float *LSE, int B, int H, int N,
+                            int d, float scale, attn_dtype dtype, const attn_block_mask *mask, void *stream) {
+    if (mask != nullptr && !mask_ok(mask->block, mask->head_stride)) return ATTN_ERR_INVALID_ARG;
+    if (mask == nullptr || mask->blocks == nullptr)
+        return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, nullptr, 128, 0, stream);
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, dtype, mask->blocks, mask->block, mask->head_stride,
+                    stream);
+}
+
 size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
     if (check_common(B, H, N, d, dtype) != ATTN_OK) return 0;
     const size_t rows = (size_t)B * H * N;
@@ -225,9 +251,13 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
     return bytes;
 }
 
-attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
-                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale,
-                     attn_dtype dtype, const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+}  // extern "C"
+
+namespace {
+
+attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                     void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, attn_dtype dtype,
+                     const uint8_t *mask, int mblock, long long mstride, void *workspace, size_t workspace_bytes,
                      void *stream) {
     attn_status s = check_common(B, H, N, d, dtype);
     if (s != ATTN_OK) return s;
@@ -242,7 +272,7 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O,
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
-    attn::Problem p{B, H, N, d, scale, block_mask, status};
+    attn::Problem p{B, H, N, d, scale, mask, status, mblock, mask ? mstride : 0};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t rows = (size_t)B * H * N;
     float *D = static_cast<float *>(workspace);
@@ -258,6 +288,28 @@ attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O,
         !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.dO, dO, d, rows, 64))
         return ATTN_ERR_CUDA;
     return launch_status(attn::launch_bwd_bf16(p, maps, O, dO, LSE, dQ, dK, dV, D, dQacc, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale,
+                     attn_dtype dtype, const uint8_t *block_mask, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, block_mask, 128, 0, workspace,
+                    workspace_bytes, stream);
+}
+
+attn_status attn_bwd_masked(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                            const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale,
+                            attn_dtype dtype, const attn_block_mask *mask, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    if (mask != nullptr && !mask_ok(mask->block, mask->head_stride)) return ATTN_ERR_INVALID_ARG;
+    const bool none = mask == nullptr || mask->blocks == nullptr;
+    return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, none ? nullptr : mask->blocks,
+                    none ? 128 : mask->block, none ? 0 : mask->head_stride, workspace, workspace_bytes, stream);
 }
 
 size_t attn_fwd_materialized_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
@@ -279,7 +331,7 @@ attn_status attn_fwd_materialized(const void *Q, const void *K, const void *V, v
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return ATTN_ERR_INVALID_ARG;
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_DTYPE_BF16 || !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_DTYPE_BF16 || !bf16_fwd_shape_ok(N, d) || scale < 0.f) return ATTN_ERR_UNSUPPORTED;
     const size_t need = attn_fwd_materialized_workspace_size(B, H, N, d, dtype);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     int *status = device_status_ptr();

@@ -23,7 +23,6 @@ namespace {
 constexpr int kWarps = 4;       // output rows per block
 constexpr int kChunk = 32;      // streamed rows per stage (one per lane)
 constexpr int kMaxDPL = 8;      // dimensions per lane: d <= 256
-constexpr int kMaskBlock = 128;
 
 __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -34,8 +33,10 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ bool block_kept(const uint8_t *mask, int nb, int qi, int kj) {
-    return mask == nullptr || mask[(size_t)(qi / kMaskBlock) * nb + kj / kMaskBlock] != 0;
+// Mask entry of (query qi, key kj) in one head's [nb][nb] block mask.  Every
+// 32-key chunk and every 4-row query group lies inside one block (64 or 128).
+__device__ __forceinline__ bool block_kept(const uint8_t *mask, int nb, int block, int qi, int kj) {
+    return mask == nullptr || mask[(size_t)(qi / block) * nb + kj / block] != 0;
 }
 
 // Stage rows [r0, r0+32) of X (one head, [N][d]) into S[32][ld]; rows past N are zero.
@@ -58,7 +59,8 @@ fwd_f32_kernel(Problem p, const float *__restrict__ Q, const float *__restrict__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * kWarps, i = row0 + warp;
     const size_t hb = (size_t)blockIdx.y * N * d;
-    const int nb = (N + kMaskBlock - 1) / kMaskBlock;
+    const int nb = p.mask_nb();
+    const uint8_t *hmask = p.head_mask(blockIdx.y);
 
     for (int t = threadIdx.x; t < kWarps * d; t += blockDim.x) {
         int r = row0 + t / d;
@@ -70,7 +72,7 @@ fwd_f32_kernel(Problem p, const float *__restrict__ Q, const float *__restrict__
     float m = -INFINITY, l = 0.f;
 
     for (int j0 = 0; j0 < N; j0 += kChunk) {
-        if (!block_kept(p.mask, nb, row0, j0)) continue;  // same for the whole block
+        if (!block_kept(hmask, nb, p.mask_block, row0, j0)) continue;  // same for the whole block
         __syncthreads();
         stage_rows(Ks, ld, K + hb, j0, N, d);
         stage_rows(Vs, ld, V + hb, j0, N, d);
@@ -139,7 +141,8 @@ bwd_f32_dq_kernel(Problem p, const float *__restrict__ Q, const float *__restric
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * kWarps, i = row0 + warp;
     const size_t hb = (size_t)blockIdx.y * N * d;
-    const int nb = (N + kMaskBlock - 1) / kMaskBlock;
+    const int nb = p.mask_nb();
+    const uint8_t *hmask = p.head_mask(blockIdx.y);
     for (int t = threadIdx.x; t < kWarps * d; t += blockDim.x) {
         int r = row0 + t / d;
         Qs[t] = r < N ? Q[hb + (size_t)r * d + t % d] : 0.f;
@@ -151,7 +154,7 @@ bwd_f32_dq_kernel(Problem p, const float *__restrict__ Q, const float *__restric
 #pragma unroll
     for (int r = 0; r < kMaxDPL; ++r) acc[r] = 0.f;
     for (int j0 = 0; j0 < N; j0 += kChunk) {
-        if (!block_kept(p.mask, nb, row0, j0)) continue;
+        if (!block_kept(hmask, nb, p.mask_block, row0, j0)) continue;
         __syncthreads();
         stage_rows(Ks, ld, K + hb, j0, N, d);
         stage_rows(Vs, ld, V + hb, j0, N, d);
@@ -202,7 +205,8 @@ bwd_f32_dkv_kernel(Problem p, const float *__restrict__ Q, const float *__restri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * kWarps, j = col0 + warp;
     const size_t hb = (size_t)blockIdx.y * N * d;
-    const int nb = (N + kMaskBlock - 1) / kMaskBlock;
+    const int nb = p.mask_nb();
+    const uint8_t *hmask = p.head_mask(blockIdx.y);
     for (int t = threadIdx.x; t < kWarps * d; t += blockDim.x) {
         int r = col0 + t / d;
         Ks[t] = r < N ? K[hb + (size_t)r * d + t % d] : 0.f;
@@ -212,7 +216,7 @@ bwd_f32_dkv_kernel(Problem p, const float *__restrict__ Q, const float *__restri
 #pragma unroll
     for (int r = 0; r < kMaxDPL; ++r) { ak[r] = 0.f; av[r] = 0.f; }
     for (int i0 = 0; i0 < N; i0 += kChunk) {
-        if (!block_kept(p.mask, nb, i0, col0)) continue;
+        if (!block_kept(hmask, nb, p.mask_block, i0, col0)) continue;
         __syncthreads();
         stage_rows(Qs, ld, Q + hb, i0, N, d);
         stage_rows(dOs, ld, dO + hb, i0, N, d);

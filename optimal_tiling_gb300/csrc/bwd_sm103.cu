@@ -12,7 +12,9 @@
 // Three kernels on the caller's stream:
 //   1. bwd_pre:     D = rowsum(dO o O) in fp32, and the fp32 dQ accumulator zeroed;
 //   2. bwd_main:    one CTA per 128-row K/V tile of one head, looping over the
-//                   64-row query blocks that the block mask keeps.  Five tcgen05
+//                   64-row query blocks that the block mask keeps (with 64-row
+//                   mask blocks one half of the tile's keys can be removed for a
+//                   visited query block: those keys get P = dS = 0).  Five tcgen05
 //                   products per block, all accumulating in tensor memory:
 //                     S^T  = K Q_i^T         (128 x 64, into S buffer)
 //                     dP^T = V dO_i^T        (128 x 64, into dP buffer)
@@ -143,21 +145,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvt = blockIdx.x, head = blockIdx.y;
-    const int nb = p.N / 128;                  // 128-row mask blocks
+    const int nq = p.N / BQ;                   // 64-row query blocks
     const int kv0 = head * p.N + kvt * BKV;    // first K/V row of this CTA in the [B*H*N, D] view
-    // query blocks (64 rows) kept for this key tile: both halves of each kept 128-row mask block
-    int n = 0;
-    for (int bi = 0; bi < nb; ++bi) n += (p.mask == nullptr || p.mask[(size_t)bi * nb + kvt]) ? 2 : 0;
-    auto qblock = [&](int it) -> int {  // it-th kept 64-row query block
-        if (p.mask == nullptr) return it;
-        int c = 0;
-        for (int bi = 0; bi < nb; ++bi)
-            if (p.mask[(size_t)bi * nb + kvt]) {
-                if (c + 2 > it) return 2 * bi + (it - c);
-                c += 2;
-            }
-        return 0;
+    const uint8_t *hm = p.head_mask(head);
+    const int mb = p.mask_block, mnb = p.mask_nb();
+    // query block iq is visited when a mask entry covering (its 64 rows, this tile's 128 keys) is kept
+    auto qvisited = [&](int iq) -> bool {
+        if (hm == nullptr) return true;
+        if (mb == 128) return hm[(size_t)(iq >> 1) * mnb + kvt] != 0;
+        const uint8_t *r = hm + (size_t)iq * mnb + 2 * kvt;
+        return (r[0] | r[1]) != 0;
     };
+    // the visited query block after iq (callers ask only while one remains)
+    auto next_q = [&](int iq) -> int {
+        do {
+            ++iq;
+        } while (!qvisited(iq));
+        return iq;
+    };
+    int n = 0;
+    for (int iq = 0; iq < nq; ++iq) n += qvisited(iq) ? 1 : 0;
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -203,12 +210,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tma_load_2d(sK + c * C::kKVSlab, &tmK, c * 64, kv0, bars.kv());
                 tma_load_2d(sV + c * C::kKVSlab, &tmV, c * 64, kv0, bars.kv());
             }
+            int iq = -1;
             for (int it = 0; it < n; ++it) {
                 const int s = it % kStages;
+                iq = next_q(iq);
                 if (it >= kStages &&
                     !mbar_wait(bars.qempty(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, abort_flag, p.dev_status))
                     break;
-                const int q0 = head * p.N + qblock(it) * BQ;
+                const int q0 = head * p.N + iq * BQ;
                 mbar_arrive_expect_tx(bars.qfull(s), 2 * C::kQTile + 2 * BQ * 4);
                 for (int c = 0; c < D / 64; ++c) {
                     tma_load_2d(sQ + s * C::kQTile + c * C::kQSlab, &tmQ, c * 64, q0, bars.qfull(s));
@@ -304,9 +313,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float sl2 = p.scale * kLog2e;
         const uint32_t my_ds_row = (uint32_t)tid * 128u;  // byte offset of dS^T row tid in a dS tile
         uint8_t *ds_gen = sm + C::kDsOff;
+        // 64-row mask blocks: this warp's 32 keys lie in one key half of the tile
+        const bool fine = hm != nullptr && mb == 64;
+        int iq = -1;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
             const int s = it % kStages, b = it & 1;
+            bool row_kept = true;
+            if (fine) {
+                iq = next_q(iq);
+                row_kept = hm[(size_t)iq * mnb + 2 * kvt + (warp >> 1)] != 0;
+            }
             ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             if (ok && it >= 2)
                 ok = mbar_wait(bars.dsfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status);
@@ -317,22 +334,28 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float *dvv = lse + BQ;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // two halves of 32 queries
-                uint32_t sr[32], pr[32];
-                tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
-                tmem_ld32(lane_base + C::kColDP + b * BQ + h * 32, pr);
-                tmem_wait_ld();
-                reg_fence(sr);
-                reg_fence(pr);
                 uint32_t pk[16], dk[16];
+                if (!row_kept) {
+                    // keys removed for this query block: P = dS = 0 (warp-uniform)
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int q = h * 32 + 2 * t;
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -lse[q] * kLog2e));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -lse[q + 1] * kLog2e));
-                    const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
-                    const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
-                    pk[t] = pack_bf16(p0, p1);
-                    dk[t] = pack_bf16(d0, d1);
+                    for (int t = 0; t < 16; ++t) pk[t] = dk[t] = 0u;
+                } else {
+                    uint32_t sr[32], pr[32];
+                    tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
+                    tmem_ld32(lane_base + C::kColDP + b * BQ + h * 32, pr);
+                    tmem_wait_ld();
+                    reg_fence(sr);
+                    reg_fence(pr);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int q = h * 32 + 2 * t;
+                        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -lse[q] * kLog2e));
+                        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -lse[q + 1] * kLog2e));
+                        const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
+                        const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
+                        pk[t] = pack_bf16(p0, p1);
+                        dk[t] = pack_bf16(d0, d1);
+                    }
                 }
                 // P^T over the first half of the S buffer's columns (bf16 pairs)
                 tmem_st16(lane_base + C::kColS + b * BQ + h * 16, pk);
@@ -395,8 +418,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         float *dq_gen = reinterpret_cast<float *>(sm + C::kDqOff);
         bool alive = true;
+        int iq = -1;
         for (int it = 0; it < n; ++it) {
             const int b = it & 1;
+            iq = next_q(iq);
             bool ok = alive && mbar_wait(bars.dqfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
             uint32_t r0[32], r1[32];
@@ -423,7 +448,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             named_bar_sync(1, 128);
             if (t == 0 && ok) {
-                const size_t q0 = (size_t)head * p.N + (size_t)qblock(it) * BQ;
+                const size_t q0 = (size_t)head * p.N + (size_t)iq * BQ;
                 bulk_reduce_add_f32(dQacc + q0 * D, sDq, C::kDqTile);
                 bulk_commit();
             }

@@ -21,7 +21,11 @@
 //     O is rescaled only when a row's max grows by more than 8 (a factor 256):
 //     the final division uses the same reference max, so the result is the same
 //     function and only rounding differs;
-//   * blocks removed by the 128x128 block mask are never loaded or multiplied.
+//   * key blocks whose mask entries for this query tile are all zero are never
+//     loaded or multiplied; with 64-row mask blocks a visited 128-key block can
+//     still be removed for one half of the keys or one half of the rows, and
+//     the softmax warps drop those 64-column halves (whole 32-column TMEM
+//     chunks, the same for every row of a warp) before the max and the exps.
 // Every mbarrier wait is bounded; an expired wait sets the device status word
 // and the CTA unwinds without touching the GPU's state.
 #include <cuda_bf16.h>
@@ -83,7 +87,15 @@ struct Bars {
     __device__ uint32_t drain() const { return base + 8u * (6 + 4 * stages); }
 };
 
-__device__ __forceinline__ bool kept(const uint8_t *mrow, int j) { return mrow == nullptr || mrow[j] != 0; }
+// Key block j (128 keys) is visited by query tile t when any mask entry that
+// covers the 128 x 128 square (t, j) is kept: one entry for 128-blocks, four
+// for 64-blocks.  hm is this head's [mnb][mnb] mask (nullptr: no mask).
+__device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int t, int j) {
+    if (hm == nullptr) return true;
+    if (mb == 128) return hm[(size_t)t * mnb + j] != 0;
+    const uint8_t *r0 = hm + (size_t)(2 * t) * mnb + 2 * j, *r1 = r0 + mnb;
+    return (r0[0] | r0[1] | r1[0] | r1[1]) != 0;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -101,9 +113,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, head = blockIdx.y;
     const int nb = p.N / BN;
-    const uint8_t *mrow = p.mask ? p.mask + (size_t)tile * nb : nullptr;
-    int n = 0;  // kept key blocks of this query tile
-    for (int j = 0; j < nb; ++j) n += kept(mrow, j) ? 1 : 0;
+    const uint8_t *hm = p.head_mask(head);
+    const int mb = p.mask_block, mnb = p.mask_nb();
+    int n = 0;  // key blocks this query tile visits
+    for (int j = 0; j < nb; ++j) n += visited(hm, mb, mnb, tile, j) ? 1 : 0;
     const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
 
     if (tid == 0) {
@@ -143,7 +156,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
             int it = 0;
             for (int j = 0; j < nb; ++j) {
-                if (!kept(mrow, j)) continue;
+                if (!visited(hm, mb, mnb, tile, j)) continue;
                 const int s = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 const int krow = head * p.N + j * BN;
@@ -209,8 +222,21 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float sl2 = p.scale * kLog2e;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each
+        // 64-key half of a visited block is kept or removed for the whole warp.
+        const bool fine = hm != nullptr && mb == 64;
+        const uint8_t *wmask = fine ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
+        int j = -1;  // key block of iteration it (tracked only for fine masks)
         for (int it = 0; it < n; ++it) {
             const int b = it & 1;
+            bool half_kept[2] = {true, true};
+            if (fine) {
+                do {
+                    ++j;
+                } while (!visited(hm, mb, mnb, tile, j));
+                half_kept[0] = wmask[2 * j] != 0;
+                half_kept[1] = wmask[2 * j + 1] != 0;
+            }
             ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -234,9 +260,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int t = 1; t < 16; ++t)
                     mxq[q] = fmax3(mxq[q], __uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1]));
+                if (!half_kept[q >> 1]) mxq[q] = -INFINITY;
             }
             const float mx = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]);
-            const float m_new = fmaxf(m_used, mx * sl2);
+            // a warp with nothing kept so far keeps m_used = -inf
+            const float m_new = mx == -INFINITY ? m_used : fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
             if (m_new > m_used + kRescaleThreshold) {
                 alpha = ex2(m_used - m_new);
@@ -251,6 +279,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int q = 0; q < 4; ++q) {
                 sumq[q] = f2_pack(0.f, 0.f);
                 uint32_t pk[16];
+                if (!half_kept[q >> 1]) {
+                    // removed half: P = 0, nothing added to the row sum
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) pk[t] = 0u;
+                    tmem_st16(scol + q * 16, pk);
+                    continue;
+                }
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1])),
@@ -306,7 +341,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const size_t grow = (size_t)row0 + tid;
         uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
         if (ok && n > 0) {
-            const float inv = 1.f / l;
+            // a row whose every visited score was removed (64-row masks) has l = 0:
+            // O = 0 and LSE = -inf, with the tensor-memory loads still warp-wide
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
@@ -321,7 +358,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int v = 0; v < 4; ++v)
                     orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
-            LSE[grow] = (m_used + __log2f(l)) * kLn2;
+            LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
         } else if (n == 0) {
             // every key block removed: O = 0, LSE = -inf
             for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);

@@ -33,8 +33,16 @@ class ProfScope {
 struct Problem {
     int B, H, N, d;
     float scale;
-    const uint8_t *mask;  // device, nb x nb, or nullptr
-    int *dev_status;      // device status word
+    const uint8_t *mask;         // device block mask, or nullptr
+    int *dev_status;             // device status word
+    int mask_block = 128;        // side of a mask block: 64 or 128
+    long long mask_stride = 0;   // bytes between the masks of consecutive (b, h); 0 = one mask for all
+
+    // Block mask of head `head` (index b * H + h): row-major [mask_nb()][mask_nb()] bytes.
+    __host__ __device__ const uint8_t *head_mask(int head) const {
+        return mask ? mask + (size_t)head * (size_t)mask_stride : nullptr;
+    }
+    __host__ __device__ int mask_nb() const { return (N + mask_block - 1) / mask_block; }
 };
 
 // ---- fp32 SIMT path (any N, d <= 256) -------------------------------------

@@ -108,3 +108,49 @@ def test_decode_argument_checks(lib):
     need = lib.attn_decode_workspace_size(2, 3, 4, 1000, 128, attn.ATTN_DTYPE_BF16)
     assert need >= 2 * 3 * 4 * 130 * 4
     assert dec(Nq=4, Nk=1000, wsz=need - 4) == attn.ATTN_ERR_WORKSPACE
+
+
+def test_masked_entry_point_checks(lib):
+    """attn_fwd_masked / attn_bwd_masked reject a block side other than 64 or 128
+    and a negative head stride before anything else happens."""
+    def fwd(block=64, stride=0, blocks=FAKE, mask=True):
+        bm = attn.BlockMask(blocks, block, stride)
+        return lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, 1.0, attn.ATTN_DTYPE_BF16,
+                                   ctypes.byref(bm) if mask else None, None)
+
+    def bwd(block=64, stride=0, d=128):
+        bm = attn.BlockMask(FAKE, block, stride)
+        return lib.attn_bwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, d, 0.1,
+                                   attn.ATTN_DTYPE_BF16, ctypes.byref(bm), FAKE, 1 << 30, None)
+    for blk in (0, 32, 96, 256):
+        assert fwd(block=blk) == attn.ATTN_ERR_INVALID_ARG
+        assert bwd(block=blk) == attn.ATTN_ERR_INVALID_ARG
+    assert fwd(stride=-1) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(stride=-64) == attn.ATTN_ERR_INVALID_ARG
+    assert bwd(d=64) == attn.ATTN_ERR_UNSUPPORTED
+    bm = attn.BlockMask(FAKE, 64, 0)
+    assert lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 200, 64, 1.0, attn.ATTN_DTYPE_BF16,
+                               ctypes.byref(bm), None) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_bf16_forwards_need_a_non_negative_scale(lib):
+    """The bf16 forwards take the row maximum of the raw products, which is the
+    maximum of the scaled scores only for s >= 0."""
+    assert _fwd(lib, scale=-0.5) == attn.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, -1.0, attn.ATTN_DTYPE_BF16,
+                                     None, FAKE, 1 << 40, None) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_block_mask_marshalling_shapes():
+    import torch
+    m = torch.ones((4, 4), dtype=torch.uint8)
+    assert attn._block_mask(m, 64, 2, 3, 256).head_stride == 0
+    per_head = torch.ones((2, 3, 4, 4), dtype=torch.uint8)
+    assert attn._block_mask(per_head, 64, 2, 3, 256).head_stride == 16
+    assert attn._block_mask(per_head.view(6, 4, 4), 64, 2, 3, 256).head_stride == 16
+    with pytest.raises(ValueError):
+        attn._block_mask(torch.ones((2, 2), dtype=torch.uint8), 64, 1, 1, 256)
+    with pytest.raises(ValueError):
+        attn._block_mask(torch.ones((5, 4, 4), dtype=torch.uint8), 64, 2, 3, 256)
+    with pytest.raises(ValueError):
+        attn._block_mask(m.float(), 64, 1, 1, 256)
