@@ -52,7 +52,9 @@ constexpr uint32_t kSCol0 = 0, kSCol1 = 128, kOCol = 256;
 template <int D>
 struct FwdCfg {
     static constexpr int kChunks = D / 64;                     // 64-element (128 B) swizzle atoms per row
-    static constexpr int kStages = D == 64 ? 4 : (D == 128 ? 2 : 1);
+    // K/V ring depth: as deep as the shared memory allows (block-sparse masks scatter the
+    // key blocks a tile visits, so their loads miss L2 and need the latency covered)
+    static constexpr int kStages = D == 64 ? 6 : (D == 128 ? 3 : 1);
     // exps per 8 pairs evaluated by the FMA-pipe polynomial instead of MUFU
 #ifdef ATTN_FWD_POLY_PAIRS
     static constexpr int kPolyPairs = ATTN_FWD_POLY_PAIRS;
@@ -71,6 +73,7 @@ struct FwdCfg {
     static constexpr int kSmemBytes = kMiscOff + 64 + 1024;    // + slack to align the base to 1024
     static_assert(kChunkBytes == 16384, "slab layout");
     static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
 struct Bars {
