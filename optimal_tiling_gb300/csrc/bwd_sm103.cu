@@ -41,6 +41,7 @@
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
+#include "visit_bits.cuh"
 
 namespace attn {
 namespace {
@@ -77,7 +78,10 @@ struct BwdCfg {
     // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull[2], dqfree[2], kvdone, drain[3]
     static constexpr int kNumBars = 1 + 2 * kStages + 2 * 5 + 1 + 3;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+    // visited query blocks as a bit set: up to 32 * kMaxMaskWords 64-row blocks (N <= 131072)
+    static constexpr int kMaxMaskWords = 64;
+    static constexpr int kBitsOff = kMiscOff + 64;
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
     // tensor memory columns
     static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 2 * BQ;
@@ -156,15 +160,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint8_t *r = hm + (size_t)iq * mnb + 2 * kvt;
         return (r[0] | r[1]) != 0;
     };
-    // the visited query block after iq (callers ask only while one remains)
-    auto next_q = [&](int iq) -> int {
-        do {
-            ++iq;
-        } while (!qvisited(iq));
-        return iq;
-    };
-    int n = 0;
-    for (int iq = 0; iq < nq; ++iq) n += qvisited(iq) ? 1 : 0;
+    uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
+    const int nwords = (nq + 31) >> 5;
+    const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
+    if (use_bits) build_visit_bits(vwords, nq, qvisited);
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -191,6 +190,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    const VisitBits vb{vwords, nwords};
+    int n = nq;  // query blocks this key tile visits
+    if (use_bits) {
+        n = vb.count();
+    } else if (hm != nullptr) {  // columns longer than the bit set: read the mask directly
+        n = 0;
+        for (int iq = 0; iq < nq; ++iq) n += qvisited(iq) ? 1 : 0;
+    }
+    // the visited query block after iq (callers ask only while one remains)
+    auto next_q = [&](int iq) -> int {
+        if (hm == nullptr) return iq + 1;
+        if (use_bits) return vb.next(iq);
+        do {
+            ++iq;
+        } while (!qvisited(iq));
+        return iq;
+    };
     const uint32_t tmem = *tmem_slot;
     const uint32_t sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
     const uint32_t sQ = smem_addr(sm + C::kQOff), sdO = smem_addr(sm + C::kdOOff);

@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
+#include "visit_bits.cuh"
 
 namespace attn {
 namespace {
@@ -70,7 +71,10 @@ struct FwdCfg {
     // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain
     static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;    // + slack to align the base to 1024
+    // visited key blocks as a bit set: masks with up to 32 * kMaxMaskWords blocks per row
+    static constexpr int kMaxMaskWords = 256;
+    static constexpr int kBitsOff = kMiscOff + 64;
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
     static_assert(kChunkBytes == 16384, "slab layout");
     static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -118,8 +122,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int nb = p.N / BN;
     const uint8_t *hm = p.head_mask(head);
     const int mb = p.mask_block, mnb = p.mask_nb();
-    int n = 0;  // key blocks this query tile visits
-    for (int j = 0; j < nb; ++j) n += visited(hm, mb, mnb, tile, j) ? 1 : 0;
+    uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
+    const int nwords = (nb + 31) >> 5;
+    const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
+    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
     const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
 
     if (tid == 0) {
@@ -148,6 +154,23 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+    const VisitBits vb{vwords, nwords};
+    int n = nb;  // key blocks this query tile visits
+    if (use_bits) {
+        n = vb.count();
+    } else if (hm != nullptr) {  // rows longer than the bit set: read the mask directly
+        n = 0;
+        for (int j = 0; j < nb; ++j) n += visited(hm, mb, mnb, tile, j) ? 1 : 0;
+    }
+    // the visited key block after j (callers ask only while one remains)
+    auto next_block = [&](int j) -> int {
+        if (hm == nullptr) return j + 1;
+        if (use_bits) return vb.next(j);
+        do {
+            ++j;
+        } while (!visited(hm, mb, mnb, tile, j));
+        return j;
+    };
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
@@ -157,9 +180,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tma_prefetch_desc(&tmV);
             mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
-            int it = 0;
-            for (int j = 0; j < nb; ++j) {
-                if (!visited(hm, mb, mnb, tile, j)) continue;
+            int j = -1;
+            for (int it = 0; it < n; ++it) {
+                j = next_block(j);
                 const int s = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 const int krow = head * p.N + j * BN;
@@ -171,7 +194,6 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
-                ++it;
             }
         }
     } else if (warp == kMmaWarp) {
@@ -234,9 +256,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int b = it & 1;
             bool half_kept[2] = {true, true};
             if (fine) {
-                do {
-                    ++j;
-                } while (!visited(hm, mb, mnb, tile, j));
+                j = next_block(j);
                 half_kept[0] = wmask[2 * j] != 0;
                 half_kept[1] = wmask[2 * j + 1] != 0;
             }

@@ -176,3 +176,30 @@ def test_all_removed_mask():
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
     for g in _bwd(x, 0.1, mask, 64, o, lse):
         assert np.all(g == 0)
+
+
+@pytest.mark.parametrize("N,with_bwd", [(133120, True), (131072, True), (1052672, False)])
+def test_long_mask_rows(oracle_mod, N, with_bwd):
+    """Block-diagonal masks on long rows.  The kernels keep the blocks a CTA visits as
+    a bit set in shared memory up to 131072 rows (backward) and 1048576 rows
+    (forward) and read the mask directly beyond: 133120 and 1052672 take the direct
+    path, 131072 the largest bit set.  With only the diagonal kept, every 128-row
+    block is an independent problem: sampled blocks are checked against the oracle
+    on that block alone."""
+    d, scale = 128, 1.0 / math.sqrt(128)
+    x = inputs.make_inputs(1, 1, N, d, torch.bfloat16, seed=N % 1000, with_do=with_bwd)
+    nb = N // 128
+    mask = torch.eye(nb, dtype=torch.uint8)
+    o, lse = _fwd(x, scale, mask, 128)
+    O, L = o.float().cpu().numpy()[0, 0], lse.cpu().numpy()[0, 0]
+    grads = _bwd(x, scale, mask, 128, o, lse) if with_bwd else None
+    for blk in (0, nb // 2 + 1, nb - 1):
+        sl = slice(blk * 128, (blk + 1) * 128)
+        sub = {k: v[:, :, sl] for k, v in x.items()}
+        Or, Lr = oracle_mod.fwd_naive(sub["q"], sub["k"], sub["v"], scale)
+        assert max_abs(O[sl], Or[0, 0]) <= TOL_BF16_O_ABS
+        assert lse_rel(L[sl], Lr[0, 0]) <= TOL_BF16_LSE_REL
+        if with_bwd:
+            gQ, gK, gV, _, _ = oracle_mod.bwd_naive(sub["q"], sub["k"], sub["v"], sub["do"], scale)
+            for g, r in zip(grads, (gQ, gK, gV)):
+                assert rel_l2(g[0, 0][sl], r[0, 0]) <= TOL_BF16_GRAD_RL2
