@@ -22,12 +22,16 @@
 //                     dK  += dS^T Q_i        (A = dS^T from shared memory)
 //                     dQ_i^T = K^T dS_i^T    (M = d: into the dP buffer, which the
 //                                             softmax warps have already read)
+//                   P and dS come from eight warps (thread = key; warps 0-3 take
+//                   queries 0-31 of a block, warps 4-7 queries 32-63): a clock trace
+//                   of one CTA showed the elementwise work of four warps, ~1,560
+//                   cycles per block, to be the longest stage of the loop.
 //                   The MMAs come from three warps, because one thread issues a
 //                   tcgen05.mma only every ~100 cycles while the tensor core takes
-//                   them several times faster: warp 9 issues S^T then dV (so that
+//                   them several times faster: warp 13 issues S^T then dV (so that
 //                   S^T of block i+2 follows, in one thread's issue order, the dV
-//                   that read P of block i from the same columns), warp 10 dP^T then
-//                   dK, warp 11 dQ^T.
+//                   that read P of block i from the same columns), warp 14 dP^T then
+//                   dK, warp 15 dQ^T; warps 8-11 drain dQ^T, warp 12 loads.
 //                   dQ_i^T is drained by its own warpgroup into shared memory as
 //                   [q][d] fp32 and added into the accumulator with one bulk
 //                   reduction (cp.reduce.async.bulk .add.f32).  S/dP are double
@@ -51,10 +55,10 @@ using namespace ptx;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int BKV = 128;   // key/value rows per CTA
 constexpr int BQ = 64;     // query rows per inner block
-constexpr int kThreads = 384;
-constexpr int kDqWarp0 = 4;     // warps 4-7 drain dQ
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;     // warps 9, 10, 11 issue MMAs (see the kernel comment)
+constexpr int kThreads = 512;
+constexpr int kDqWarp0 = 8;     // warps 0-7 P/dS, warps 8-11 drain dQ
+constexpr int kTmaWarp = 12;
+constexpr int kMmaWarp = 13;    // warps 13, 14, 15 issue MMAs (see the kernel comment)
 constexpr int kStages = 3;      // Q/dO/LSE/D ring depth (loads run two blocks ahead of the MMAs)
 constexpr uint32_t kTmemCols = 512;
 
@@ -174,7 +178,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bars.sfull(b), 2);    // S^T (warp 9) and dP^T (warp 10)
-            mbar_init(bars.pfull(b), 128);
+            mbar_init(bars.pfull(b), 256);
             mbar_init(bars.dsfree(b), 2);   // dK (warp 10) and dQ^T (warp 11) read dS
             mbar_init(bars.dqfull(b), 1);
             mbar_init(bars.dqfree(b), 128);
@@ -283,10 +287,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tc_fence_after();
                     const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile, dsb = sDs + b * C::kDsTile;
                     if (role == 0) {
-                        // dV += P^T dO_i : A = P^T (bf16 pairs in the S buffer), B = dO_i (d contiguous)
+                        // dV += P^T dO_i : A = P^T (bf16 pairs; queries 32h.. at S column 32h),
+                        // B = dO_i (d contiguous)
 #pragma unroll
                         for (int ks = 0; ks < BQ / 16; ++ks)
-                            mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + ks * 8,
+                            mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + (ks >> 1) * 32 + (ks & 1) * 8,
                                    smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV,
                                    (it > 0 || ks > 0) ? 1u : 0u);
                     } else {
@@ -324,10 +329,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
         }
     } else if (warp < kDqWarp0) {
-        // ------------------------------------------------------------ P / dS warps 0-3
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // ------------------------------------------------------------ P / dS warps 0-7
+        // Thread = key (tensor memory lane 32 (warp % 4) + lane); warps 0-3 take queries 0-31 of
+        // each block, warps 4-7 queries 32-63: the work is elementwise given LSE and D, so the
+        // two halves of a key row need nothing from each other.
+        const int h = warp >> 2;
+        const int key = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const float sl2 = p.scale * kLog2e;
-        const uint32_t my_ds_row = (uint32_t)tid * 128u;  // byte offset of dS^T row tid in a dS tile
+        const uint32_t my_ds_row = (uint32_t)key * 128u;  // byte offset of dS^T row `key` in a dS tile
         uint8_t *ds_gen = sm + C::kDsOff;
         // 64-row mask blocks: this warp's 32 keys lie in one key half of the tile
         const bool fine = hm != nullptr && mb == 64;
@@ -338,7 +348,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             bool row_kept = true;
             if (fine) {
                 iq = next_q(iq);
-                row_kept = hm[(size_t)iq * mnb + 2 * kvt + (warp >> 1)] != 0;
+                row_kept = hm[(size_t)iq * mnb + 2 * kvt + ((warp & 3) >> 1)] != 0;
             }
             ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             if (ok && it >= 2)
@@ -348,82 +358,71 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after();
             const float *lse = ld_f + s * 2 * BQ;  // LSE of the 64 queries, then D
             const float *dvv = lse + BQ;
+            uint32_t pk[16], dk[16];
+            if (!row_kept) {
+                // keys removed for this query block: P = dS = 0 (warp-uniform)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two halves of 32 queries
-                uint32_t pk[16], dk[16];
-                if (!row_kept) {
-                    // keys removed for this query block: P = dS = 0 (warp-uniform)
+                for (int t = 0; t < 16; ++t) pk[t] = dk[t] = 0u;
+            } else {
+                uint32_t sr[32], pr[32];
+                tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
+                tmem_ld32(lane_base + C::kColDP + b * BQ + h * 32, pr);
+                tmem_wait_ld();
+                reg_fence(sr);
+                reg_fence(pr);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) pk[t] = dk[t] = 0u;
-                } else {
-                    uint32_t sr[32], pr[32];
-                    tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
-                    tmem_ld32(lane_base + C::kColDP + b * BQ + h * 32, pr);
-                    tmem_wait_ld();
-                    reg_fence(sr);
-                    reg_fence(pr);
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int q = h * 32 + 2 * t;
-                        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -lse[q] * kLog2e));
-                        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -lse[q + 1] * kLog2e));
-                        const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
-                        const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
-                        pk[t] = pack_bf16(p0, p1);
-                        dk[t] = pack_bf16(d0, d1);
-                    }
+                for (int t = 0; t < 16; ++t) {
+                    const int q = h * 32 + 2 * t;
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -lse[q] * kLog2e));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -lse[q + 1] * kLog2e));
+                    const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
+                    const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
+                    pk[t] = pack_bf16(p0, p1);
+                    dk[t] = pack_bf16(d0, d1);
                 }
-                // P^T over the first half of the S buffer's columns (bf16 pairs)
-                tmem_st16(lane_base + C::kColS + b * BQ + h * 16, pk);
-                // dS^T row into shared memory, 128-byte swizzle: 16-byte chunk c at c ^ (row % 8)
+            }
+            // P^T as bf16 pairs over the first 16 of this half's own 32 S columns
+            tmem_st16(lane_base + C::kColS + b * BQ + h * 32, pk);
+            // dS^T row into shared memory, 128-byte swizzle: 16-byte chunk c at c ^ (row % 8)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = h * 4 + c;
-                    const uint32_t off = my_ds_row + (uint32_t)((chunk ^ (tid & 7)) * 16);
-                    *reinterpret_cast<uint4 *>(ds_gen + b * C::kDsTile + off) =
-                        make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-                }
+            for (int c = 0; c < 4; ++c) {
+                const int chunk = h * 4 + c;
+                const uint32_t off = my_ds_row + (uint32_t)((chunk ^ (key & 7)) * 16);
+                *reinterpret_cast<uint4 *>(ds_gen + b * C::kDsTile + off) =
+                    make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
             }
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bars.pfull(b));
         }
-        // ------------------------------------------------------------ dK, dV epilogue
+        // ------------------------------------------------------------ dK (warps 0-3), dV (warps 4-7)
         if (ok && n > 0) {
             ok = mbar_wait(bars.kvdone(), 0, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
         }
-        const size_t grow = (size_t)kv0 + tid;
-        uint4 *dkrow = reinterpret_cast<uint4 *>(dK + grow * D);
-        uint4 *dvrow = reinterpret_cast<uint4 *>(dV + grow * D);
+        const size_t grow = (size_t)kv0 + key;
+        uint4 *orow = reinterpret_cast<uint4 *>((h == 0 ? dK : dV) + grow * D);
+        const uint32_t acc = lane_base + (h == 0 ? C::kColDK : C::kColDV);
+        const float mul = h == 0 ? p.scale : 1.f;
         if (ok && n > 0) {
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t a[32], v[32];
-                tmem_ld32(lane_base + C::kColDK + c0, a);
-                tmem_ld32(lane_base + C::kColDV + c0, v);
+                uint32_t a[32];
+                tmem_ld32(acc + c0, a);
                 tmem_wait_ld();
                 reg_fence(a);
-                reg_fence(v);
-                uint32_t pa[16], pv[16];
+                uint32_t pa[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * p.scale, __uint_as_float(a[2 * t + 1]) * p.scale);
-                    pv[t] = pack_bf16(__uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
-                }
+                for (int t = 0; t < 16; ++t)
+                    pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * mul, __uint_as_float(a[2 * t + 1]) * mul);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    dkrow[c0 / 8 + q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
-                    dvrow[c0 / 8 + q] = make_uint4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
-                }
+                for (int q = 0; q < 4; ++q)
+                    orow[c0 / 8 + q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
             }
         } else if (n == 0) {
-            for (int q = 0; q < D / 8; ++q) {
-                dkrow[q] = make_uint4(0, 0, 0, 0);
-                dvrow[q] = make_uint4(0, 0, 0, 0);
-            }
+            for (int q = 0; q < D / 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
         }
     } else if (warp < kTmaWarp) {
         // ------------------------------------------------------------ dQ drain warps 4-7
