@@ -10,21 +10,24 @@
 // it runs on the CUDA cores, not the tensor cores.
 //
 // Two kernels:
-//   decode_split: the key range of each head is cut into splits (about four
-//     waves of CTAs, one CTA per SM at a time).  A producer warp streams the
-//     split's K and V rows with TMA, 32-key step by 32-key step, into a ring of
-//     shared-memory stages per consumer warp (~190 KB in flight per SM, which is
-//     what keeps HBM busy).  Each consumer warp scores its step with one lane per
+//   decode_split: one persistent CTA per SM.  The 32-key steps of all heads,
+//     taken in order (head by head), are cut into one contiguous equal range
+//     per CTA, so every SM streams the same number of bytes and there is no
+//     partial last wave; a range can start and end inside a head.  A producer
+//     warp streams the range's K and V rows with TMA, step by step, into a ring
+//     of shared-memory stages per consumer warp (~190 KB in flight per SM, which
+//     is what keeps HBM busy), running on across head boundaries.  Each consumer warp scores its step with one lane per
 //     key against all queries (q pre-scaled by s log2 e, fp32 accumulation) and
 //     keeps per query the running max m, sum l and unnormalised output u (lane t
 //     owns output columns [t*d/32, (t+1)*d/32)) -- the online update of the
 //     page's section "Softmax without storing the score matrix".  The 128-byte
 //     TMA swizzle makes both the per-key row reads and the per-column V reads
-//     conflict-free.  The warps' states are merged in shared memory and the CTA
-//     writes (u, m, l) of its split.
-//   decode_merge: for each (head, query) the splits are merged with the same
-//     rule (m' = max m_s, l' = sum e^{m_s - m'} l_s, u' likewise), o = u'/l',
-//     LSE = (m' + log2 l') ln 2.
+//     conflict-free.  At the end of each head segment of its range the CTA
+//     merges the warps' states in shared memory and writes (u, m, l) of the
+//     segment.
+//   decode_merge: for each (head, query) the segments of the CTAs whose ranges
+//     meet the head are merged with the same rule (m' = max m_s,
+//     l' = sum e^{m_s - m'} l_s, u' likewise), o = u'/l', LSE = (m' + log2 l') ln 2.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -41,6 +44,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kGroup = 32;  // keys per warp step (one per lane)
 
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
@@ -50,10 +57,15 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Partial state layout per (head, split, query): [u_0 .. u_{D-1}, m, l] fp32.
+// Partial state layout per (CTA, segment, query): [u_0 .. u_{D-1}, m, l] fp32.
 template <int D>
-__device__ __forceinline__ size_t part_index(int head, int split, int q, int splits, int nq) {
-    return (((size_t)head * splits + split) * nq + q) * (D + 2);
+__device__ __forceinline__ size_t part_index(int cta, int seg, int q, int max_seg, int nq) {
+    return (((size_t)cta * max_seg + seg) * nq + q) * (D + 2);
+}
+
+// First global step of CTA c when S steps are cut into C equal contiguous ranges.
+__host__ __device__ __forceinline__ long long range_begin(int c, long long S, int C) {
+    return (long long)c * S / C;
 }
 
 // Shared-memory plan of decode_split: per consumer warp a ring of NS stages, each
@@ -86,7 +98,7 @@ template <int D, int NQ>
 __global__ void __launch_bounds__(DecCfg<D, NQ>::kThreads, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __nv_bfloat16 *__restrict__ Q, float *__restrict__ part, int Nq, int Nk, float scale,
-                    int keys_per_split, int splits, int *dev_status) {
+                    int sph, long long S, int max_seg, int *dev_status) {
     using C = DecCfg<D, NQ>;
     constexpr int W = C::kConsumers, NS = C::kStages;
     constexpr int DPL = D / 32;  // output columns per lane: lane owns [lane*DPL, lane*DPL + DPL)
@@ -99,11 +111,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     auto empty = [&](int w, int s) { return bar0 + 8u * (W * NS + w * NS + s); };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kBarOff + C::kBarBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, head = blockIdx.y;
+    const int cta = blockIdx.x;
     const float sl2 = scale * kLog2e;
-    const int k_begin = split * keys_per_split;
-    const int k_end = min(Nk, k_begin + keys_per_split);
-    const int nsteps = (k_end - k_begin + kGroup - 1) / kGroup;  // 32-key steps of this split
+    const long long sb = range_begin(cta, S, gridDim.x), se = range_begin(cta + 1, S, gridDim.x);
+    const int nloc = (int)(se - sb);             // steps of this CTA's range
+    const int first_head = (int)(sb / sph);
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -113,10 +125,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         }
         fence_barrier_init();
     }
-    for (int t = threadIdx.x; t < NQ * D; t += blockDim.x) {
-        const int q = t / D, c = t % D;
-        qs[q][c] = q < Nq ? __bfloat162float(Q[((size_t)head * Nq + q) * D + c]) * sl2 : 0.f;
-    }
     __syncthreads();
 
     if (warp == W) {
@@ -124,11 +132,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            for (int t = 0; t < nsteps; ++t) {
+            for (int t = 0; t < nloc; ++t) {
                 const int w = t % W, s = (t / W) % NS, use = t / (W * NS);
                 if (use > 0 && !mbar_wait(empty(w, s), (uint32_t)(use - 1) & 1u, abort_flag, dev_status)) break;
                 const uint32_t kb = smem_addr(sm + C::kRingOff) + (uint32_t)((w * NS + s) * C::kStageBytes);
-                const int row = head * Nk + k_begin + t * kGroup;
+                const long long g = sb + t;
+                // rows past this head's keys (a ragged last step) belong to the next head or lie
+                // past the tensor (zero fill); the consumers give them no weight
+                const int row = (int)(g / sph) * Nk + (int)(g % sph) * kGroup;
                 mbar_arrive_expect_tx(full(w, s), C::kStageBytes);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
@@ -137,8 +148,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 }
             }
         }
-    } else {
-        // ------------------------------------------------------------ consumers
+        return;  // the consumers' named barriers do not include this warp
+    }
+    // ---------------------------------------------------------------- consumers
+    // Every consumer thread runs the same sequence of named barriers (the head segments of
+    // the range are fixed); after a failed wait the work is skipped but the barriers kept.
+    bool alive = true;
+    int t = warp;  // next local step of this warp
+    for (long long g0 = sb; g0 < se;) {
+        const int head = (int)(g0 / sph);
+        const long long g1 = min(se, (long long)(head + 1) * sph);
+        for (int i = threadIdx.x; i < NQ * D; i += W * 32) {
+            const int q = i / D, c = i % D;
+            qs[q][c] = q < Nq ? __bfloat162float(Q[((size_t)head * Nq + q) * D + c]) * sl2 : 0.f;
+        }
+        named_bar_sync(1, W * 32);
         float m[NQ], l[NQ], u[NQ][DPL];
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
@@ -147,14 +171,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 #pragma unroll
             for (int c = 0; c < DPL; ++c) u[q][c] = 0.f;
         }
-        for (int t = warp; t < nsteps; t += W) {
+        for (; sb + t < g1; t += W) {
             const int s = (t / W) % NS, use = t / (W * NS);
-            bool ok = mbar_wait(full(warp, s), (uint32_t)use & 1u, abort_flag, dev_status);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            bool ok = alive && mbar_wait(full(warp, s), (uint32_t)use & 1u, abort_flag, dev_status);
+            alive = __all_sync(0xffffffffu, ok);
+            if (!alive) continue;
             const uint8_t *kt = sm + C::kRingOff + (warp * NS + s) * C::kStageBytes;
             const uint8_t *vt = kt + C::kTile;
-            const int g0 = k_begin + t * kGroup;
-            const bool valid = g0 + lane < k_end;
+            const int key0 = (int)((sb + t) % sph) * kGroup;  // first key of the step within the head
+            const bool valid = key0 + lane < Nk;
             // scores: lane = key (row `lane` of the step); q columns are a broadcast
             float sc[NQ];
 #pragma unroll
@@ -186,7 +211,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 m[q] = m_new;
             }
             // u_q += sum_j p_qj v_j: lane reads its DPL columns of row j (2*DPL bytes)
-            const int nvalid = min(kGroup, k_end - g0);
+            const int nvalid = min(kGroup, Nk - key0);
             const int byte0 = lane * DPL * 2;                 // byte offset of the lane's columns in a row
             const int vslab = byte0 >> 7, vin = byte0 & 127;  // 64-column slab, offset inside its 128 B
             auto accumulate_row = [&](int jj) {
@@ -238,58 +263,75 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
                 st[(size_t)W * NQ * D + W * NQ + warp * NQ + q] = l[q];
             }
         }
-    }
-    __syncthreads();
-    for (int t = threadIdx.x; t < NQ * D; t += blockDim.x) {
-        const int q = t / D, c = t % D;
-        if (q >= Nq) continue;
-        float M = -INFINITY;
+        named_bar_sync(1, W * 32);
+        const int seg = head - first_head;
+        for (int i = threadIdx.x; i < NQ * D; i += W * 32) {
+            const int q = i / D, c = i % D;
+            if (q >= Nq) continue;
+            float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < W; ++w) M = fmaxf(M, st[(size_t)W * NQ * D + w * NQ + q]);
-        float uu = 0.f, ll = 0.f;
-        if (M != -INFINITY) {
+            for (int w = 0; w < W; ++w) M = fmaxf(M, st[(size_t)W * NQ * D + w * NQ + q]);
+            float uu = 0.f, ll = 0.f;
+            if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < W; ++w) {
-                const float a = ex2(st[(size_t)W * NQ * D + w * NQ + q] - M);
-                uu = fmaf(a, st[((size_t)w * NQ + q) * D + c], uu);
-                ll = fmaf(a, st[(size_t)W * NQ * D + W * NQ + w * NQ + q], ll);
+                for (int w = 0; w < W; ++w) {
+                    const float a = ex2(st[(size_t)W * NQ * D + w * NQ + q] - M);
+                    uu = fmaf(a, st[((size_t)w * NQ + q) * D + c], uu);
+                    ll = fmaf(a, st[(size_t)W * NQ * D + W * NQ + w * NQ + q], ll);
+                }
+            }
+            float *dst = part + part_index<D>(cta, seg, q, max_seg, Nq);
+            dst[c] = uu;
+            if (c == 0) {
+                dst[D] = M;
+                dst[D + 1] = ll;
             }
         }
-        float *dst = part + part_index<D>(head, split, q, splits, Nq);
-        dst[c] = uu;
-        if (c == 0) {
-            dst[D] = M;
-            dst[D + 1] = ll;
-        }
+        named_bar_sync(1, W * 32);  // qs and st are rewritten by the next segment
+        g0 = g1;
     }
 }
 
-// One warp per (head, query): merge the splits, normalise, store O (bf16) and LSE.
+// One warp per (head, query): merge the segments of the CTAs whose step ranges meet
+// the head, normalise, store O (bf16) and LSE.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const float *__restrict__ part,
                                                            __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE,
-                                                           int heads, int Nq, int splits) {
+                                                           int heads, int Nq, int sph, long long S, int ctas,
+                                                           int max_seg) {
     constexpr int DPL = D / 32;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= heads * Nq) return;
     const int head = gw / Nq, q = gw % Nq;
+    // CTAs holding the head's first and last steps
+    auto owner = [&](long long g) {
+        int c = (int)(g * ctas / S);
+        while (c + 1 < ctas && range_begin(c + 1, S, ctas) <= g) ++c;
+        while (c > 0 && range_begin(c, S, ctas) > g) --c;
+        return c;
+    };
+    const int c_lo = owner((long long)head * sph), c_hi = owner((long long)(head + 1) * sph - 1);
+    auto src_of = [&](int c) {
+        const int seg = head - (int)(range_begin(c, S, ctas) / sph);
+        return part + part_index<D>(c, seg, q, max_seg, Nq);
+    };
     float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, part[part_index<D>(head, s, q, splits, Nq) + D]);
+    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, src_of(c)[D]);
     float uu[DPL], L = 0.f;
 #pragma unroll
     for (int c = 0; c < DPL; ++c) uu[c] = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float *src = part + part_index<D>(head, s, q, splits, Nq);
-        const float a = ex2(src[D] - M);  // 0 for an empty split (m = -inf)
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const float *src = src_of(c);
+        const float a = ex2(src[D] - M);
         L = fmaf(a, src[D + 1], L);
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) uu[c] = fmaf(a, src[lane + 32 * c], uu[c]);
+        for (int k = 0; k < DPL; ++k) uu[k] = fmaf(a, src[lane + 32 * k], uu[k]);
     }
     const float inv = 1.f / L;
     __nv_bfloat16 *orow = O + ((size_t)head * Nq + q) * D;
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) orow[lane + 32 * c] = __float2bfloat16_rn(uu[c] * inv);
+    for (int k = 0; k < DPL; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(uu[k] * inv);
     if (lane == 0) LSE[(size_t)head * Nq + q] = (M + __log2f(L)) * kLn2;
 }
 
@@ -303,15 +345,15 @@ cudaError_t launch_dq(const DecodeShape &sh, const DecodeMaps &maps, const void 
     if (e != cudaSuccess) return e;
     {
         ProfScope prof_("decode_split", st);
-        kern<<<dim3(sh.splits, heads), C::kThreads, C::kSmemBytes, st>>>(
-            maps.k, maps.v, static_cast<const __nv_bfloat16 *>(Q), part, sh.Nq, sh.Nk, sh.scale, sh.keys_per_split,
-            sh.splits, dev_status);
+        kern<<<sh.ctas, C::kThreads, C::kSmemBytes, st>>>(maps.k, maps.v, static_cast<const __nv_bfloat16 *>(Q),
+                                                         part, sh.Nq, sh.Nk, sh.scale, sh.sph, sh.steps, sh.max_seg,
+                                                         dev_status);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
         ProfScope prof_("decode_merge", st);
-        decode_merge_kernel<D><<<(heads * sh.Nq + 3) / 4, 128, 0, st>>>(part, static_cast<__nv_bfloat16 *>(O), LSE,
-                                                                      heads, sh.Nq, sh.splits);
+        decode_merge_kernel<D><<<(heads * sh.Nq + 3) / 4, 128, 0, st>>>(
+            part, static_cast<__nv_bfloat16 *>(O), LSE, heads, sh.Nq, sh.sph, sh.steps, sh.ctas, sh.max_seg);
     }
     return cudaGetLastError();
 }
@@ -329,21 +371,31 @@ cudaError_t launch_d(const DecodeShape &sh, const DecodeMaps &m, const void *Q, 
 }  // namespace
 
 DecodeShape decode_shape(int B, int H, int Nq, int Nk, int d, float scale) {
-    DecodeShape sh{B, H, Nq, Nk, d, scale, 1, Nk};
-    const int heads = B * H;
-    // one CTA per SM at a time (a deep TMA ring each): enough splits for about four
-    // waves, each split at least one 32-key step per consumer warp
-    const int want = std::max(1, (4 * 152 + heads - 1) / heads);
-    const int max_splits = std::max(1, (Nk + 4 * kGroup - 1) / (4 * kGroup));
-    sh.splits = std::min(want, max_splits);
-    const int per = (Nk + sh.splits - 1) / sh.splits;
-    sh.keys_per_split = (per + kGroup - 1) / kGroup * kGroup;
-    sh.splits = (Nk + sh.keys_per_split - 1) / sh.keys_per_split;
+    DecodeShape sh{};
+    sh.B = B;
+    sh.H = H;
+    sh.Nq = Nq;
+    sh.Nk = Nk;
+    sh.d = d;
+    sh.scale = scale;
+    // one persistent CTA per SM of the current device (152 when it cannot be asked)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        sms = 152;
+    }
+    sh.sph = (Nk + kGroup - 1) / kGroup;
+    sh.steps = (long long)B * H * sh.sph;
+    sh.ctas = (int)std::min<long long>(sms, sh.steps);
+    // a range of ceil(steps / ctas) steps meets at most this many heads
+    const long long per = (sh.steps + sh.ctas - 1) / sh.ctas;
+    sh.max_seg = (int)((per + sh.sph - 1) / sh.sph) + 1;
     return sh;
 }
 
 size_t decode_workspace_bytes(const DecodeShape &sh) {
-    return (size_t)sh.B * sh.H * sh.splits * sh.Nq * (sh.d + 2) * sizeof(float);
+    return (size_t)sh.ctas * sh.max_seg * sh.Nq * (sh.d + 2) * sizeof(float);
 }
 
 cudaError_t launch_decode_bf16(const DecodeShape &sh, const DecodeMaps &maps, const void *Q, void *O, float *LSE,

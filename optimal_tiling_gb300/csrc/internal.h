@@ -81,11 +81,15 @@ struct MatBwdMaps {
 cudaError_t launch_bwd_materialized_bf16(const Problem &p, const MatBwdMaps &maps, const void *O, const void *dO,
                                          const float *LSE, float *Dv, void *dQ, void *dK, void *dV, cudaStream_t st);
 
-// Decode-shaped attention (Nq <= 16 queries against Nk keys, split over keys).
+// Decode-shaped attention (Nq <= 16 queries against Nk keys): the 32-key steps of all
+// heads cut into one equal contiguous range per CTA (one CTA per SM).
 struct DecodeShape {
     int B, H, Nq, Nk, d;
     float scale;
-    int splits, keys_per_split;
+    int sph;          // 32-key steps per head
+    long long steps;  // steps of all heads
+    int ctas;         // CTAs (ranges)
+    int max_seg;      // most head segments one range can meet
 };
 struct DecodeMaps {
     CUtensorMap k, v;  // [B*H*Nk, d] bf16, boxes of 32 rows x 64 columns, 128-byte swizzle
