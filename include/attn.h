@@ -208,7 +208,9 @@ ATTN_API attn_status attn_bwd_materialized(const void *Q, const void *K, const v
                                            const uint8_t *block_mask, void *workspace,
                                            size_t workspace_bytes, void *stream);
 
-/* Bytes of scratch attn_decode needs (per-split partial states). */
+/* Bytes of scratch attn_decode needs (partial states per head segment).  The
+ * size depends on the current device's SM count: query it with the device that
+ * will run attn_decode current. */
 ATTN_API size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d, attn_dtype dtype);
 
 /*
@@ -216,9 +218,10 @@ ATTN_API size_t attn_decode_workspace_size(int B, int H, int Nq, int Nk, int d, 
  * Nk keys, O = softmax(s Q K^T) V and LSE, no mask.  "The I/O Complexity of
  * Attention" exposition notes that single-token decoding (query length one)
  * needs a rectangular account rather than the N^2 formula: here every K/V
- * element is read from HBM once and the pass is bandwidth-bound.  The key range
- * is split across CTAs and the partial states (running max, sum, output) are
- * merged with the online-softmax rescale rule.
+ * element is read from HBM once and the pass is bandwidth-bound.  The 32-key
+ * steps of all heads are cut into one equal range per SM; the partial states
+ * (running max, sum, output) of each head segment are merged with the
+ * online-softmax rescale rule.
  * Layout: Q, O [B][H][Nq][d]; K, V [B][H][Nk][d]; LSE [B][H][Nq] fp32.
  * bf16 only; 1 <= Nq <= 16, Nk >= 1, d in {64, 128, 256}.
  * workspace: at least attn_decode_workspace_size() bytes, 16-byte aligned.
