@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
+#include "visit_bits.cuh"
 
 namespace attn {
 namespace gemm {
@@ -38,7 +39,10 @@ struct Cfg {
     static constexpr int kBarOff = kBOff + kStages * kBTile;
     static constexpr int kNumBars = 2 * kStages + 2;  // full[S], empty[S], done, drain
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 64 + 1024;
+    // kept blocks of the CTA's row (or column) of the mask as a bit set, up to 32 * kMaxMaskWords
+    static constexpr int kMaxMaskWords = 256;
+    static constexpr int kBitsOff = kMiscOff + 64;
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;
     static constexpr uint32_t kTmemCols = D < 32 ? 32 : D;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
@@ -68,8 +72,10 @@ block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = blockIdx.x, head = blockIdx.y;
     const int nb = p.N / BT;
-    int n = 0;
-    for (int k = 0; k < nb; ++k) n += kept_block(p.mask, nb, t, k, kTransA) ? 1 : 0;
+    uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
+    const int nwords = (nb + 31) >> 5;
+    const bool use_bits = p.mask != nullptr && nwords <= C::kMaxMaskWords;
+    if (use_bits) build_visit_bits(vwords, nb, [&](int k) { return kept_block(p.mask, nb, t, k, kTransA); });
     const int hrow = head * p.N;
     if (tid == 0) {
         *abort_flag = 0;
@@ -90,11 +96,27 @@ block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sA = smem_addr(sm + C::kAOff), sB = smem_addr(sm + C::kBOff);
+    const VisitBits vb{vwords, nwords};
+    int n = nb;  // kept blocks
+    if (use_bits) {
+        n = vb.count();
+    } else if (p.mask != nullptr) {  // rows longer than the bit set: read the mask directly
+        n = 0;
+        for (int k = 0; k < nb; ++k) n += kept_block(p.mask, nb, t, k, kTransA) ? 1 : 0;
+    }
+    auto next_block = [&](int k) -> int {
+        if (p.mask == nullptr) return k + 1;
+        if (use_bits) return vb.next(k);
+        do {
+            ++k;
+        } while (!kept_block(p.mask, nb, t, k, kTransA));
+        return k;
+    };
     if (warp == 4) {
         if (lane == 0 && n > 0) {
-            int it = 0;
-            for (int k = 0; k < nb; ++k) {
-                if (!kept_block(p.mask, nb, t, k, kTransA)) continue;
+            int k = -1;
+            for (int it = 0; it < n; ++it) {
+                k = next_block(k);
                 const int s = it % S;
                 if (it >= S && !mbar_wait(empty(s), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, p.dev_status)) break;
                 mbar_arrive_expect_tx(full(s), C::kATile + C::kBTile);
@@ -105,7 +127,6 @@ block_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 tma_load_2d(sA + s * C::kATile + C::kSlab, &tmA, ax + 64, ay, full(s));
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_2d(sB + s * C::kBTile + c * C::kSlab, &tmB, c * 64, hrow + k * BT, full(s));
-                ++it;
             }
         }
     } else if (warp == 5) {
