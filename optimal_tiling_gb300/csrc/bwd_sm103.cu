@@ -167,7 +167,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
     const int nwords = (nq + 31) >> 5;
     const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
-    if (use_bits) build_visit_bits(vwords, nq, qvisited);
+    const uint32_t sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -186,7 +186,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bars.kvdone(), 2);        // dV and dK complete
         for (int r = 0; r < 3; ++r) mbar_init(bars.drain(r), 1);
         fence_barrier_init();
+        // the K/V tile is needed whatever the mask says: start its load before the mask is read
+        mbar_arrive_expect_tx(bars.kv(), 2 * C::kKVTile);
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_2d(sK + c * C::kKVSlab, &tmK, c * 64, kv0, bars.kv());
+            tma_load_2d(sV + c * C::kKVSlab, &tmV, c * 64, kv0, bars.kv());
+        }
     }
+    if (use_bits) build_visit_bits(vwords, nq, qvisited);
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -212,7 +219,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         return iq;
     };
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
     const uint32_t sQ = smem_addr(sm + C::kQOff), sdO = smem_addr(sm + C::kdOOff);
     const uint32_t sDs = smem_addr(sm + C::kDsOff), sDq = smem_addr(sm + C::kDqOff);
     const uint32_t sLd = smem_addr(sm + C::kLdOff);
@@ -220,16 +226,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmdO);
-            mbar_arrive_expect_tx(bars.kv(), 2 * C::kKVTile);
-            for (int c = 0; c < D / 64; ++c) {
-                tma_load_2d(sK + c * C::kKVSlab, &tmK, c * 64, kv0, bars.kv());
-                tma_load_2d(sV + c * C::kKVSlab, &tmV, c * 64, kv0, bars.kv());
-            }
             int iq = -1;
             for (int it = 0; it < n; ++it) {
                 const int s = it % kStages;
@@ -472,6 +471,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (t == 0) bulk_wait_all();
     }
 
+    // a tile that visits no query block still received its K/V tile: let that copy land first
+    if (n == 0 && tid == 0) mbar_wait(bars.kv(), 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {

@@ -125,8 +125,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
     const int nwords = (nb + 31) >> 5;
     const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
-    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
     const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -144,7 +144,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bars.odone(), 1);
         mbar_init(bars.drain(), 1);
         fence_barrier_init();
+        // the Q tile is needed whatever the mask says: start its load before the mask is read
+        mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
     }
+    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -153,7 +157,6 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
     const VisitBits vb{vwords, nwords};
     int n = nb;  // key blocks this query tile visits
     if (use_bits) {
@@ -175,11 +178,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
-            tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
             int j = -1;
             for (int it = 0; it < n; ++it) {
                 j = next_block(j);
@@ -389,6 +389,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     }
 
+    // a tile that visits no key block still received its Q tile: let that copy land first
+    if (n == 0 && tid == 0) mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
