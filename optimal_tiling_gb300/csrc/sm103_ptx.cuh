@@ -199,8 +199,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // ---------------------------------------------------------------- tcgen05
 // Descriptor of a 128B-swizzled shared-memory operand (see the file comment).
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    // Shared-memory addresses of a CTA are below 2^18, so start >> 4 fits the 14-bit field
+    // without a mask; leaving the mask out lets the compiler turn the descriptors of
+    // consecutive k-steps into one base plus constant offsets (fewer instructions in the
+    // single thread that issues the MMAs).
     uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);                 // bits 0-13: start >> 4
+    d |= static_cast<uint64_t>(saddr >> 4);                              // bits 0-13: start >> 4
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;        // bits 16-29: leading byte offset >> 4
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;        // bits 32-45: stride byte offset >> 4
     d |= static_cast<uint64_t>(1) << 46;                                 // bits 46-48: fixed 0b001
