@@ -15,8 +15,9 @@
 //     per CTA, so every SM streams the same number of bytes and there is no
 //     partial last wave; a range can start and end inside a head.  A producer
 //     warp streams the range's K and V rows with TMA, step by step, into a ring
-//     of shared-memory stages per consumer warp (~190 KB in flight per SM, which
-//     is what keeps HBM busy), running on across head boundaries.  Each consumer warp scores its step with one lane per
+//     of shared-memory stages per consumer warp (~190 KB in flight per SM),
+//     running on across head boundaries; six consumer warps (three at d = 256)
+//     keep up with HBM.  Each consumer warp scores its step with one lane per
 //     key against all queries (q pre-scaled by s log2 e, fp32 accumulation) and
 //     keeps per query the running max m, sum l and unnormalised output u (lane t
 //     owns output columns [t*d/32, (t+1)*d/32)) -- the online update of the
@@ -75,7 +76,12 @@ __host__ __device__ __forceinline__ long long range_begin(int c, long long S, in
 // the barriers.
 template <int D, int NQ>
 struct DecCfg {
-    static constexpr int kConsumers = D == 256 ? 2 : 4;              // consumer warps
+    // consumer warps: as many as leave two ring stages each.  Measured on the 8 x 32 x 32768
+    // workload: the per-step scoring and V accumulation of a warp, not the bytes in flight,
+    // set the pace (4 -> 6 warps at d = 128: 0.749 -> 0.632 ms; 2 -> 3 at d = 256:
+    // 1.149 -> 0.765 ms).  More queries per step need the registers and shared memory of
+    // the narrower configuration.
+    static constexpr int kConsumers = NQ > 4 ? (D == 256 ? 2 : 4) : (D == 256 ? 3 : 6);
     static constexpr int kSlab = kGroup * 128;                        // 4 KB: 32 rows x 64 columns
     static constexpr int kTile = kGroup * D * 2;                      // K (or V) rows of one step
     static constexpr int kStageBytes = 2 * kTile;
