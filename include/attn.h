@@ -40,8 +40,8 @@
  *   Shapes      fp32: any N >= 1, 1 <= d <= 256 (SIMT kernels).
  *               bf16: N a multiple of 128; forward d in {64, 128, 256};
  *               backward d = 128; materialising forward d in {64, 128, 256};
- *               materialising backward d in {64, 128}.  Anything else returns
- *               ATTN_ERR_UNSUPPORTED.
+ *               materialising backward d in {64, 128}.  All: B * H <= 65535
+ *               and B * H * N <= 2^31.  Anything else returns ATTN_ERR_UNSUPPORTED.
  *   Scale       Any finite s.  The bf16 forwards (fused and materialising)
  *               take the row maximum of the raw products and so need s >= 0;
  *               they return ATTN_ERR_UNSUPPORTED for s < 0.

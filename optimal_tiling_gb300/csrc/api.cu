@@ -77,6 +77,8 @@ attn_status check_common(int B, int H, int N, int d, attn_dtype dt) {
     if (dt != ATTN_DTYPE_F32 && dt != ATTN_DTYPE_BF16) return ATTN_ERR_INVALID_ARG;
     // every index fits in 32-bit rows for the tensor maps and in size_t for offsets
     if ((uint64_t)B * H * N > (1ull << 31)) return ATTN_ERR_UNSUPPORTED;
+    // the kernels give each (b, h) its own grid row (gridDim.y <= 65535)
+    if ((uint64_t)B * H > 65535) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 

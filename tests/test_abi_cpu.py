@@ -63,6 +63,9 @@ def test_forward_argument_checks(lib):
     assert _fwd(lib, N=200) == attn.ATTN_ERR_UNSUPPORTED          # bf16 needs N % 128 == 0
     assert _fwd(lib, d=96) == attn.ATTN_ERR_UNSUPPORTED           # bf16 d in {64,128,256}
     assert _fwd(lib, d=300, dt=attn.ATTN_DTYPE_F32) == attn.ATTN_ERR_UNSUPPORTED
+    # more (b, h) pairs than a grid dimension holds: refused before any CUDA call
+    assert _fwd(lib, B=300, H=300) == attn.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, B=300, H=300, dt=attn.ATTN_DTYPE_F32) == attn.ATTN_ERR_UNSUPPORTED
 
 
 def test_backward_argument_checks(lib):
