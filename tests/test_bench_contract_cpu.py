@@ -1,0 +1,32 @@
+"""The bench's output contract, checked on the CPU through its reference arm
+(`bench.py --impl reference`, the oracle on a bounded row sample): one JSON line
+with the keys and types the contract names."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "fp32_small", "--steps", "1", "--warmup", "0"], capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["impl"] == "reference"
+    assert out["n_gpus"] == 1 and out["steps"] == 1 and out["warmup"] == 0
+    assert out["unit"] == "TFLOP/s" and out["higher_is_better"] is True
+    assert isinstance(out["value"], (int, float)) and out["value"] > 0
+    assert out["config"]["workload"].startswith("fp32_small")
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == out["value"] and cb["sample"]
+    e2e = out["e2e"]
+    assert e2e["value"] == out["value"] and e2e["unit"] == out["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
