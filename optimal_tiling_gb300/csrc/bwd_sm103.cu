@@ -20,23 +20,29 @@
 //                     dP^T = V dO_i^T        (128 x 64, into dP buffer)
 //                     dV  += P^T dO_i        (A = P^T from tensor memory)
 //                     dK  += dS^T Q_i        (A = dS^T from shared memory)
-//                     dQ_i^T = K^T dS_i^T    (M = d: into the dP buffer, which the
-//                                             softmax warps have already read)
+//                     dQ_i^T = K^T dS_i^T    (M = d: into a buffer of its own)
 //                   P and dS come from eight warps (thread = key; warps 0-3 take
 //                   queries 0-31 of a block, warps 4-7 queries 32-63): a clock trace
 //                   of one CTA showed the elementwise work of four warps, ~1,560
 //                   cycles per block, to be the longest stage of the loop.
-//                   The MMAs come from three warps, because one thread issues a
-//                   tcgen05.mma only every ~100 cycles while the tensor core takes
-//                   them several times faster: warp 13 issues S^T then dV (so that
-//                   S^T of block i+2 follows, in one thread's issue order, the dV
-//                   that read P of block i from the same columns), warp 14 dP^T then
-//                   dK, warp 15 dQ^T; warps 8-11 drain dQ^T, warp 12 loads.
+//                   The MMAs come from three warps, each waiting only for what its
+//                   own products need (one thread issuing all five stalls every
+//                   product behind each wait on another role): warp 13 issues S^T
+//                   then dV (so that S^T of block i+2 follows, in one thread's issue
+//                   order, the dV that read P of block i from the same columns),
+//                   warp 14 dP^T then dK, warp 15 dQ^T; warps 8-11 drain dQ^T,
+//                   warp 12 loads.
 //                   dQ_i^T is drained by its own warpgroup into shared memory as
-//                   [q][d] fp32 and added into the accumulator with one bulk
-//                   reduction (cp.reduce.async.bulk .add.f32).  S/dP are double
-//                   buffered so that the next block's two products overlap the
-//                   elementwise work of this one.  dK and dV leave tensor memory
+//                   [q][d] fp32 and added into the accumulator by two bulk
+//                   reductions (cp.reduce.async.bulk .add.f32), one per 32-query
+//                   half, so that rewriting a half waits only for the reduction
+//                   of the same half one block back.  S is double
+//                   buffered (it holds P until dV has read it); dP has one buffer,
+//                   released as soon as the P/dS warps have loaded it, so dP^T of
+//                   the next block overlaps this block's elementwise work and no
+//                   longer waits for the dQ^T drain (when dQ^T shared the dP
+//                   buffers, the chain P/dS -> dQ^T -> drain -> dP^T of block
+//                   i+2 set the pace of the loop).  dK and dV leave tensor memory
 //                   once, at the end.
 //   3. bwd_dq_convert: dQ = bf16(s * accumulator).
 #include <cuda_bf16.h>
@@ -79,8 +85,8 @@ struct BwdCfg {
     static constexpr int kDqOff = kDsOff + 2 * kDsTile;
     static constexpr int kLdOff = kDqOff + kDqTile;      // per stage: LSE[64], D[64]
     static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
-    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull[2], dqfree[2], kvdone, drain[3]
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 5 + 1 + 3;
+    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull, dqfree, dpfree, kvdone, drain[3]
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // visited query blocks as a bit set: up to 32 * kMaxMaskWords 64-row blocks (N <= 131072)
     static constexpr int kMaxMaskWords = 64;
@@ -88,8 +94,10 @@ struct BwdCfg {
     static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
     // tensor memory columns
-    static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 2 * BQ;
-    static_assert(kColDP + 2 * BQ <= kTmemCols, "tensor memory budget");
+    // dV, dK accumulators; S^T twice (it holds P until dV has read it); dP^T once (read into
+    // registers at the start of a block's elementwise work); dQ^T of one block
+    static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 2 * BQ, kColQ = kColDP + BQ;
+    static_assert(kColQ + BQ <= kTmemCols, "tensor memory budget");
 };
 
 struct BwdBars {
@@ -100,10 +108,11 @@ struct BwdBars {
     __device__ uint32_t sfull(int b) const { return base + 8u * (1 + 2 * kStages + b); }
     __device__ uint32_t pfull(int b) const { return base + 8u * (3 + 2 * kStages + b); }
     __device__ uint32_t dsfree(int b) const { return base + 8u * (5 + 2 * kStages + b); }
-    __device__ uint32_t dqfull(int b) const { return base + 8u * (7 + 2 * kStages + b); }
-    __device__ uint32_t dqfree(int b) const { return base + 8u * (9 + 2 * kStages + b); }
-    __device__ uint32_t kvdone() const { return base + 8u * (11 + 2 * kStages); }
-    __device__ uint32_t drain(int role) const { return base + 8u * (12 + 2 * kStages + role); }
+    __device__ uint32_t dqfull() const { return base + 8u * (7 + 2 * kStages); }
+    __device__ uint32_t dqfree() const { return base + 8u * (8 + 2 * kStages); }
+    __device__ uint32_t dpfree() const { return base + 8u * (9 + 2 * kStages); }
+    __device__ uint32_t kvdone() const { return base + 8u * (10 + 2 * kStages); }
+    __device__ uint32_t drain(int role) const { return base + 8u * (11 + 2 * kStages + role); }
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -180,9 +189,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bars.sfull(b), 2);    // S^T (warp 9) and dP^T (warp 10)
             mbar_init(bars.pfull(b), 256);
             mbar_init(bars.dsfree(b), 2);   // dK (warp 10) and dQ^T (warp 11) read dS
-            mbar_init(bars.dqfull(b), 1);
-            mbar_init(bars.dqfree(b), 128);
         }
+        mbar_init(bars.dqfull(), 1);
+        mbar_init(bars.dqfree(), 128);      // the drain warps have read dQ^T
+        mbar_init(bars.dpfree(), 256);      // the P/dS warps have read dP^T
         mbar_init(bars.kvdone(), 2);        // dV and dK complete
         for (int r = 0; r < 3; ++r) mbar_init(bars.drain(r), 1);
         fence_barrier_init();
@@ -260,14 +270,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const int s = it % kStages, b = it & 1;
                     if (!mbar_wait(bars.qfull(s), (uint32_t)(it / kStages) & 1u, abort_flag, p.dev_status))
                         return false;
-                    // the dP buffer held dQ^T of block it-2: wait until it was drained
-                    if (role == 1 && it >= 2 &&
-                        !mbar_wait(bars.dqfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status))
+                    // one dP buffer: the P/dS warps must have read dP^T of block it-1
+                    if (role == 1 && it >= 1 &&
+                        !mbar_wait(bars.dpfree(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status))
                         return false;
                     tc_fence_after();
                     const uint32_t xb = (role == 0 ? sQ : sdO) + s * C::kQTile;
                     const uint32_t kb = role == 0 ? sK : sV;
-                    const uint32_t dcol = tmem + (role == 0 ? C::kColS : C::kColDP) + b * BQ;
+                    const uint32_t dcol = tmem + (role == 0 ? C::kColS + b * BQ : C::kColDP);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
@@ -309,16 +319,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int it = 0; it < n && ok; ++it) {
                     const int b = it & 1;
                     if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                    // one dQ^T buffer: the drain warps must have read dQ^T of block it-1
+                    if (it >= 1 && !(ok = mbar_wait(bars.dqfree(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status)))
+                        break;
                     tc_fence_after();
                     const uint32_t dsb = sDs + b * C::kDsTile;
-                    // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous); into the dP
-                    // buffer, whose dP^T the softmax warps have read (pfull)
+                    // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous)
 #pragma unroll
                     for (int ks = 0; ks < BKV / 16; ++ks)
-                        mma_ss(tmem + C::kColDP + b * BQ, smem_desc_sw128(sK + ks * 2048, C::kKVSlab, 1024),
+                        mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + ks * 2048, C::kKVSlab, 1024),
                                smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
                     mma_commit(bars.dsfree(b));
-                    mma_commit(bars.dqfull(b));
+                    mma_commit(bars.dqfull());
                 }
             }
             if (!ok) {
@@ -358,17 +370,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float *lse = ld_f + s * 2 * BQ;  // LSE of the 64 queries, then D
             const float *dvv = lse + BQ;
             uint32_t pk[16], dk[16];
+            uint32_t sr[32], pr[32];
+            if (row_kept) {
+                tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
+                tmem_ld32(lane_base + C::kColDP + h * 32, pr);
+                tmem_wait_ld();
+                reg_fence(sr);
+                reg_fence(pr);
+            }
+            // dP^T is in registers: the single dP buffer may take the next block's product
+            tc_fence_before();
+            mbar_arrive(bars.dpfree());
             if (!row_kept) {
                 // keys removed for this query block: P = dS = 0 (warp-uniform)
 #pragma unroll
                 for (int t = 0; t < 16; ++t) pk[t] = dk[t] = 0u;
             } else {
-                uint32_t sr[32], pr[32];
-                tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
-                tmem_ld32(lane_base + C::kColDP + b * BQ + h * 32, pr);
-                tmem_wait_ld();
-                reg_fence(sr);
-                reg_fence(pr);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int q = h * 32 + 2 * t;
@@ -424,7 +441,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int q = 0; q < D / 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
         }
     } else if (warp < kTmaWarp) {
-        // ------------------------------------------------------------ dQ drain warps 4-7
+        // ------------------------------------------------------------ dQ drain warps 8-11
         // Every drain thread runs the same sequence of named barriers whatever happens:
         // after a failed (timed-out) wait the work is skipped but the barriers are kept,
         // and the CTA abort flag makes every later wait return at once.
@@ -434,38 +451,41 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool alive = true;
         int iq = -1;
         for (int it = 0; it < n; ++it) {
-            const int b = it & 1;
             iq = next_q(iq);
-            bool ok = alive && mbar_wait(bars.dqfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
+            bool ok = alive && mbar_wait(bars.dqfull(), (uint32_t)it & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
             uint32_t r0[32], r1[32];
             if (ok) {
                 tc_fence_after();
-                tmem_ld32(lane_base + C::kColDP + b * BQ, r0);
-                tmem_ld32(lane_base + C::kColDP + b * BQ + 32, r1);
+                tmem_ld32(lane_base + C::kColQ, r0);
+                tmem_ld32(lane_base + C::kColQ + 32, r1);
                 tmem_wait_ld();
                 reg_fence(r0);
                 reg_fence(r1);
                 tc_fence_before();
-                mbar_arrive(bars.dqfree(b));
+                mbar_arrive(bars.dqfree());
             }
-            // the previous bulk reduction must have finished reading the staging tile
-            if (t == 0) bulk_wait_read_all();
-            named_bar_sync(1, 128);
-            if (ok) {
+            // Two halves (queries 0-31 from r0, 32-63 from r1), each with its own 16 KB of the
+            // staging tile and its own bulk reduction: before a half is rewritten only the
+            // reduction of the same half one block back must have read it, not the one just issued.
+            const size_t q0 = (size_t)head * p.N + (size_t)iq * BQ;
+            auto stage = [&](const uint32_t(&r)[32], int hq) {
+                if (t == 0) bulk_wait_read_but_one();
+                named_bar_sync(1, 128);
+                if (ok) {
+                    float *dst = dq_gen + hq * 32 * D;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    dq_gen[q * D + t] = __uint_as_float(r0[q]);
-                    dq_gen[(q + 32) * D + t] = __uint_as_float(r1[q]);
+                    for (int q = 0; q < 32; ++q) dst[q * D + t] = __uint_as_float(r[q]);
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
-            }
-            named_bar_sync(1, 128);
-            if (t == 0 && ok) {
-                const size_t q0 = (size_t)head * p.N + (size_t)iq * BQ;
-                bulk_reduce_add_f32(dQacc + q0 * D, sDq, C::kDqTile);
-                bulk_commit();
-            }
+                named_bar_sync(1, 128);
+                if (t == 0 && ok) {
+                    bulk_reduce_add_f32(dQacc + (q0 + 32 * hq) * D, sDq + hq * (C::kDqTile / 2), C::kDqTile / 2);
+                    bulk_commit();
+                }
+            };
+            stage(r0, 0);
+            stage(r1, 1);
             alive = alive && ok;
         }
         if (t == 0) bulk_wait_all();

@@ -137,6 +137,10 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// All but the most recent committed bulk group have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- tcgen05
 // Descriptor of a 128B-swizzled shared-memory operand (see the file comment).
