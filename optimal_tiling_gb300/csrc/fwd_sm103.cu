@@ -223,8 +223,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int it = 0; it < n && ok; ++it) {
                 if (it + 1 < n && !(ok = issue_s(it + 1))) break;
                 const int s = it % S;
-                if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                // V_it was loaded long ago: check it before waiting for P_it, so that only P_it is
+                // waited for on the path from the softmax to PV
                 if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
                 tc_fence_after();
                 const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
                 const uint32_t vb = sV + s * C::kTileBytes;
@@ -547,11 +549,13 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const int s = j % S;
                 const bool more = j + 1 < n;
                 const uint32_t ph = (uint32_t)j & 1u;
-                if (!(ok = mbar_wait(bars.pfull(0), ph, abort_flag, p.dev_status))) break;
+                // V_j and K_{j+1} were loaded long ago: check them while tile A's softmax still
+                // runs, so that only P_A(j) is waited for on the path from softmax to PV
                 if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(j / S) & 1u, abort_flag, p.dev_status))) break;
                 if (more && !(ok = mbar_wait(bars.kfull((j + 1) % S), (uint32_t)((j + 1) / S) & 1u, abort_flag,
                                              p.dev_status)))
                     break;
+                if (!(ok = mbar_wait(bars.pfull(0), ph, abort_flag, p.dev_status))) break;
                 tc_fence_after();
                 mma_pv(0, j);
                 if (more) mma_s(0, j + 1);
