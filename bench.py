@@ -247,16 +247,19 @@ def run_cuda(args):
     total_flops = _sum_over_ranks(dist, step_flops, dev)
     value = total_flops / (ms * 1e-3) / 1e12
 
-    # per-pass and per-kernel figures from the launch timing (same timed region)
+    # per-pass and per-kernel figures from the launch timing (same timed region), per step: a
+    # family may launch more than one kernel per step (bwd_main: the full tiles, then the
+    # query halves of a split last wave)
     def kms(name):
         n, t = prof.get(name, (0, 0.0))
-        return (t / n if n else float("nan")), n
+        return (t / args.steps if n else float("nan")), n
 
     fwd_ms, fwd_n = kms("fwd_bf16")
     main_ms, main_n = kms("bwd_main")
     pre_ms, _ = kms("bwd_pre")
     conv_ms, _ = kms("bwd_dq_convert")
-    bwd_ms = main_ms + pre_ms + conv_ms
+    fin_ms = kms("bwd_kv_finish")[0] if "bwd_kv_finish" in prof else 0.0
+    bwd_ms = main_ms + pre_ms + conv_ms + fin_ms
     peak = float(peaks["bf16_tflops"])
     peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
     # dominant kernel: the one with the largest share of the timed region
@@ -295,7 +298,7 @@ def run_cuda(args):
         "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 1),
                 "frac_of_peak": round(bwd_flops / (bwd_ms * 1e-3) / 1e12 / peak, 4),
                 "kernels_ms": {"bwd_pre": round(pre_ms, 4), "bwd_main": round(main_ms, 4),
-                               "bwd_dq_convert": round(conv_ms, 4)}},
+                               "bwd_kv_finish": round(fin_ms, 4), "bwd_dq_convert": round(conv_ms, 4)}},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"

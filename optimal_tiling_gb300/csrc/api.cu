@@ -97,10 +97,12 @@ attn_status launch_status(cudaError_t e) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+
 // ---- launch timing ---------------------------------------------------------
 struct ProfFamily {
     std::string name;
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;  // one event pair per scope
+    long long launches;                                    // kernels the scopes cover
 };
 bool g_prof_on = false;
 std::vector<ProfFamily> g_prof;
@@ -117,7 +119,7 @@ ProfScope::ProfScope(const char *kernel, cudaStream_t st) : slot_(-1), idx_(0), 
     for (size_t i = 0; i < g_prof.size(); ++i)
         if (g_prof[i].name == kernel) fam = (int)i;
     if (fam < 0) {
-        g_prof.push_back(ProfFamily{kernel, {}});
+        g_prof.push_back(ProfFamily{kernel, {}, 0});
         fam = (int)g_prof.size() - 1;
     }
     cudaEvent_t a, b;
@@ -128,8 +130,15 @@ ProfScope::ProfScope(const char *kernel, cudaStream_t st) : slot_(-1), idx_(0), 
     }
     cudaEventRecord(a, st);
     g_prof[fam].ev.emplace_back(a, b);
+    g_prof[fam].launches += 1;
     slot_ = fam;
     idx_ = g_prof[fam].ev.size() - 1;
+}
+
+void ProfScope::add_launch() {
+    if (slot_ < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if ((size_t)slot_ < g_prof.size()) g_prof[slot_].launches += 1;
 }
 
 ProfScope::~ProfScope() {
@@ -137,6 +146,23 @@ ProfScope::~ProfScope() {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if ((size_t)slot_ < g_prof.size() && idx_ < g_prof[slot_].ev.size())
         cudaEventRecord(g_prof[slot_].ev[idx_].second, st_);
+}
+
+size_t bwd_base_bytes(int B, int H, int N, int d, bool bf16) {
+    const size_t rows = (size_t)B * H * N;
+    size_t bytes = (rows * sizeof(float) + 255) / 256 * 256;                    // D
+    if (bf16) bytes += (rows * (size_t)d * sizeof(float) + 255) / 256 * 256;   // dQ accumulator
+    return bytes;
+}
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0) {
+        cudaGetLastError();
+        sms = 152;
+    }
+    return sms;
 }
 
 }  // namespace attn
@@ -165,7 +191,7 @@ attn_status attn_profile_query(int index, char *name, int name_capacity, int *la
         if (cudaEventElapsedTime(&ms, e.first, e.second) != cudaSuccess) return ATTN_ERR_CUDA;
         tot += ms;
     }
-    if (launches) *launches = (int)f.ev.size();
+    if (launches) *launches = (int)f.launches;
     if (total_ms) *total_ms = tot;
     return ATTN_OK;
 }
@@ -247,9 +273,9 @@ attn_status attn_fwd_masked(const void *Q, const void *K, const void *V, void *O
 
 size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
     if (check_common(B, H, N, d, dtype) != ATTN_OK) return 0;
-    const size_t rows = (size_t)B * H * N;
-    size_t bytes = align_up(rows * sizeof(float), 256);              // D
-    if (dtype == ATTN_DTYPE_BF16) bytes += align_up(rows * d * sizeof(float), 256);  // dQ accumulator
+    size_t bytes = attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16);
+    if (dtype == ATTN_DTYPE_BF16)  // fp32 partial dK, dV of the last wave's split tiles
+        bytes += align_up(attn::bwd_split_bytes(attn::bwd_split_tiles(B, H, N), d), 256);
     return bytes;
 }
 
@@ -270,7 +296,7 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_BF16 && !bf16_bwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
-    const size_t need = attn_bwd_workspace_size(B, H, N, d, dtype);
+    const size_t need = attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
@@ -285,11 +311,15 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
             static_cast<float *>(dK), static_cast<float *>(dV), D, st));
     }
     float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(rows * sizeof(float), 256));
+    // split the last wave (dense problems) when the workspace also holds the partial dK, dV
+    int split = mask == nullptr ? attn::bwd_split_tiles(B, H, N) : 0;
+    if (split > 0 && workspace_bytes < need + attn::bwd_split_bytes(split, d)) split = 0;
+    float *kvacc = split > 0 ? reinterpret_cast<float *>(static_cast<char *>(workspace) + need) : nullptr;
     attn::BwdMaps maps;
     if (!make_map_bf16(&maps.q, Q, d, rows, 64) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
         !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.dO, dO, d, rows, 64))
         return ATTN_ERR_CUDA;
-    return launch_status(attn::launch_bwd_bf16(p, maps, O, dO, LSE, dQ, dK, dV, D, dQacc, st));
+    return launch_status(attn::launch_bwd_bf16(p, maps, O, dO, LSE, dQ, dK, dV, D, dQacc, kvacc, split, st));
 }
 
 }  // namespace

@@ -121,11 +121,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 // ------------------------------------------------------------------------- 1
 // D_i = sum_t dO_it O_it; the dQ accumulator row is zeroed.  One warp per row.
+// The split tiles' partial dK, dV (kv4: kv_n4 float4) are zeroed grid-stride.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       float *__restrict__ Dv, float *__restrict__ dQacc,
-                                                      size_t rows) {
+                                                      size_t rows, float4 *__restrict__ kv4, size_t kv_n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < kv_n4; i += (size_t)gridDim.x * blockDim.x)
+        kv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -147,12 +150,17 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
 }
 
 // ------------------------------------------------------------------------- 2
-template <int D>
+// HALVES = false: grid (N / 128, B * H), CTA (x, y) takes key tile x of head y; a tile at or
+// after split_from (in the order head * (N / 128) + x) belongs to the split last wave and its
+// CTA returns at once.  HALVES = true: grid 2 * (tiles - split_from), two CTAs per split tile,
+// each taking one half of the query blocks and adding fp32 partial dK, dV into kvacc.
+template <int D, bool HALVES>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const Problem p, const float *__restrict__ LSE, const float *__restrict__ Dv,
-                float *__restrict__ dQacc, __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV) {
+                float *__restrict__ dQacc, __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV,
+                const int split_from, float *__restrict__ kvacc) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,8 +169,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kvt = blockIdx.x, head = blockIdx.y;
     const int nq = p.N / BQ;                   // 64-row query blocks
+    int kvt, head, q_lo;                       // key tile, head, first query block
+    if constexpr (HALVES) {
+        const int tile = split_from + (int)(blockIdx.x >> 1);
+        kvt = tile % (p.N / BKV);
+        head = tile / (p.N / BKV);
+        q_lo = (blockIdx.x & 1) * (nq / 2);
+    } else {
+        // The HALVES grid reads nothing this grid writes (both only add into accumulators),
+        // so it may start on SMs this grid frees: allow that as soon as every CTA is running.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        kvt = blockIdx.x;
+        head = blockIdx.y;
+        q_lo = 0;
+        if (head * (int)gridDim.x + kvt >= split_from) return;  // run by the HALVES launch
+    }
     const int kv0 = head * p.N + kvt * BKV;    // first K/V row of this CTA in the [B*H*N, D] view
     const uint8_t *hm = p.head_mask(head);
     const int mb = p.mask_block, mnb = p.mask_nb();
@@ -212,7 +234,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const VisitBits vb{vwords, nwords};
-    int n = nq;  // query blocks this key tile visits
+    int n = HALVES ? nq / 2 : nq;  // query blocks this CTA visits
     if (use_bits) {
         n = vb.count();
     } else if (hm != nullptr) {  // columns longer than the bit set: read the mask directly
@@ -239,7 +261,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmdO);
-            int iq = -1;
+            int iq = q_lo - 1;
             for (int it = 0; it < n; ++it) {
                 const int s = it % kStages;
                 iq = next_q(iq);
@@ -352,7 +374,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint8_t *ds_gen = sm + C::kDsOff;
         // 64-row mask blocks: this warp's 32 keys lie in one key half of the tile
         const bool fine = hm != nullptr && mb == 64;
-        int iq = -1;
+        int iq = q_lo - 1;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
             const int s = it % kStages, b = it & 1;
@@ -422,7 +444,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint4 *orow = reinterpret_cast<uint4 *>((h == 0 ? dK : dV) + grow * D);
         const uint32_t acc = lane_base + (h == 0 ? C::kColDK : C::kColDV);
         const float mul = h == 0 ? p.scale : 1.f;
-        if (ok && n > 0) {
+        if (HALVES && ok && n > 0) {
+            // one query half of a split tile: add this row's partial dK or dV in fp32
+            float4 *prow = reinterpret_cast<float4 *>(kvacc + ((size_t)(blockIdx.x >> 1) * 2 + h) * BKV * D +
+                                                      (size_t)key * D);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t a[32];
+                tmem_ld32(acc + c0, a);
+                tmem_wait_ld();
+                reg_fence(a);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    atomicAdd(prow + c0 / 4 + q,
+                              make_float4(__uint_as_float(a[4 * q]) * mul, __uint_as_float(a[4 * q + 1]) * mul,
+                                          __uint_as_float(a[4 * q + 2]) * mul, __uint_as_float(a[4 * q + 3]) * mul));
+            }
+        } else if (ok && n > 0) {
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t a[32];
@@ -449,7 +487,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         float *dq_gen = reinterpret_cast<float *>(sm + C::kDqOff);
         bool alive = true;
-        int iq = -1;
+        int iq = q_lo - 1;
         for (int it = 0; it < n; ++it) {
             iq = next_q(iq);
             bool ok = alive && mbar_wait(bars.dqfull(), (uint32_t)it & 1u, abort_flag, p.dev_status);
@@ -499,6 +537,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // The HALVES grid may run beside the full-tile grid; it completes only after that grid has
+    // (whose work is done by then, this wait ends), so that later work on the stream, which
+    // reads the dQ accumulator both add into, follows both grids.
+    if constexpr (HALVES) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------- 3
@@ -517,30 +559,82 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__rest
     }
 }
 
+// ------------------------------------------------------------------------- 4
+// Split tiles: dK and dV rows are bf16 of the fp32 sum of the two query halves (dK is
+// already scaled).  One CTA per (split tile, dK or dV).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_kv_finish_kernel(const float *__restrict__ kvacc,
+                                                             __nv_bfloat16 *__restrict__ dK,
+                                                             __nv_bfloat16 *__restrict__ dV, int split_from,
+                                                             int tiles_per_head, int N) {
+    const int s = blockIdx.x >> 1, h = blockIdx.x & 1;
+    const int tile = split_from + s;
+    const size_t kv0 = (size_t)(tile / tiles_per_head) * N + (size_t)(tile % tiles_per_head) * BKV;
+    const float4 *src = reinterpret_cast<const float4 *>(kvacc + ((size_t)s * 2 + h) * BKV * D);
+    uint4 *dst = reinterpret_cast<uint4 *>((h == 0 ? dK : dV) + kv0 * D);
+    for (int i = threadIdx.x; i < BKV * D / 8; i += blockDim.x) {
+        const float4 a = src[2 * i], b = src[2 * i + 1];
+        dst[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+    }
+}
+
 template <int D>
 cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const void *dO, const float *LSE,
-                     void *dQ, void *dK, void *dV, float *Dv, float *dQacc, cudaStream_t st) {
+                     void *dQ, void *dK, void *dV, float *Dv, float *dQacc, float *kvacc, int split,
+                     cudaStream_t st) {
     const size_t rows = (size_t)p.B * p.H * p.N;
+    const int tiles = (p.N / BKV) * p.B * p.H;
+    if (kvacc == nullptr) split = 0;
     {
         ProfScope prof_("bwd_pre", st);
-        bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(O),
-                                                                       static_cast<const __nv_bfloat16 *>(dO), Dv,
-                                                                       dQacc, rows);
+        bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dv, dQacc, rows,
+            reinterpret_cast<float4 *>(kvacc), bwd_split_bytes(split, D) / sizeof(float4));
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto kern = bwd_main_kernel<D>;
+    auto kern = bwd_main_kernel<D, false>;
+    auto kh = bwd_main_kernel<D, true>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
+    if (e == cudaSuccess && split > 0)
+        e = cudaFuncSetAttribute(kh, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.N / BKV, p.B * p.H);
     {
+        // one timing scope over both launches: together they are the five products of every tile
         ProfScope prof_("bwd_main", st);
-        kern<<<grid, kThreads, BwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.dO, p, LSE, Dv, dQacc,
-                                                             static_cast<__nv_bfloat16 *>(dK),
-                                                             static_cast<__nv_bfloat16 *>(dV));
+        kern<<<dim3(p.N / BKV, p.B * p.H), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
+            m.q, m.k, m.v, m.dO, p, LSE, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
+            static_cast<__nv_bfloat16 *>(dV), tiles - split, kvacc);
+        e = cudaGetLastError();
+        if (e == cudaSuccess && split > 0) {
+            // programmatic dependent launch: the halves may start while the last full tiles run
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(2 * split));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = BwdCfg<D>::kSmemBytes;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, kh, m.q, m.k, m.v, m.dO, p, LSE, static_cast<const float *>(Dv), dQacc,
+                                   static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), tiles - split,
+                                   kvacc);
+            if (e == cudaSuccess) prof_.add_launch();
+        }
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (split > 0) {
+        {
+            ProfScope prof_("bwd_kv_finish", st);
+            bwd_kv_finish_kernel<D><<<(unsigned)(2 * split), 256, 0, st>>>(
+                kvacc, static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), tiles - split,
+                p.N / BKV, p.N);
+        }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const size_t n8 = rows * D / 8;
     {
         ProfScope prof_("bwd_dq_convert", st);
@@ -552,12 +646,21 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
 
 }  // namespace
 
+int bwd_split_tiles(int B, int H, int N) {
+    const long long tiles = (long long)B * H * (N / BKV);
+    const int sms = device_sm_count();
+    const long long r = tiles % sms;
+    return (tiles > sms && r > 0 && 2 * r <= sms) ? (int)r : 0;
+}
+
+size_t bwd_split_bytes(int split_tiles, int d) { return (size_t)split_tiles * 2 * BKV * d * sizeof(float); }
+
 cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O, const void *dO,
                             const float *LSE, void *dQ, void *dK, void *dV, float *Dv, float *dQacc,
-                            cudaStream_t st) {
+                            float *kvacc, int split_tiles, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
     switch (p.d) {
-        case 128: return launch_d<128>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, st);
+        case 128: return launch_d<128>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, kvacc, split_tiles, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "internal.h"
 
 namespace {
 
@@ -54,8 +55,10 @@ extern "C" attn_status attn_bwd_static_workspace(const void *Q, const void *K, c
                                                  int B, int H, int N, int d, float scale, attn_dtype dtype,
                                                  const uint8_t *block_mask, void *stream) {
     if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
-    const size_t need = attn_bwd_workspace_size(B, H, N, d, dtype);
-    if (need > kStaticWorkspaceBytes) return ATTN_ERR_WORKSPACE;  // shape needs more than the fixed array
+    // the shape's D and dQ scratch must fit the array; attn_bwd splits the last wave only
+    // when the split's scratch fits as well
+    if (attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16) > kStaticWorkspaceBytes)
+        return ATTN_ERR_WORKSPACE;
     void *ws = static_ws_address();
     if (ws == nullptr) return ATTN_ERR_CUDA;
     return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype, block_mask, ws,

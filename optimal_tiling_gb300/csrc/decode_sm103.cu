@@ -384,13 +384,8 @@ DecodeShape decode_shape(int B, int H, int Nq, int Nk, int d, float scale) {
     sh.Nk = Nk;
     sh.d = d;
     sh.scale = scale;
-    // one persistent CTA per SM of the current device (152 when it cannot be asked)
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess || sms <= 0) {
-        cudaGetLastError();
-        sms = 152;
-    }
+    // one persistent CTA per SM of the current device
+    const int sms = device_sm_count();
     sh.sph = (Nk + kGroup - 1) / kGroup;
     sh.steps = (long long)B * H * sh.sph;
     sh.ctas = (int)std::min<long long>(sms, sh.steps);

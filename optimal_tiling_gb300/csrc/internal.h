@@ -22,6 +22,7 @@ class ProfScope {
   public:
     ProfScope(const char *kernel, cudaStream_t st);
     ~ProfScope();
+    void add_launch();  // the scope covers one more kernel launch than the first
 
   private:
     int slot_;
@@ -63,9 +64,22 @@ cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, floa
 struct BwdMaps {
     CUtensorMap q, k, v, dO;
 };
+// The backward runs one CTA per 128-key tile of one head.  When the SM count does not
+// divide the number of tiles and the last wave would be at most half full, the tiles of
+// that wave are split into two query halves each (dense problems), so that the wave takes
+// half a tile's time; the halves add fp32 partial dK and dV into scratch (kvacc, zeroed by
+// the launch) and a small kernel converts them.
+// Scratch every backward needs: D (B*H*N fp32) and, for bf16, the fp32 dQ accumulator,
+// each rounded up to 256 bytes; the last-wave split's scratch follows it.
+size_t bwd_base_bytes(int B, int H, int N, int d, bool bf16);
+int bwd_split_tiles(int B, int H, int N);        // tiles to split, 0 for none
+size_t bwd_split_bytes(int split_tiles, int d);  // fp32 dK and dV of the split tiles
 cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O,
                             const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
-                            float *D, float *dQacc, cudaStream_t st);
+                            float *D, float *dQacc, float *kvacc, int split_tiles, cudaStream_t st);
+
+// SM count of the current device (152 when it cannot be asked).
+int device_sm_count();
 
 struct MatMaps {
     CUtensorMap q, k, e, v;

@@ -82,6 +82,22 @@ def test_backward_argument_checks(lib):
     assert lib.attn_bwd_workspace_size(0, 2, 256, 64, attn.ATTN_DTYPE_F32) == 0
 
 
+def test_bwd_workspace_holds_the_last_wave_split(lib):
+    """The size query adds fp32 dK and dV for the tiles of a last wave that is split into
+    query halves: when the SM count does not divide the 128-key tiles and the remainder
+    is at most half the SMs (a machine without a GPU is taken to have 152)."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    up = lambda x: -(-x // 256) * 256
+    for tiles in (sms - 1, sms, sms + 1, sms + sms // 2, sms + sms // 2 + 1, 2 * sms, 3 * sms + 7):
+        N = 128 * tiles
+        r = tiles % sms
+        split = r if tiles > sms and 0 < r and 2 * r <= sms else 0
+        base = up(N * 4) + up(N * 128 * 4)
+        assert lib.attn_bwd_workspace_size(1, 1, N, 128, attn.ATTN_DTYPE_BF16) == base + split * 2 * 128 * 128 * 4
+        assert lib.attn_bwd_workspace_size(1, 1, N, 128, attn.ATTN_DTYPE_F32) == up(N * 4)
+
+
 def test_materialized_argument_checks(lib):
     need = lib.attn_fwd_materialized_workspace_size(2, 3, 256, 64, attn.ATTN_DTYPE_BF16)
     assert need >= 6 * 256 * 256 * 2

@@ -113,3 +113,37 @@ def test_full_size_workloads_sampled(oracle_mod, name, with_kv):
             assert rel_l2(dk[b, h][kr], gK) <= TOL_BF16_GRAD_RL2
             assert rel_l2(dv[b, h][kr], gV) <= TOL_BF16_GRAD_RL2
     assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+
+
+def test_last_wave_split_matches_unsplit(oracle_mod):
+    """A dense shape whose last wave is split into query halves (the SM count does not
+    divide the 128-key tiles and the remainder is at most half the SMs).  With r tiles
+    per head and r dividing the SM count, the split tiles are exactly the last head.
+    dK and dV of the other heads are bit-identical to the masked path, which never
+    splits; the split head, whose two fp32 partials are added in either order, agrees
+    to a few bf16 roundings, and with the oracle on sampled rows."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    r = max(t for t in range(1, sms // 4 + 1) if sms % t == 0)
+    H, N, d = sms // r + 1, 128 * r, 128
+    s = 1.0 / math.sqrt(d)
+    x = inputs.make_inputs(1, H, N, d, torch.bfloat16, seed=31)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = attn.attn_fwd(q, k, v, s)
+    lib = attn.load()
+    rows = H * N
+    base = -(-rows * 4 // 256) * 256 + -(-rows * d * 4 // 256) * 256
+    assert lib.attn_bwd_workspace_size(1, H, N, d, attn.ATTN_DTYPE_BF16) == base + r * 2 * 128 * d * 4
+    split = attn.attn_bwd(q, k, v, o, do, lse, s)
+    ones = torch.ones((r, r), dtype=torch.uint8, device=DEV)
+    whole = attn.attn_bwd_masked(q, k, v, o, do, lse, s, ones)
+    assert attn.attn_device_status() == attn.ATTN_OK
+    dq_s, dk_s, dv_s = (t.float().cpu().numpy()[0] for t in split)
+    dq_w, dk_w, dv_w = (t.float().cpu().numpy()[0] for t in whole)
+    assert np.array_equal(dk_s[:-1], dk_w[:-1]) and np.array_equal(dv_s[:-1], dv_w[:-1])
+    assert rel_l2(dk_s[-1], dk_w[-1]) <= 2e-3 and rel_l2(dv_s[-1], dv_w[-1]) <= 2e-3
+    assert rel_l2(dq_s, dq_w) <= 1e-3
+    kr = _sample(16, N, 7)
+    qr = _sample(8, N, 8)
+    gQ, gK, gV = oracle_mod.bwd_rows(x["q"][0, -1], x["k"][0, -1], x["v"][0, -1], x["do"][0, -1], s, qr, kr, None)
+    assert rel_l2(dk_s[-1][kr], gK) <= TOL_BF16_GRAD_RL2 and rel_l2(dv_s[-1][kr], gV) <= TOL_BF16_GRAD_RL2
+    assert rel_l2(dq_s[-1][qr], gQ) <= TOL_BF16_GRAD_RL2
