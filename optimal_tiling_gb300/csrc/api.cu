@@ -317,7 +317,8 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
     float *kvacc = split > 0 ? reinterpret_cast<float *>(static_cast<char *>(workspace) + need) : nullptr;
     attn::BwdMaps maps;
     if (!make_map_bf16(&maps.q, Q, d, rows, 64) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
-        !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.dO, dO, d, rows, 64))
+        !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.dO, dO, d, rows, 64) ||
+        !make_map_bf16(&maps.dk, dK, d, rows, 128) || !make_map_bf16(&maps.dv, dV, d, rows, 128))
         return ATTN_ERR_CUDA;
     return launch_status(attn::launch_bwd_bf16(p, maps, O, dO, LSE, dQ, dK, dV, D, dQacc, kvacc, split, st));
 }

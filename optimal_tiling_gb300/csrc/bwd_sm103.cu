@@ -158,6 +158,7 @@ template <int D, bool HALVES>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                 const Problem p, const float *__restrict__ LSE, const float *__restrict__ Dv,
                 float *__restrict__ dQacc, __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV,
                 const int split_from, float *__restrict__ kvacc) {
@@ -461,6 +462,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                           __uint_as_float(a[4 * q + 2]) * mul, __uint_as_float(a[4 * q + 3]) * mul));
             }
         } else if (ok && n > 0) {
+            // Stage the bf16 tile (dK in the Q ring, dV in the dO ring: every MMA that reads them
+            // completed before kvdone) in the 128-byte-swizzled layout of a 64-column TMA box, then
+            // one thread of the four warps stores it with two tensor stores.
+            uint8_t *stage = sm + (h == 0 ? C::kQOff : C::kdOOff);
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t a[32];
@@ -471,9 +476,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
                     pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * mul, __uint_as_float(a[2 * t + 1]) * mul);
+                uint8_t *slab = stage + (c0 >> 6) * C::kKVSlab + key * 128;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    orow[c0 / 8 + q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) {
+                    const int u = ((c0 & 63) >> 3) + q;  // 16-byte unit within the 128-byte row
+                    *reinterpret_cast<uint4 *>(slab + ((u ^ (key & 7)) << 4)) =
+                        make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2 + h, 128);
+            if ((tid & 127) == 0) {
+                const CUtensorMap *tm = h == 0 ? &tmdK : &tmdV;
+                const uint32_t src = smem_addr(stage);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) tma_store_2d(tm, c * 64, kv0, src + c * C::kKVSlab);
+                bulk_commit();
+                bulk_wait_all();
             }
         } else if (n == 0) {
             for (int q = 0; q < D / 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
@@ -603,7 +622,7 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
         // one timing scope over both launches: together they are the five products of every tile
         ProfScope prof_("bwd_main", st);
         kern<<<dim3(p.N / BKV, p.B * p.H), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
-            m.q, m.k, m.v, m.dO, p, LSE, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
+            m.q, m.k, m.v, m.dO, m.dk, m.dv, p, LSE, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
             static_cast<__nv_bfloat16 *>(dV), tiles - split, kvacc);
         e = cudaGetLastError();
         if (e == cudaSuccess && split > 0) {
@@ -618,7 +637,7 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, kh, m.q, m.k, m.v, m.dO, p, LSE, static_cast<const float *>(Dv), dQacc,
+            e = cudaLaunchKernelEx(&cfg, kh, m.q, m.k, m.v, m.dO, m.dk, m.dv, p, LSE, static_cast<const float *>(Dv), dQacc,
                                    static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), tiles - split,
                                    kvacc);
             if (e == cudaSuccess) prof_.add_launch();

@@ -63,6 +63,7 @@ cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, floa
 
 struct BwdMaps {
     CUtensorMap q, k, v, dO;
+    CUtensorMap dk, dv;  // outputs, 128-row boxes (tensor stores of the dK, dV tiles)
 };
 // The backward runs one CTA per 128-key tile of one head.  When the SM count does not
 // divide the number of tiles and the last wave would be at most half full, the tiles of
