@@ -461,32 +461,36 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                               make_float4(__uint_as_float(a[4 * q]) * mul, __uint_as_float(a[4 * q + 1]) * mul,
                                           __uint_as_float(a[4 * q + 2]) * mul, __uint_as_float(a[4 * q + 3]) * mul));
             }
-        } else if (ok && n > 0) {
+        } else if (!HALVES && n > 0) {
             // Stage the bf16 tile (dK in the Q ring, dV in the dO ring: every MMA that reads them
             // completed before kvdone) in the 128-byte-swizzled layout of a 64-column TMA box, then
-            // one thread of the four warps stores it with two tensor stores.
+            // one thread of the four warps stores it with two tensor stores.  The four warps meet
+            // at the named barrier whatever `ok` says (a warp that gave up after a timed-out wait
+            // still arrives), so that no warp waits there for one that skipped it.
             uint8_t *stage = sm + (h == 0 ? C::kQOff : C::kdOOff);
+            if (ok) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t a[32];
-                tmem_ld32(acc + c0, a);
-                tmem_wait_ld();
-                reg_fence(a);
-                uint32_t pa[16];
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(acc + c0, a);
+                    tmem_wait_ld();
+                    reg_fence(a);
+                    uint32_t pa[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * mul, __uint_as_float(a[2 * t + 1]) * mul);
-                uint8_t *slab = stage + (c0 >> 6) * C::kKVSlab + key * 128;
+                    for (int t = 0; t < 16; ++t)
+                        pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * mul, __uint_as_float(a[2 * t + 1]) * mul);
+                    uint8_t *slab = stage + (c0 >> 6) * C::kKVSlab + key * 128;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int u = ((c0 & 63) >> 3) + q;  // 16-byte unit within the 128-byte row
-                    *reinterpret_cast<uint4 *>(slab + ((u ^ (key & 7)) << 4)) =
-                        make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                    for (int q = 0; q < 4; ++q) {
+                        const int u = ((c0 & 63) >> 3) + q;  // 16-byte unit within the 128-byte row
+                        *reinterpret_cast<uint4 *>(slab + ((u ^ (key & 7)) << 4)) =
+                            make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                    }
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             named_bar_sync(2 + h, 128);
-            if ((tid & 127) == 0) {
+            if ((tid & 127) == 0 && ok) {
                 const CUtensorMap *tm = h == 0 ? &tmdK : &tmdV;
                 const uint32_t src = smem_addr(stage);
 #pragma unroll

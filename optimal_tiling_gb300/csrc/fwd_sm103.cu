@@ -39,6 +39,10 @@ namespace {
 
 using namespace ptx;
 
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 constexpr int BM = 128;             // query rows per CTA
 constexpr int BN = 128;             // keys per streamed block
 constexpr int kThreads = 192;       // 4 softmax warps + TMA warp + MMA warp
@@ -107,8 +111,8 @@ __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const Problem p, __nv_bfloat16 *__restrict__ O,
-                float *__restrict__ LSE) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
+                __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
     using C = FwdCfg<D>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -364,28 +368,47 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after();
         }
         const size_t grow = (size_t)row0 + tid;
-        uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
-        if (ok && n > 0) {
-            // a row whose every visited score was removed (64-row masks) has l = 0:
-            // O = 0 and LSE = -inf, with the tensor-memory loads still warp-wide
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (n > 0) {
+            // O leaves through the Q tile (the last MMA that read it completed before odone):
+            // rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
+            // stores the tile.  The four warps meet at the named barrier whatever `ok` says.
+            uint8_t *stage = sm + C::kQOff;
+            if (ok) {
+                // a row whose every visited score was removed (64-row masks) has l = 0:
+                // O = 0 and LSE = -inf, with the tensor-memory loads still warp-wide
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + kOCol + c0, o);
-                tmem_wait_ld();
-                reg_fence(o);
-                uint32_t pk[16];
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kOCol + c0, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                    for (int t = 0; t < 16; ++t)
+                        pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                    uint8_t *slab = stage + (c0 >> 6) * C::kChunkBytes + tid * 128;
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int v = 0; v < 4; ++v) {
+                        const int u = ((c0 & 63) >> 3) + v;  // 16-byte unit within the 128-byte row
+                        *reinterpret_cast<uint4 *>(slab + ((u ^ (tid & 7)) << 4)) =
+                            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+                fence_proxy_async_smem();
             }
-            LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-        } else if (n == 0) {
+            named_bar_sync(1, 128);
+            if (tid == 0 && ok) {
+                const uint32_t src = smem_addr(stage);
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&tmO, c * 64, row0, src + c * C::kChunkBytes);
+                bulk_commit();
+                bulk_wait_all();
+            }
+        } else {
             // every key block removed: O = 0, LSE = -inf
+            uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
             for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
             LSE[grow] = -INFINITY;
         }
@@ -451,8 +474,8 @@ struct PPBars {
 template <int D>
 __global__ void __launch_bounds__(kPPThreads, 1)
 fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Problem p, __nv_bfloat16 *__restrict__ O,
-                   float *__restrict__ LSE) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
+                   __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
     using C = PPCfg<D>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -661,9 +684,12 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
         }
+        // O leaves through this tile's Q region (the last MMA that read Q_X completed before
+        // odone): rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
+        // stores the tile.  The tile's four warps meet at the named barrier whatever `ok` says.
+        uint8_t *stage = sm + C::kQOff + x * C::kTileBytes;
         if (ok) {
             const size_t grow = (size_t)row0 + x * BM + r;
-            uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
             const float inv = 1.f / l;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -675,11 +701,24 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                 for (int t = 0; t < 16; ++t)
                     pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                uint8_t *slab = stage + (c0 >> 6) * C::kChunkBytes + r * 128;
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    orow[c0 / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                for (int v = 0; v < 4; ++v) {
+                    const int u = ((c0 & 63) >> 3) + v;  // 16-byte unit within the 128-byte row
+                    *reinterpret_cast<uint4 *>(slab + ((u ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
             }
             LSE[grow] = (m_used + __log2f(l)) * kLn2;
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(1 + x, 128);
+        if (r == 0 && ok) {
+            const uint32_t src = smem_addr(stage);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&tmO, c * 64, row0 + x * BM, src + c * C::kChunkBytes);
+            bulk_commit();
+            bulk_wait_all();
         }
     }
 
@@ -699,7 +738,8 @@ cudaError_t launch_pp(const Problem &p, const FwdMaps &m, void *O, float *LSE, c
     dim3 grid(p.N / (2 * BM), p.B * p.H);
     {
         ProfScope prof_("fwd_bf16", st);
-        kern<<<grid, kPPThreads, PPCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, p, static_cast<__nv_bfloat16 *>(O), LSE);
+        kern<<<grid, kPPThreads, PPCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, static_cast<__nv_bfloat16 *>(O),
+                                                              LSE);
     }
     return cudaGetLastError();
 }
@@ -712,7 +752,8 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
     dim3 grid(p.N / BM, p.B * p.H);
     {
         ProfScope prof_("fwd_bf16", st);
-        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, p, static_cast<__nv_bfloat16 *>(O), LSE);
+        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, static_cast<__nv_bfloat16 *>(O),
+                                                            LSE);
     }
     return cudaGetLastError();
 }
