@@ -9,8 +9,9 @@
 //   P = exp(s Q K^T - LSE),  dV = P^T dO,  dP = dO V^T,  D_i = sum_t dO_it O_it,
 //   dS = P o (dP - D),  dQ = s dS K,  dK = s dS^T Q.
 //
-// Three kernels on the caller's stream:
-//   1. bwd_pre:     D = rowsum(dO o O) in fp32, and the fp32 dQ accumulator zeroed;
+// Kernels on the caller's stream:
+//   1. bwd_pre:     D = rowsum(dO o O) in fp32, the fp32 dQ accumulator zeroed (and
+//                   the split tiles' fp32 dK, dV scratch, see 2);
 //   2. bwd_main:    one CTA per 128-row K/V tile of one head, looping over the
 //                   64-row query blocks that the block mask keeps (with 64-row
 //                   mask blocks one half of the tile's keys can be removed for a
@@ -43,8 +44,14 @@
 //                   longer waits for the dQ^T drain (when dQ^T shared the dP
 //                   buffers, the chain P/dS -> dQ^T -> drain -> dP^T of block
 //                   i+2 set the pace of the loop).  dK and dV leave tensor memory
-//                   once, at the end.
-//   3. bwd_dq_convert: dQ = bf16(s * accumulator).
+//                   once, at the end, through shared memory and tensor stores.
+//                   When the SM count does not divide the tiles and the last wave
+//                   would be at most half full, the tiles of that wave run as a
+//                   second grid (a programmatic dependent launch) of two CTAs per
+//                   tile, each over half of the query blocks, adding fp32 dK and dV
+//                   into scratch;
+//   3. bwd_kv_finish (split tiles only): dK, dV = bf16 of that scratch;
+//   4. bwd_dq_convert: dQ = bf16(s * accumulator).
 #include <cuda_bf16.h>
 
 #include <algorithm>
