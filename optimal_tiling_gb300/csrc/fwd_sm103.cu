@@ -614,25 +614,35 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t rr[4][32];
+            // S in two 64-column halves, so that only 64 scores are live at a time: the max over
+            // both halves, the exps of the high half (still in registers), then the low half
+            // loaded again; P of the high half (columns 32..63, which hold S of keys 32..63) is
+            // written only after that reload
+            uint32_t rr[2][32];
             tmem_ld32(scol + 0, rr[0]);
             tmem_ld32(scol + 32, rr[1]);
-            tmem_ld32(scol + 64, rr[2]);
-            tmem_ld32(scol + 96, rr[3]);
             tmem_wait_ld();
             reg_fence(rr[0]);
             reg_fence(rr[1]);
-            reg_fence(rr[2]);
-            reg_fence(rr[3]);
-            float mxq[4];
+            float mxh[2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                mxq[q] = fmaxf(__uint_as_float(rr[q][0]), __uint_as_float(rr[q][1]));
+            for (int q = 0; q < 2; ++q) {
+                mxh[q] = fmaxf(__uint_as_float(rr[q][0]), __uint_as_float(rr[q][1]));
 #pragma unroll
                 for (int t = 1; t < 16; ++t)
-                    mxq[q] = fmax3(mxq[q], __uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1]));
+                    mxh[q] = fmax3(mxh[q], __uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1]));
             }
-            const float mx = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]);
+            tmem_ld32(scol + 64, rr[0]);
+            tmem_ld32(scol + 96, rr[1]);
+            tmem_wait_ld();
+            reg_fence(rr[0]);
+            reg_fence(rr[1]);
+            float mx = fmaxf(mxh[0], mxh[1]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    mx = fmax3(mx, __uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1]));
             const float m_new = fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
             if (m_new > m_used + kRescaleThreshold) {
@@ -656,8 +666,28 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t negm2 = f2_pack(-m_used, -m_used);
             uint64_t sumq[4];
+            uint32_t pkh[2][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int qq = 0; qq < 2; ++qq) {
+                sumq[2 + qq] = f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[qq][2 * t]), __uint_as_float(rr[qq][2 * t + 1])),
+                                               sl2x2, negm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[2 + qq] = f2_add(sumq[2 + qq], f2_pack(y0, y1));
+                    pkh[qq][t] = pack_bf16(y0, y1);
+                }
+            }
+            tmem_ld32(scol + 0, rr[0]);
+            tmem_ld32(scol + 32, rr[1]);
+            tmem_wait_ld();
+            reg_fence(rr[0]);
+            reg_fence(rr[1]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
                 sumq[q] = f2_pack(0.f, 0.f);
                 uint32_t pk[16];
 #pragma unroll
@@ -672,6 +702,8 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 tmem_st16(scol + q * 16, pk);
             }
+            tmem_st16(scol + 32, pkh[0]);
+            tmem_st16(scol + 48, pkh[1]);
             float rs0, rs1;
             f2_unpack(f2_add(f2_add(sumq[0], sumq[1]), f2_add(sumq[2], sumq[3])), rs0, rs1);
             l = l * alpha + (rs0 + rs1);
