@@ -130,13 +130,13 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype d
  * Out: dQ, dK, dV [B,H,N,d] (dtype).
  * workspace: device scratch of at least attn_bwd_workspace_size() bytes
  *      (16-byte aligned, contents on entry ignored); it holds D and, for bf16,
- *      the fp32 dQ accumulator.  For bf16 without a mask, when the current
+ *      LSE log2(e) and the fp32 dQ accumulator.  For bf16 without a mask, when the current
  *      device's SM count does not divide the 128-key tiles and the last wave of
  *      tiles would be at most half full, the size also covers fp32 dK and dV of
  *      that wave's tiles, which are then split into two query halves each (so
  *      that the wave takes half a tile's time); the size therefore depends on
- *      the current device.  A workspace that holds only D and the dQ
- *      accumulator also works: the last wave is then not split.
+ *      the current device.  A workspace that holds only those row terms and
+ *      the dQ accumulator also works: the last wave is then not split.
  */
 ATTN_API attn_status attn_bwd(const void *Q, const void *K, const void *V, const void *O,
                      const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
@@ -164,8 +164,8 @@ ATTN_API attn_status attn_bwd_masked(const void *Q, const void *K, const void *V
  * Same arguments and results as attn_bwd, without the workspace: the scratch
  * comes from a fixed 64 MiB array compiled into the library, held in device
  * memory of every GPU that loads the library until the process exits.
- *   - Shapes whose D and dQ scratch exceeds 64 MiB (B*H*N rows of 4 bytes,
- *     plus 4d bytes for bf16, each part rounded up to 256 bytes) return
+ *   - Shapes whose row-term and dQ scratch exceeds 64 MiB (B*H*N rows of 4
+ *     bytes, 8 + 4d bytes for bf16, each part rounded up to 256 bytes) return
  *     ATTN_ERR_WORKSPACE and launch nothing (bf16, d = 128: B*H*N up to
  *     about 129,000 rows; fp32: B*H*N up to 16 million rows).  The last-wave
  *     split of attn_bwd is used when its scratch fits as well.

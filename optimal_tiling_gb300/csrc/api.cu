@@ -150,7 +150,8 @@ ProfScope::~ProfScope() {
 
 size_t bwd_base_bytes(int B, int H, int N, int d, bool bf16) {
     const size_t rows = (size_t)B * H * N;
-    size_t bytes = (rows * sizeof(float) + 255) / 256 * 256;                    // D
+    // D (and, for bf16, LSE log2(e) after it)
+    size_t bytes = ((bf16 ? 2 : 1) * rows * sizeof(float) + 255) / 256 * 256;
     if (bf16) bytes += (rows * (size_t)d * sizeof(float) + 255) / 256 * 256;   // dQ accumulator
     return bytes;
 }
@@ -310,7 +311,8 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
             static_cast<const float *>(O), static_cast<const float *>(dO), LSE, static_cast<float *>(dQ),
             static_cast<float *>(dK), static_cast<float *>(dV), D, st));
     }
-    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(rows * sizeof(float), 256));
+    // D, LSE log2(e), then the fp32 dQ accumulator
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(2 * rows * sizeof(float), 256));
     // split the last wave (dense problems) when the workspace also holds the partial dK, dV
     int split = mask == nullptr ? attn::bwd_split_tiles(B, H, N) : 0;
     if (split > 0 && workspace_bytes < need + attn::bwd_split_bytes(split, d)) split = 0;

@@ -10,8 +10,9 @@
 //   dS = P o (dP - D),  dQ = s dS K,  dK = s dS^T Q.
 //
 // Kernels on the caller's stream:
-//   1. bwd_pre:     D = rowsum(dO o O) in fp32, the fp32 dQ accumulator zeroed (and
-//                   the split tiles' fp32 dK, dV scratch, see 2);
+//   1. bwd_pre:     D = rowsum(dO o O) and L2 = LSE log2(e) in fp32 (so that P is
+//                   one FMA and one exp2 per score), the fp32 dQ accumulator zeroed
+//                   (and the split tiles' fp32 dK, dV scratch, see 2);
 //   2. bwd_main:    one CTA per 128-row K/V tile of one head, looping over the
 //                   64-row query blocks that the block mask keeps (with 64-row
 //                   mask blocks one half of the tile's keys can be removed for a
@@ -72,7 +73,7 @@ constexpr int kThreads = 512;
 constexpr int kDqWarp0 = 8;     // warps 0-7 P/dS, warps 8-11 drain dQ
 constexpr int kTmaWarp = 12;
 constexpr int kMmaWarp = 13;    // warps 13, 14, 15 issue MMAs (see the kernel comment)
-constexpr int kStages = 3;      // Q/dO/LSE/D ring depth (loads run two blocks ahead of the MMAs)
+constexpr int kStages = 3;      // Q/dO/L2/D ring depth (loads run two blocks ahead of the MMAs)
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
@@ -90,7 +91,7 @@ struct BwdCfg {
     static constexpr int kdOOff = kQOff + kStages * kQTile;
     static constexpr int kDsOff = kdOOff + kStages * kQTile;
     static constexpr int kDqOff = kDsOff + 2 * kDsTile;
-    static constexpr int kLdOff = kDqOff + kDqTile;      // per stage: LSE[64], D[64]
+    static constexpr int kLdOff = kDqOff + kDqTile;      // per stage: L2[64], D[64]
     static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
     // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull, dqfree, dpfree, kvdone, drain[3]
     static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3;
@@ -127,13 +128,15 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // ------------------------------------------------------------------------- 1
-// D_i = sum_t dO_it O_it; the dQ accumulator row is zeroed.  One warp per row.
+// D_i = sum_t dO_it O_it and L2_i = LSE_i log2(e) (the row's log-sum-exp in the base-2 units of
+// the exponentials below); the dQ accumulator row is zeroed.  One warp per row.
 // The split tiles' partial dK, dV (kv4: kv_n4 float4) are zeroed grid-stride.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       float *__restrict__ Dv, float *__restrict__ dQacc,
-                                                      size_t rows, float4 *__restrict__ kv4, size_t kv_n4) {
+                                                      size_t rows, float4 *__restrict__ kv4, size_t kv_n4,
+                                                      const float *__restrict__ LSE, float *__restrict__ L2) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < kv_n4; i += (size_t)gridDim.x * blockDim.x)
         kv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -151,7 +154,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
         acc = fmaf(a.y, b.y, acc);
     }
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) Dv[row] = acc;
+    if (lane == 0) {
+        Dv[row] = acc;
+        L2[row] = LSE[row] * kLog2e;
+    }
     float4 *z = reinterpret_cast<float4 *>(dQacc + row * D);
     for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
-                const Problem p, const float *__restrict__ LSE, const float *__restrict__ Dv,
+                const Problem p, const float *__restrict__ L2, const float *__restrict__ Dv,
                 float *__restrict__ dQacc, __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV,
                 const int split_from, float *__restrict__ kvacc) {
     using C = BwdCfg<D>;
@@ -213,16 +219,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_init(bars.kv(), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bars.qfull(s), 1);
-            mbar_init(bars.qempty(s), 2);   // dV (warp 9) and dK (warp 10) are the last readers
+            mbar_init(bars.qempty(s), 2);   // dV (warp 13) and dK (warp 14) are the last readers
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bars.sfull(b), 2);    // S^T (warp 9) and dP^T (warp 10)
-            mbar_init(bars.pfull(b), 256);
-            mbar_init(bars.dsfree(b), 2);   // dK (warp 10) and dQ^T (warp 11) read dS
+            mbar_init(bars.sfull(b), 2);    // S^T (warp 13) and dP^T (warp 14)
+            mbar_init(bars.pfull(b), 8);    // one lane of each P/dS warp
+            mbar_init(bars.dsfree(b), 2);   // dK (warp 14) and dQ^T (warp 15) read dS
         }
         mbar_init(bars.dqfull(), 1);
-        mbar_init(bars.dqfree(), 128);      // the drain warps have read dQ^T
-        mbar_init(bars.dpfree(), 256);      // the P/dS warps have read dP^T
+        mbar_init(bars.dqfree(), 4);        // the drain warps have read dQ^T (one lane each)
+        mbar_init(bars.dpfree(), 8);        // the P/dS warps have read dP^T (one lane each)
         mbar_init(bars.kvdone(), 2);        // dV and dK complete
         for (int r = 0; r < 3; ++r) mbar_init(bars.drain(r), 1);
         fence_barrier_init();
@@ -282,7 +288,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tma_load_2d(sQ + s * C::kQTile + c * C::kQSlab, &tmQ, c * 64, q0, bars.qfull(s));
                     tma_load_2d(sdO + s * C::kQTile + c * C::kQSlab, &tmdO, c * 64, q0, bars.qfull(s));
                 }
-                bulk_load(sLd + s * 2 * BQ * 4, LSE + q0, BQ * 4, bars.qfull(s));
+                bulk_load(sLd + s * 2 * BQ * 4, L2 + q0, BQ * 4, bars.qfull(s));
                 bulk_load(sLd + s * 2 * BQ * 4 + BQ * 4, Dv + q0, BQ * 4, bars.qfull(s));
             }
         }
@@ -397,8 +403,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const float *lse = ld_f + s * 2 * BQ;  // LSE of the 64 queries, then D
-            const float *dvv = lse + BQ;
+            const float *l2 = ld_f + s * 2 * BQ;  // LSE log2(e) of the 64 queries, then D
+            const float *dvv = l2 + BQ;
             uint32_t pk[16], dk[16];
             uint32_t sr[32], pr[32];
             if (row_kept) {
@@ -408,9 +414,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 reg_fence(sr);
                 reg_fence(pr);
             }
-            // dP^T is in registers: the single dP buffer may take the next block's product
+            // dP^T is in registers: the single dP buffer may take the next block's product.
+            // A warp signals through one lane after a warp sync (256 single-thread arrivals on
+            // one barrier per block made the backward ~1.5% slower).
             tc_fence_before();
-            mbar_arrive(bars.dpfree());
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.dpfree());
             if (!row_kept) {
                 // keys removed for this query block: P = dS = 0 (warp-uniform)
 #pragma unroll
@@ -419,8 +428,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int q = h * 32 + 2 * t;
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -lse[q] * kLog2e));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -lse[q + 1] * kLog2e));
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -l2[q]));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -l2[q + 1]));
                     const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
                     const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
                     pk[t] = pack_bf16(p0, p1);
@@ -440,7 +449,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bars.pfull(b));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.pfull(b));
         }
         // ------------------------------------------------------------ dK (warps 0-3), dV (warps 4-7)
         if (ok && n > 0) {
@@ -531,7 +541,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 reg_fence(r0);
                 reg_fence(r1);
                 tc_fence_before();
-                mbar_arrive(bars.dqfree());
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.dqfree());
             }
             // Two halves (queries 0-31 from r0, 32-63 from r1), each with its own 16 KB of the
             // staging tile and its own bulk reduction: before a half is rewritten only the
@@ -567,9 +578,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    // The HALVES grid may run beside the full-tile grid; it completes only after that grid has
-    // (whose work is done by then, this wait ends), so that later work on the stream, which
-    // reads the dQ accumulator both add into, follows both grids.
+    // The HALVES grid may run beside the full-tile grid. Each of its CTAs ends by waiting for
+    // that grid to complete (its last tiles are done or nearly so by then), so that later work
+    // on the stream, which reads the dQ accumulator both grids add into, follows both.
     if constexpr (HALVES) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -619,7 +630,7 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
         ProfScope prof_("bwd_pre", st);
         bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dv, dQacc, rows,
-            reinterpret_cast<float4 *>(kvacc), bwd_split_bytes(split, D) / sizeof(float4));
+            reinterpret_cast<float4 *>(kvacc), bwd_split_bytes(split, D) / sizeof(float4), LSE, Dv + rows);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -633,7 +644,7 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
         // one timing scope over both launches: together they are the five products of every tile
         ProfScope prof_("bwd_main", st);
         kern<<<dim3(p.N / BKV, p.B * p.H), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
-            m.q, m.k, m.v, m.dO, m.dk, m.dv, p, LSE, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
+            m.q, m.k, m.v, m.dO, m.dk, m.dv, p, Dv + rows, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
             static_cast<__nv_bfloat16 *>(dV), tiles - split, kvacc);
         e = cudaGetLastError();
         if (e == cudaSuccess && split > 0) {
@@ -648,7 +659,8 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, kh, m.q, m.k, m.v, m.dO, m.dk, m.dv, p, LSE, static_cast<const float *>(Dv), dQacc,
+            e = cudaLaunchKernelEx(&cfg, kh, m.q, m.k, m.v, m.dO, m.dk, m.dv, p, static_cast<const float *>(Dv + rows),
+                                   static_cast<const float *>(Dv), dQacc,
                                    static_cast<__nv_bfloat16 *>(dK), static_cast<__nv_bfloat16 *>(dV), tiles - split,
                                    kvacc);
             if (e == cudaSuccess) prof_.add_launch();

@@ -1,8 +1,8 @@
 // attn_bwd_static_workspace: the backward pass for callers that cannot
 // allocate device memory.
 //
-// attn_bwd needs scratch (the row terms D and, for bf16, the fp32 dQ
-// accumulator) that the caller normally allocates and passes in.  Some callers
+// attn_bwd needs scratch (the row terms D and, for bf16, LSE log2(e) and the
+// fp32 dQ accumulator) that the caller normally allocates and passes in.  Some callers
 // cannot do that: code that runs inside a host framework which owns every device
 // allocation through its own pool and forbids allocations made behind its back,
 // or code on a latency-critical path that must not allocate after start-up
@@ -12,8 +12,8 @@
 //
 // The array lives in device memory of every GPU that loads the library, for as
 // long as the process runs.  It is shared by every call on a device and keeps
-// the contents of the last call; the backward writes D in full and zeroes the
-// dQ accumulator before adding into it, so nothing stale is read.  Two calls
+// the contents of the last call; the backward writes its row terms in full and
+// zeroes the dQ accumulator before adding into it, so nothing stale is read.  Two calls
 // whose work overlaps on the GPU (for example on two streams without ordering
 // between them) race on the array.
 #include <cuda_runtime.h>
@@ -55,7 +55,7 @@ extern "C" attn_status attn_bwd_static_workspace(const void *Q, const void *K, c
                                                  int B, int H, int N, int d, float scale, attn_dtype dtype,
                                                  const uint8_t *block_mask, void *stream) {
     if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
-    // the shape's D and dQ scratch must fit the array; attn_bwd splits the last wave only
+    // the shape's row terms and dQ scratch must fit the array; attn_bwd splits the last wave only
     // when the split's scratch fits as well
     if (attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16) > kStaticWorkspaceBytes)
         return ATTN_ERR_WORKSPACE;

@@ -93,7 +93,7 @@ def test_bwd_workspace_holds_the_last_wave_split(lib):
         N = 128 * tiles
         r = tiles % sms
         split = r if tiles > sms and 0 < r and 2 * r <= sms else 0
-        base = up(N * 4) + up(N * 128 * 4)
+        base = up(2 * N * 4) + up(N * 128 * 4)   # D and LSE log2(e), then the fp32 dQ accumulator
         assert lib.attn_bwd_workspace_size(1, 1, N, 128, attn.ATTN_DTYPE_BF16) == base + split * 2 * 128 * 128 * 4
         assert lib.attn_bwd_workspace_size(1, 1, N, 128, attn.ATTN_DTYPE_F32) == up(N * 4)
 

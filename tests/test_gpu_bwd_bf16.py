@@ -131,7 +131,7 @@ def test_last_wave_split_matches_unsplit(oracle_mod):
     o, lse = attn.attn_fwd(q, k, v, s)
     lib = attn.load()
     rows = H * N
-    base = -(-rows * 4 // 256) * 256 + -(-rows * d * 4 // 256) * 256
+    base = -(-rows * 8 // 256) * 256 + -(-rows * d * 4 // 256) * 256
     assert lib.attn_bwd_workspace_size(1, H, N, d, attn.ATTN_DTYPE_BF16) == base + r * 2 * 128 * d * 4
     split = attn.attn_bwd(q, k, v, o, do, lse, s)
     ones = torch.ones((r, r), dtype=torch.uint8, device=DEV)
