@@ -624,25 +624,28 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             tmem_wait_ld();
             reg_fence(rr[0]);
             reg_fence(rr[1]);
-            float mxh[2];
+            // row max in four independent chains of 16-column runs (a single chain through the
+            // second half made the max a long dependent sequence)
+            float mx4[4];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                mxh[q] = fmaxf(__uint_as_float(rr[q][0]), __uint_as_float(rr[q][1]));
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
+                mx4[c] = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
 #pragma unroll
-                for (int t = 1; t < 16; ++t)
-                    mxh[q] = fmax3(mxh[q], __uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1]));
+                for (int t = 1; t < 8; ++t) mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
             }
             tmem_ld32(scol + 64, rr[0]);
             tmem_ld32(scol + 96, rr[1]);
             tmem_wait_ld();
             reg_fence(rr[0]);
             reg_fence(rr[1]);
-            float mx = fmaxf(mxh[0], mxh[1]);
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
 #pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    mx = fmax3(mx, __uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1]));
+                for (int t = 0; t < 8; ++t) mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+            }
+            const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
             const float m_new = fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
             if (m_new > m_used + kRescaleThreshold) {
