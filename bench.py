@@ -501,8 +501,9 @@ def _time(fn, torch, dev, stream, iters=10):
 
 def _workloads(attn, torch, dev, stream, inputs, iomodel, peaks):
     """Every named workload, device-timed: the fused forward, the backward where
-    the workload has one, the materialising forward for the d-sweep.  FLOPs count
-    kept blocks only (the block-sparse workload)."""
+    the workload has one, the materialising forward for the d-sweep and the
+    materialising backward beside the fused one.  FLOPs count kept blocks only
+    (the block-sparse workload)."""
     peak = float(peaks["bf16_tflops"])
     out = {}
     for name in ("teaching", "dsweep_d64", "dsweep_d128", "dsweep_d256", "bwd_d128", "sparse_16k"):
@@ -529,7 +530,20 @@ def _workloads(attn, torch, dev, stream, inputs, iomodel, peaks):
                                              workspace=wsp, stream=stream), torch, dev, stream)
             r.update({"bwd_ms": round(ms, 4), "bwd_tflops": round(bf / ms / 1e9, 1),
                       "bwd_frac": round(bf / ms / 1e9 / peak, 4)})
-            del do, dq, dk, dv, wsp
+            del wsp
+            if "matbwd" in w.passes:
+                # the small-cache schedule: P and dS stored in HBM, credited the same FLOPs
+                wsp = torch.empty(attn.attn_bwd_materialized_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16),
+                                  device=dev, dtype=torch.uint8)
+                ms = _time(lambda: attn.attn_bwd_materialized(q, k, v, o, do, l, w.scale, dq=dq, dk=dk, dv=dv,
+                                                              workspace=wsp, stream=stream), torch, dev, stream)
+                extra = iomodel.materialized_bwd_extra_bytes(N, B * H, 2)
+                floor = (extra + iomodel.bwd_dram_compulsory_bytes(N, d, B * H, 2)) / (float(peaks["hbm_gbs"]) * 1e9)
+                r.update({"materialized_bwd_ms": round(ms, 4), "materialized_bwd_tflops": round(bf / ms / 1e9, 1),
+                          "materialized_bwd_extra_hbm_bytes": extra,
+                          "materialized_bwd_hbm_floor_ms": round(floor * 1e3, 4)})
+                del wsp
+            del do, dq, dk, dv
         if "mat" in w.passes:
             wsp = torch.empty(attn.attn_fwd_materialized_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16),
                               device=dev, dtype=torch.uint8)

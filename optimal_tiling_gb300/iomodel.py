@@ -130,6 +130,12 @@ def materialized_extra_bytes(N: int, heads: int, w: int) -> float:
     return heads * 2.0 * N * N * w
 
 
+def materialized_bwd_extra_bytes(N: int, heads: int, w: int) -> float:
+    """The small-cache backward's stored N x N matrices: P written and read once (dV = P^T dO),
+    dS written once and read twice (dK = s dS^T Q, dQ = s dS K)."""
+    return heads * 5.0 * N * N * w
+
+
 def report(N: int, d: int, heads: int, elem_bytes: int, M: float, hbm_bytes_per_s: float,
            flops_per_s: float, kept_fraction: float = 1.0) -> dict:
     """The pages' bounds for one workload, per GPU, as a flat dict.
