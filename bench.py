@@ -555,7 +555,37 @@ def _workloads(attn, torch, dev, stream, inputs, iomodel, peaks):
         out[name] = r
         del q, k, v, o, l
         torch.cuda.empty_cache()
+    out["sparse_16k_fine"] = _fine_masks(attn, torch, dev, stream, inputs, iomodel, peak)
     return out
+
+
+def _fine_masks(attn, torch, dev, stream, inputs, iomodel, peak):
+    """The block-sparse workload's shape with one mask per head over 64-row blocks (the band and
+    random off-band blocks of the 128-block workload, at half the block side): the masked entry
+    points, forward and backward, credited the kept-block FLOPs."""
+    w = inputs.WORKLOADS["sparse_16k"]
+    B, H, N, d = w.shape
+    x, _ = inputs.workload_inputs(w)
+    mask = inputs.band_random_mask_fine(N, B * H, seed=0)
+    kept = float(mask.float().mean())
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    dm = mask.to(dev)
+    o = torch.empty_like(q)
+    l = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    ff = iomodel.fwd_flops(N, d, B * H) * kept
+    bf = iomodel.bwd_flops(N, d, B * H) * kept
+    ms_f = _time(lambda: attn.attn_fwd_masked(q, k, v, w.scale, mask=dm, block=64, out=o, lse=l, stream=stream),
+                 torch, dev, stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    wsp = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16), device=dev, dtype=torch.uint8)
+    ms_b = _time(lambda: attn.attn_bwd_masked(q, k, v, o, do, l, w.scale, mask=dm, block=64, dq=dq, dk=dk, dv=dv,
+                                              workspace=wsp, stream=stream), torch, dev, stream)
+    r = {"shape": [B, H, N, d], "mask": "per head, 64-row blocks", "kept_block_fraction": round(kept, 4),
+         "fwd_ms": round(ms_f, 4), "fwd_tflops": round(ff / ms_f / 1e9, 1), "fwd_frac": round(ff / ms_f / 1e9 / peak, 4),
+         "bwd_ms": round(ms_b, 4), "bwd_tflops": round(bf / ms_b / 1e9, 1), "bwd_frac": round(bf / ms_b / 1e9 / peak, 4)}
+    del q, k, v, do, o, l, dq, dk, dv, wsp, dm
+    torch.cuda.empty_cache()
+    return r
 
 
 def _decode(attn, torch, dev, stream, inputs, peaks):

@@ -112,6 +112,23 @@ def band_random_mask(N: int, seed: int = 0, p: float = 0.1) -> torch.Tensor:
     return (band | (r < p)).to(torch.uint8)
 
 
+def band_random_mask_fine(N: int, heads: int, seed: int = 0, p: float = 0.1) -> torch.Tensor:
+    """One mask per head over 64-row blocks, [heads, nb, nb] with nb = ceil(N / 64): the same band
+    {-2,-1,0,+1} around the diagonal (now of 64-blocks) plus independent off-band blocks with
+    probability p, head h drawn from a generator seeded seed + h."""
+    nb = (N + 63) // 64
+    bi = torch.arange(nb).view(nb, 1)
+    bj = torch.arange(nb).view(1, nb)
+    off = bj - bi
+    band = (off >= -2) & (off <= 1)
+    out = torch.empty((heads, nb, nb), dtype=torch.uint8)
+    for h in range(heads):
+        g = torch.Generator(device="cpu")
+        g.manual_seed(seed + h)
+        out[h] = (band | (torch.rand((nb, nb), generator=g) < p)).to(torch.uint8)
+    return out
+
+
 def block_diagonal_mask(N: int) -> torch.Tensor:
     nb = num_mask_blocks(N)
     return torch.eye(nb, dtype=torch.uint8)
