@@ -40,7 +40,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of a process that already runs threads
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     for rank in range(world):
