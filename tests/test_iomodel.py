@@ -72,3 +72,27 @@ def test_report_at_teaching_example():
     assert r["fwd_time_lower_bound_s"] == max(2 * r["fwd_bound_elements"] / 1e12, G["fwd_flops"] / 1e15)
     s = iomodel.report(4096, 64, 1, 2, 65536, 1e12, 1e15, kept_fraction=0.25)
     assert s["sparse_bound_elements"] == iomodel.sparse_io_bound(2 * 4096 * 64, 0.25 * 4096 ** 2, 65536)
+
+
+def test_byte_counts_match_the_buffers_they_describe():
+    """The bench's byte helpers against the sizes of the buffers each pass must move once:
+    counted from tensors of those shapes, not from the helpers' formulas."""
+    import torch
+
+    N, d, heads = 384, 64, 3
+    nb = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt).nbytes
+    x = nb(heads, N, d)            # one of Q, K, V, O, dO, dQ, dK, dV
+    row = nb(heads, N, dt=torch.float32)  # one of LSE, D
+    nn = nb(heads, N, N)           # one N x N bf16 matrix per head
+    # forward: Q, K, V read, O written, LSE written
+    assert iomodel.fwd_dram_compulsory_bytes(N, d, heads, 2) == 4 * x + row
+    # backward: Q, K, V, O, dO read, dQ, dK, dV written, LSE read, D written and read back
+    assert iomodel.bwd_dram_compulsory_bytes(N, d, heads, 2) == 8 * x + 3 * row
+    # materialising forward: the exp-score matrix written, then read by the E V product
+    assert iomodel.materialized_extra_bytes(N, heads, 2) == 2 * nn
+    # materialising backward: P written and read by dV; dS written, read by dK and by dQ
+    assert iomodel.materialized_bwd_extra_bytes(N, heads, 2) == (1 + 1) * nn + (1 + 2) * nn
+    # K and V re-read once per 128-row query tile (N / 128 tiles), scaled by the kept share
+    kv = 2 * x
+    assert iomodel.fwd_kv_rescan_bytes(N, d, heads, 2, 128) == kv * (N // 128)
+    assert iomodel.fwd_kv_rescan_bytes(N, d, heads, 2, 128, 0.25) == kv * (N // 128) * 0.25
