@@ -30,3 +30,13 @@ def test_reference_arm_prints_one_contract_line():
     e2e = out["e2e"]
     assert e2e["value"] == out["value"] and e2e["unit"] == out["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_cuda_arm_rejects_workloads_it_does_not_time():
+    """The CUDA arm times the bf16 pipeline; asking it for the fp32 correctness workload (or an
+    unknown name) fails before any device work, with the bf16 choices listed."""
+    for name in ("fp32_small", "no_such_workload"):
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", name, "--steps", "1"],
+                           capture_output=True, text=True, timeout=300, cwd=ROOT)
+        assert r.returncode == 2 and r.stdout == ""
+        assert "dense_16k" in r.stderr and name in r.stderr
