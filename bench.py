@@ -624,20 +624,33 @@ def _decode(attn, torch, dev, stream, inputs, peaks):
 
 # ------------------------------------------------------------------------- CPU oracle
 
+def oracle_sample_flops(rows, N, d, mask=None, block=128):
+    """Floating-point operations the oracle performs for the sampled query rows in
+    cpu_baseline: for each row i with K_i kept keys, the forward row (scores and the
+    weighted sum of V: 4 d K_i) and the backward dQ row (scores again, dP = dO_i . v_j
+    and dQ_i += dS_ij k_j: 6 d K_i), 10 d K_i in all.  Masked keys cost nothing there."""
+    import numpy as np
+    rows = np.asarray(rows, dtype=np.int64)
+    if mask is None:
+        kept = np.full(rows.shape, N, dtype=np.int64)
+    else:
+        m = np.asarray(mask).astype(np.int64)
+        per_qblock = np.minimum(block * np.arange(1, m.shape[1] + 1), N) - block * np.arange(m.shape[1])
+        kept = (m * per_qblock[None, :]).sum(axis=1)[rows // block]
+    return float(10 * d * kept.sum())
+
+
 def cpu_baseline(w, budget_s: float = 10.0, seed: int = 0, data=None):
     """The oracle (as it stands) on a bounded sample of the workload: R query rows
-    of head 0 -- forward (O, LSE) and backward dQ for those rows -- credited with
-    R / (B H N) of the step's algorithmic FLOPs."""
+    of head 0 -- forward (O, LSE) and backward dQ for those rows -- credited with the
+    FLOPs those rows take (oracle_sample_flops), not a share of the whole step."""
     import oracle
-    from optimal_tiling_gb300 import inputs, iomodel
 
     oracle.build()
     B, H, N, d = w.shape
-    x, mask = data if data is not None else inputs.workload_inputs(w, seed=seed)
+    x, mask = data if data is not None else _inputs().workload_inputs(w, seed=seed)
     qh, kh, vh, doh = (x[n][0, 0] for n in ("q", "k", "v", "do"))
     m = None if mask is None else mask.numpy()
-    kept = float(mask.float().mean()) if mask is not None else 1.0
-    step_flops = (iomodel.fwd_flops(N, d, B * H) + iomodel.bwd_flops(N, d, B * H)) * kept
     R, el = 16, 0.0
     while True:
         rows = (torch_arange(R) * 7919 % N).astype("int32")
@@ -648,11 +661,17 @@ def cpu_baseline(w, budget_s: float = 10.0, seed: int = 0, data=None):
         if el >= budget_s / 4 or R >= N:
             break
         R = min(N, R * 4)
-    credited = step_flops * R / (B * H * N)
+    credited = oracle_sample_flops(rows, N, d, m)
     return {"value": round(credited / el / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(el, 3),
+            "kind": "oracle", "seconds": round(el, 3), "flops": credited,
             "sample": f"{R} query rows of head 0 (of {B * H * N} rows): oracle forward rows + backward dQ rows, "
-                      f"credited {R}/{B * H * N} of the step's 14 N^2 d B H FLOPs"}
+                      f"credited 10 d FLOPs per kept key of each sampled row (4 d forward, 6 d for the dQ "
+                      f"row's scores, dP and dQ): {credited:.4g} FLOPs"}
+
+
+def _inputs():
+    from optimal_tiling_gb300 import inputs
+    return inputs
 
 
 def torch_arange(n):

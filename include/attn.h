@@ -24,8 +24,11 @@
  *               call's dtype (fp32 or bf16); LSE is always fp32, natural log of
  *               the scaled scores.
  *   Memory      Every pointer is a DEVICE pointer on the current CUDA device,
- *               owned by the caller; the library allocates no device memory.
- *               Pointers must be 16-byte aligned and must not alias each other.
+ *               owned by the caller.  No call allocates device memory; the
+ *               library's own device footprint is static (a status word, and
+ *               the 64 MiB array of attn_bwd_static_workspace) and is held on
+ *               every device the library is loaded on.  Pointers must be
+ *               16-byte aligned and must not alias each other.
  *   Block mask  Optional (NULL = keep everything).  A device array of nb x nb
  *               bytes, nb = ceil(N / 128), row-major, shared by all (b, h):
  *               mask[i/128][j/128] == 0 removes score (i, j).  A row with no
@@ -42,9 +45,8 @@
  *               backward d = 128; materialising forward d in {64, 128, 256};
  *               materialising backward d in {64, 128}.  All: B * H <= 65535
  *               and B * H * N <= 2^31.  Anything else returns ATTN_ERR_UNSUPPORTED.
- *   Scale       Any finite s.  The bf16 forwards (fused and materialising)
- *               take the row maximum of the raw products and so need s >= 0;
- *               they return ATTN_ERR_UNSUPPORTED for s < 0.
+ *   Scale       Any finite s, of either sign (a non-finite s is
+ *               ATTN_ERR_INVALID_ARG).
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -169,9 +171,13 @@ ATTN_API attn_status attn_bwd_masked(const void *Q, const void *K, const void *V
  *     ATTN_ERR_WORKSPACE and launch nothing (bf16, d = 128: B*H*N up to
  *     about 129,000 rows; fp32: B*H*N up to 16 million rows).  The last-wave
  *     split of attn_bwd is used when its scratch fits as well.
+ *   - Arguments are checked as attn_bwd checks them (same statuses) before
+ *     the size check and before any CUDA call.
  *   - The first call on a device looks up the array's device address (one
- *     cudaGetSymbolAddress with that device current); make that first call
- *     before any stream capture.  No call allocates.
+ *     cudaGetSymbolAddress with that device current) and keeps it for the
+ *     current CUDA context; a call in a new context (after cudaDeviceReset)
+ *     looks it up again.  Make the first call on a device before any stream
+ *     capture.  No call allocates.
  *   - Every call on a device shares the array, which keeps the last call's
  *     contents; the kernels rewrite D and zero the dQ accumulator before use.
  *     Calls whose work overlaps on the GPU (e.g. unordered streams) race.

@@ -7,6 +7,7 @@ fallback of any kind.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -136,6 +137,13 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _on(stream):
+    """Context for the tensors a wrapper allocates (outputs, LSE, workspace): they belong to
+    the stream the library launches on, so that the caching allocator does not hand their
+    memory to another stream's allocation while the kernels still use it."""
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 def _raise(status, where):
     if status != ATTN_OK:
         raise AttnError(status, where)
@@ -153,10 +161,11 @@ def attn_fwd(q, k, v, scale: float, block_mask=None, out=None, lse=None, stream=
     """O, LSE = softmax(scale q k^T) v, logsumexp; tensors [B, H, N, d]."""
     lib = load()
     B, H, N, d = _shape(q)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     _check(q, k, v, out, lse, block_mask)
     st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
                       _dtype_code(q), _ptr(block_mask), _stream(stream))
@@ -187,10 +196,11 @@ def attn_fwd_masked(q, k, v, scale: float, mask=None, block: int = 128, out=None
     """attn_fwd with a general block mask: 64- or 128-blocks, shared or one per head."""
     lib = load()
     B, H, N, d = _shape(q)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     _check(q, k, v, out, lse, mask)
     bm = _block_mask(mask, block, B, H, N)
     st = lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
@@ -205,12 +215,13 @@ def attn_bwd_masked(q, k, v, o, do, lse, scale: float, mask=None, block: int = 1
     lib = load()
     B, H, N, d = _shape(q)
     code = _dtype_code(q)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
     need = attn_bwd_workspace_size(B, H, N, d, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with _on(stream):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(q) if dk is None else dk
+        dv = torch.empty_like(q) if dv is None else dv
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     _check(q, k, v, o, do, lse, dq, dk, dv, workspace, mask)
     bm = _block_mask(mask, block, B, H, N)
     st = lib.attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
@@ -226,12 +237,13 @@ def attn_bwd(q, k, v, o, do, lse, scale: float, block_mask=None, dq=None, dk=Non
     lib = load()
     B, H, N, d = _shape(q)
     code = _dtype_code(q)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
     need = attn_bwd_workspace_size(B, H, N, d, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with _on(stream):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(q) if dk is None else dk
+        dv = torch.empty_like(q) if dv is None else dv
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     _check(q, k, v, o, do, lse, dq, dk, dv, workspace, block_mask)
     st = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
                       B, H, N, d, float(scale), code, _ptr(block_mask), _ptr(workspace),
@@ -246,9 +258,10 @@ def attn_bwd_static_workspace(q, k, v, o, do, lse, scale: float, block_mask=None
     64 MiB device array (for callers that cannot allocate device memory)."""
     lib = load()
     B, H, N, d = _shape(q)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    with _on(stream):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(q) if dk is None else dk
+        dv = torch.empty_like(q) if dv is None else dv
     _check(q, k, v, o, do, lse, dq, dk, dv, block_mask)
     st = lib.attn_bwd_static_workspace(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                                        _ptr(dk), _ptr(dv), B, H, N, d, float(scale), _dtype_code(q),
@@ -263,13 +276,14 @@ def attn_fwd_materialized(q, k, v, scale: float, block_mask=None, out=None, lse=
     lib = load()
     B, H, N, d = _shape(q)
     code = _dtype_code(q)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     need = attn_fwd_materialized_workspace_size(B, H, N, d, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     _check(q, k, v, out, lse, workspace, block_mask)
     st = lib.attn_fwd_materialized(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
                                    code, _ptr(block_mask), _ptr(workspace),
@@ -288,12 +302,13 @@ def attn_bwd_materialized(q, k, v, o, do, lse, scale: float, block_mask=None, dq
     lib = load()
     B, H, N, d = _shape(q)
     code = _dtype_code(q)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
     need = attn_bwd_materialized_workspace_size(B, H, N, d, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with _on(stream):
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(q) if dk is None else dk
+        dv = torch.empty_like(q) if dv is None else dv
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     _check(q, k, v, o, do, lse, dq, dk, dv, workspace, block_mask)
     st = lib.attn_bwd_materialized(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
                                    _ptr(dv), B, H, N, d, float(scale), code, _ptr(block_mask), _ptr(workspace),
@@ -314,13 +329,14 @@ def attn_decode(q, k, v, scale: float, out=None, lse=None, workspace=None, strea
     if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != tuple(k.shape):
         raise ValueError("k and v must be [B, H, Nk, d] with q's B, H and d")
     code = _dtype_code(q)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
     need = attn_decode_workspace_size(B, H, Nq, Nk, d, code)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    with _on(stream):
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     _check(q, k, v, out, lse, workspace)
     st = lib.attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, float(scale), code,
                          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))

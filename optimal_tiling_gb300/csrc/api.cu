@@ -21,8 +21,16 @@ namespace {
 __device__ int g_dev_status;
 
 constexpr int kMaxDevices = 64;
-int *g_status_ptr[kMaxDevices];
+struct StatusAddr {
+    void *ctx;   // CUDA context the address was looked up in
+    int *ptr;
+};
+StatusAddr g_status_addr[kMaxDevices];
 std::mutex g_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+bool g_ctx_looked_up = false;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -30,17 +38,50 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Address of the status word on the current device (looked up once per device).
+}  // namespace
+
+namespace attn {
+
+void *current_context() {
+    CtxGetCurrentFn fn;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_ctx_looked_up) {
+            void *f = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                    cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+            g_ctx_looked_up = true;
+        }
+        fn = g_ctx_get_current;
+    }
+    CUcontext c = nullptr;
+    if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+}  // namespace attn
+
+namespace {
+
+// Address of the status word on the current device.  It is looked up with the device
+// current and kept for the CUDA context it was found in; a call in another context (the
+// primary context torn down and created again, e.g. after cudaDeviceReset) looks it up again.
 int *device_status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    void *ctx = attn::current_context();
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_status_ptr[dev] == nullptr) {
+    StatusAddr &a = g_status_addr[dev];
+    if (ctx == nullptr || a.ctx != ctx || a.ptr == nullptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
-        g_status_ptr[dev] = static_cast<int *>(p);
+        a.ptr = static_cast<int *>(p);
+        a.ctx = attn::current_context();  // the lookup makes the device's primary context current
     }
-    return g_status_ptr[dev];
+    return a.ptr;
 }
 
 EncodeTiledFn encode_fn() {
@@ -237,7 +278,7 @@ attn_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float
         return ATTN_ERR_INVALID_ARG;
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
-    if (dtype == ATTN_DTYPE_BF16 && (!bf16_fwd_shape_ok(N, d) || scale < 0.f)) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_DTYPE_BF16 && !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
     int *status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
     attn::Problem p{B, H, N, d, scale, mask, status, mblock, mask ? mstride : 0};
@@ -284,10 +325,13 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
 
 namespace {
 
-attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
-                     void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, attn_dtype dtype,
-                     const uint8_t *mask, int mblock, long long mstride, void *workspace, size_t workspace_bytes,
-                     void *stream) {
+}  // namespace
+
+namespace attn {
+
+attn_status bwd_args_status(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                            const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale,
+                            attn_dtype dtype) {
     attn_status s = check_common(B, H, N, d, dtype);
     if (s != ATTN_OK) return s;
     if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
@@ -297,6 +341,19 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_BF16 && !bf16_bwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+}  // namespace attn
+
+namespace {
+
+attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, const float *LSE,
+                     void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale, attn_dtype dtype,
+                     const uint8_t *mask, int mblock, long long mstride, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    attn_status s = attn::bwd_args_status(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype);
+    if (s != ATTN_OK) return s;
     const size_t need = attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     int *status = device_status_ptr();
@@ -366,7 +423,7 @@ attn_status attn_fwd_materialized(const void *Q, const void *K, const void *V, v
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return ATTN_ERR_INVALID_ARG;
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_DTYPE_BF16 || !bf16_fwd_shape_ok(N, d) || scale < 0.f) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_DTYPE_BF16 || !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
     const size_t need = attn_fwd_materialized_workspace_size(B, H, N, d, dtype);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     int *status = device_status_ptr();

@@ -30,22 +30,32 @@ constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;  // 64 MiB, the docum
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWorkspaceBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_static_ws_ptr[kMaxDevices];
+struct WsAddr {
+    void *ctx;   // CUDA context the address was looked up in
+    void *ptr;
+};
+WsAddr g_static_ws_addr[kMaxDevices];
 std::mutex g_static_ws_mu;
 
 // Device address of the array on the current device.  In host code the name
-// g_static_ws is only a host-side stand-in, so the real address is looked up
-// once per device, with that device current.
+// g_static_ws is only a host-side stand-in, so the real address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first call on that device,
+// and kept for the CUDA context it was found in: a later call in another context
+// (the primary context torn down and created again, e.g. after cudaDeviceReset)
+// looks it up again instead of handing the kernels a stale address.
 void *static_ws_address() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    void *ctx = attn::current_context();
     std::lock_guard<std::mutex> lk(g_static_ws_mu);
-    if (g_static_ws_ptr[dev] == nullptr) {
+    WsAddr &a = g_static_ws_addr[dev];
+    if (ctx == nullptr || a.ctx != ctx || a.ptr == nullptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess) return nullptr;
-        g_static_ws_ptr[dev] = p;
+        a.ptr = p;
+        a.ctx = attn::current_context();  // the lookup makes the device's primary context current
     }
-    return g_static_ws_ptr[dev];
+    return a.ptr;
 }
 
 }  // namespace
@@ -54,7 +64,10 @@ extern "C" attn_status attn_bwd_static_workspace(const void *Q, const void *K, c
                                                  const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
                                                  int B, int H, int N, int d, float scale, attn_dtype dtype,
                                                  const uint8_t *block_mask, void *stream) {
-    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    // attn_bwd's own argument checks first, so that a bad argument gets the same status as
+    // from attn_bwd whatever the shape's size; then the size, then the array's address
+    const attn_status s = attn::bwd_args_status(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, dtype);
+    if (s != ATTN_OK) return s;
     // the shape's row terms and dQ scratch must fit the array; attn_bwd splits the last wave only
     // when the split's scratch fits as well
     if (attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16) > kStaticWorkspaceBytes)

@@ -203,7 +203,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+            // a negative scale: S = (-Q) K^T, scaled by |s| below
+            const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
             // S_it = Q K_it^T into S buffer (it & 1)
@@ -250,7 +251,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else {
         // ------------------------------------------------------------ softmax warps 0-3
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float sl2 = p.scale * kLog2e;
+        const float sl2 = fabsf(p.scale) * kLog2e;  // S holds sign(s) Q K^T
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each
@@ -541,7 +542,8 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
     } else if (warp == kPPMmaWarp) {
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+            // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
+            const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             auto mma_s = [&](int x, int j) {
                 const uint32_t kb = sK + (j % S) * C::kTileBytes, qb = sQ + x * C::kTileBytes;
@@ -606,7 +608,7 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t scol = lane_base + C::scol(x);
         const uint32_t ocol = lane_base + C::kOCol0 + x * D;
-        const float sl2 = p.scale * kLog2e;
+        const float sl2 = fabsf(p.scale) * kLog2e;  // S holds sign(s) Q K^T
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/attn.h"
+
 namespace attn {
 
 // Device status word values (written by kernels, read by attn_device_status).
@@ -81,6 +83,17 @@ cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O
 
 // SM count of the current device (152 when it cannot be asked).
 int device_sm_count();
+
+// The calling thread's current CUDA context (cuCtxGetCurrent), or nullptr when none is
+// current or the driver entry point is unavailable.  Device addresses of the library's
+// __device__ variables are cached per context with it.
+void *current_context();
+
+// Every check attn_bwd makes on its arguments before any CUDA call, except the workspace's:
+// sizes, dtype, null and misaligned pointers, a non-finite scale, supported shapes.
+attn_status bwd_args_status(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                            const float *LSE, void *dQ, void *dK, void *dV, int B, int H, int N, int d, float scale,
+                            attn_dtype dtype);
 
 struct MatMaps {
     CUtensorMap q, k, e, v;

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(128) mat_scores_kernel(const __grid_constant__
     tc_fence_after();
     if (ok) {
         const float sl2 = p.scale * kLog2e;
-        const float c2 = p.scale * qnorm[q0 + tid] * kmax[head] * kLog2e;  // row bound, log2 domain
+        const float c2 = fabsf(p.scale) * qnorm[q0 + tid] * kmax[head] * kLog2e;  // row bound, log2 domain
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         uint8_t *stage = sm + C::kQOff;  // the Q tile is no longer read: stage E there (two 64-column slabs)
         float rs = 0.f;
@@ -188,7 +188,7 @@ struct MatOutEpi {
         gemm::store_row_chunk<D>(O, grow, r, c0, 1.f / rowl[grow]);
     }
     __device__ void finish(size_t grow) const {
-        LSE[grow] = scale * qnorm[grow] * kmax[grow / N] + __log2f(rowl[grow]) * kLn2;
+        LSE[grow] = fabsf(scale) * qnorm[grow] * kmax[grow / N] + __log2f(rowl[grow]) * kLn2;
     }
     __device__ void empty(size_t grow) const {
         gemm::zero_row<D>(O, grow);

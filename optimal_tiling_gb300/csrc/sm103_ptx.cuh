@@ -167,6 +167,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | (static_cast<uint32_t>(M >> 4) << 24);    // M >> 4
 }
 
+// Bit of the instruction descriptor that negates the A operand (exact: a sign flip of
+// every product).  With it the forwards compute (-Q) K^T, so that for a negative score
+// scale s the scores s Q K^T = |s| (-Q) K^T are a non-negative multiple of what the
+// tensor core returns and the row maximum of the returned products is still the one
+// the softmax needs.
+constexpr uint32_t kIdescNegateA = 1u << 13;
+
 // Whole-warp TMEM allocation; the base address is written to smem at dst_slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_slot),

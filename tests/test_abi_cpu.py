@@ -152,12 +152,31 @@ def test_masked_entry_point_checks(lib):
                                ctypes.byref(bm), None) == attn.ATTN_ERR_UNSUPPORTED
 
 
-def test_bf16_forwards_need_a_non_negative_scale(lib):
-    """The bf16 forwards take the row maximum of the raw products, which is the
-    maximum of the scaled scores only for s >= 0."""
-    assert _fwd(lib, scale=-0.5) == attn.ATTN_ERR_UNSUPPORTED
+def test_negative_scale_passes_the_argument_checks(lib):
+    """A negative score scale is a valid input for every forward: with a bad pointer
+    the call fails on the pointer, not on the scale."""
+    assert _fwd(lib, scale=-0.5, q=MIS) == attn.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("-inf")) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_materialized(MIS, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, -1.0, attn.ATTN_DTYPE_BF16,
+                                     None, FAKE, 1 << 40, None) == attn.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 256, 64, -1.0, attn.ATTN_DTYPE_BF16,
-                                     None, FAKE, 1 << 40, None) == attn.ATTN_ERR_UNSUPPORTED
+                                     None, FAKE, 16, None) == attn.ATTN_ERR_WORKSPACE
+
+
+def test_static_workspace_checks_arguments_before_its_size(lib):
+    """attn_bwd_static_workspace returns attn_bwd's status for a bad argument whatever
+    the shape's size (64 x 16 x 4096 rows need ~270 MB, above its 64 MiB array), and
+    ATTN_ERR_WORKSPACE only for a valid call that does not fit; all before any CUDA call."""
+    def call(q=FAKE, d=128, dt=attn.ATTN_DTYPE_BF16, N=4096, scale=0.1):
+        return lib.attn_bwd_static_workspace(q, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 16, N, d,
+                                             ctypes.c_float(scale), dt, None, None)
+    assert call(q=None) == attn.ATTN_ERR_INVALID_ARG
+    assert call(q=MIS) == attn.ATTN_ERR_INVALID_ARG
+    assert call(dt=7) == attn.ATTN_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert call(d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(N=4000) == attn.ATTN_ERR_UNSUPPORTED
+    assert call() == attn.ATTN_ERR_WORKSPACE
 
 
 def test_block_mask_marshalling_shapes():

@@ -40,3 +40,26 @@ def test_cuda_arm_rejects_workloads_it_does_not_time():
                            capture_output=True, text=True, timeout=300, cwd=ROOT)
         assert r.returncode == 2 and r.stdout == ""
         assert "dense_16k" in r.stderr and name in r.stderr
+
+
+def test_cpu_baseline_credits_the_rows_the_oracle_computes():
+    """cpu_baseline credits 10 d FLOPs per kept key of each sampled row: the forward row
+    (N d products for the scores and N d for P V, multiply and add counted separately)
+    and the dQ row (scores, dP and dS K again).  Counted here from the definition, row by
+    row, against the helper the bench uses, with and without a block mask."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    N, d = 512, 64
+    rows = np.array([0, 1, 127, 128, 300, 511])
+    assert bench.oracle_sample_flops(rows, N, d) == len(rows) * (4 * N * d + 6 * N * d)
+    mask = np.zeros((4, 4), dtype=np.uint8)
+    mask[0, 0] = 1
+    mask[1, :2] = 1
+    mask[2, [0, 3]] = 1
+    mask[3, :] = 1
+    want = 0
+    for i in rows:
+        keys = sum(1 for j in range(N) if mask[i // 128, j // 128])
+        want += 4 * keys * d + 6 * keys * d
+    assert bench.oracle_sample_flops(rows, N, d, mask) == want

@@ -92,11 +92,14 @@ def _sample(n, N, seed):
     return np.unique(np.concatenate([[0, N - 1], r.integers(0, N, n - 2)])).astype(np.int32)
 
 
-@pytest.mark.parametrize("name,with_kv", [("bwd_d128", True), ("sparse_16k", True), ("dense_16k", False)])
-def test_full_size_workloads_sampled(oracle_mod, name, with_kv):
+@pytest.mark.parametrize("name", ["bwd_d128", "sparse_16k", "dense_16k"])
+def test_full_size_workloads_sampled(oracle_mod, name):
     """Full-size workloads in the bench's launch configuration; the oracle computes
-    sampled gradient rows of two heads (dQ rows need one query row each; dK and dV
-    rows need every row's LSE and D, so they are checked where that stays cheap)."""
+    sampled gradient rows of the first and the last head: dQ rows (one query row each)
+    and dK, dV rows (which need every query row's LSE and D of that head).  On the
+    N = 16384 shapes the last head holds tiles of the split last wave (2048 key tiles
+    on 152 SMs leave 72 in the last wave), each accumulating 128 query blocks per
+    half; the key rows sampled there include the head's last one."""
     w = inputs.WORKLOADS[name]
     x, mask = inputs.workload_inputs(w)
     dq, dk, dv = _fwd_bwd(x, w.scale, mask, guarded=False)
@@ -105,13 +108,12 @@ def test_full_size_workloads_sampled(oracle_mod, name, with_kv):
     for head in (0, B * H - 1):
         b, h = divmod(head, H)
         qr = _sample(24, N, head)
-        kr = _sample(16, N, head + 100) if with_kv else np.zeros(0, np.int32)
+        kr = _sample(16, N, head + 100)
         gQ, gK, gV = oracle_mod.bwd_rows(x["q"][b, h], x["k"][b, h], x["v"][b, h], x["do"][b, h], w.scale,
                                          qr, kr, m)
         assert rel_l2(dq[b, h][qr], gQ) <= TOL_BF16_GRAD_RL2
-        if with_kv:
-            assert rel_l2(dk[b, h][kr], gK) <= TOL_BF16_GRAD_RL2
-            assert rel_l2(dv[b, h][kr], gV) <= TOL_BF16_GRAD_RL2
+        assert rel_l2(dk[b, h][kr], gK) <= TOL_BF16_GRAD_RL2
+        assert rel_l2(dv[b, h][kr], gV) <= TOL_BF16_GRAD_RL2
     assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
 
 
@@ -147,3 +149,34 @@ def test_last_wave_split_matches_unsplit(oracle_mod):
     gQ, gK, gV = oracle_mod.bwd_rows(x["q"][0, -1], x["k"][0, -1], x["v"][0, -1], x["do"][0, -1], s, qr, kr, None)
     assert rel_l2(dk_s[-1][kr], gK) <= TOL_BF16_GRAD_RL2 and rel_l2(dv_s[-1][kr], gV) <= TOL_BF16_GRAD_RL2
     assert rel_l2(dq_s[-1][qr], gQ) <= TOL_BF16_GRAD_RL2
+
+
+def test_negative_scale_forward_and_backward(oracle_mod):
+    """s < 0 through the whole step: the forward's O and LSE feed the backward, whose
+    gradients match the oracle's chain rule for the same negative scale."""
+    N, d = 512, 128
+    x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=33)
+    _check_full(x, -1.0 / math.sqrt(d), oracle_mod)
+
+
+def test_side_stream_without_workspace(oracle_mod):
+    """A call on a stream other than the current one, with no workspace or outputs given:
+    the binding allocates them for that stream, so the caching allocator does not reuse
+    their memory while the kernels run.  Results equal the current-stream call's."""
+    N, d = 1024, 128
+    s = 1.0 / math.sqrt(d)
+    x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=34)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    o, lse = attn.attn_fwd(q, k, v, s, stream=side)
+    got = attn.attn_bwd(q, k, v, o, do, lse, s, stream=side)
+    # allocations on the current stream meanwhile must not land in the side stream's buffers
+    junk = [torch.full((1 << 20,), 7.0, device=DEV) for _ in range(8)]
+    side.synchronize()
+    ref = attn.attn_bwd(q, k, v, o, do, lse, s)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    assert rel_l2(got[0].float().cpu().numpy(), ref[0].float().cpu().numpy()) <= 1e-3
+    del junk

@@ -136,3 +136,18 @@ def test_full_size_workloads_sampled(oracle_mod, name):
     assert max_abs(Of, Or) <= TOL_BF16_O_ABS
     assert lse_rel(Lf, Lr) <= TOL_BF16_LSE_REL
     assert np.all(np.isfinite(O))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_negative_scale(oracle_mod, d):
+    """A negative score scale (the softmax of the first page's definition takes any real
+    scores): the two-tile kernel (no mask, N % 256 == 0), the single-tile kernel (N = 384,
+    and under a block mask) against the oracle; and s Q K^T = |s| (-Q) K^T exactly, so the
+    call with -s equals the call with -Q and +s bit for bit."""
+    s = -1.0 / math.sqrt(d)
+    for N, mask in ((512, None), (384, None), (512, inputs.random_block_mask(512, seed=3, p=0.5))):
+        x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=N + d + 1, with_do=False)
+        O, L = _check_full(x, s, oracle_mod, mask)
+        flipped = dict(x, q=-x["q"])
+        O2, L2 = _fwd(flipped, -s, mask)
+        assert np.array_equal(O, O2) and np.array_equal(L, L2)

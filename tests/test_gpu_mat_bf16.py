@@ -70,3 +70,16 @@ def test_dsweep_workloads_sampled_and_against_fused(oracle_mod, name):
     assert lse_rel(Lm[heads, rows], Lr) <= TOL_BF16_LSE_REL
     assert float((om.float() - of.float()).abs().max()) <= 2 * TOL_BF16_O_ABS
     assert float(((lm - lf).abs() / lf.abs()).max()) <= 2 * TOL_BF16_LSE_REL
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_negative_scale(oracle_mod, d):
+    """s < 0: the row bound c_i = |s| |q_i| max_j |k_j| still bounds every score s q_i . k_j
+    from above, so the stored exponentials stay <= 1 and O, LSE match the oracle."""
+    N = 384
+    x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=N + d + 5, with_do=False)
+    s = -1.0 / math.sqrt(d)
+    O, L = _mat(x, s)
+    Or, Lr = oracle_mod.fwd_naive(x["q"], x["k"], x["v"], s)
+    assert max_abs(O, Or) <= TOL_BF16_O_ABS
+    assert lse_rel(L, Lr) <= TOL_BF16_LSE_REL

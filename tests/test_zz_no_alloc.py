@@ -3,7 +3,9 @@ device memory (a host framework that owns every device allocation, or a path
 that must not allocate after start-up).  Called through the C ABI and compared
 with attn_bwd on the same inputs, on two calls in a row with different inputs,
 so that the fixed scratch array's leftover contents from the first call cannot
-leak into the second.  This file is collected last on purpose."""
+leak into the second: dK and dV must be bit-identical (the same kernels run),
+dQ equal to the rounding of its fp32 accumulation order.  This file is
+collected last on purpose."""
 import ctypes
 import math
 
@@ -38,11 +40,13 @@ def _call_static(lib, q, k, v, o, do, lse, scale, dq, dk, dv):
         B, H, N, d, ctypes.c_float(scale), attn.ATTN_DTYPE_BF16, None, stream)
 
 
-def test_static_workspace_matches_attn_bwd_twice(lib):
+def _compare_twice(lib, B, H, N, d, seeds):
+    """Two calls in a row on different inputs; each against attn_bwd with its own workspace.
+    Both run the same kernels: dK and dV come out bit-identical, dQ (whose fp32 accumulation
+    order between key tiles is not fixed) to the rounding of those additions."""
     dev = torch.device("cuda")
-    B, H, N, d = 1, 4, 1024, 128
     s = 1.0 / math.sqrt(d)
-    for seed in (41, 42):  # two calls in a row, different inputs
+    for seed in seeds:
         x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=seed)
         q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
         o, lse = attn.attn_fwd(q, k, v, s)
@@ -51,9 +55,28 @@ def test_static_workspace_matches_attn_bwd_twice(lib):
         st = _call_static(lib, q, k, v, o, do, lse, s, *got)
         assert st == attn.ATTN_OK, attn.status_string(st)
         assert attn.attn_device_status() == attn.ATTN_OK
-        for g, r in zip(got, ref):
+        for g in got:
             assert torch.isfinite(g).all()
+        assert torch.equal(got[1], ref[1]), "dK differs from attn_bwd"
+        assert torch.equal(got[2], ref[2]), "dV differs from attn_bwd"
+        assert _rl2(got[0], ref[0]) <= 1e-3
+        for g, r in zip(got, ref):
             assert _rl2(g, r) <= TOL_GRAD_RL2
+
+
+def test_static_workspace_matches_attn_bwd_twice(lib):
+    _compare_twice(lib, 1, 4, 1024, 128, (41, 42))
+
+
+def test_static_workspace_with_a_split_last_wave(lib):
+    """A dense shape whose last wave of 128-key tiles is split into query halves: the
+    fp32 partial dK and dV of the split tiles then also live in the fixed array (after
+    the row terms and the dQ accumulator), and must start from zero on every call."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    r = max(t for t in range(1, sms // 4 + 1) if sms % t == 0)
+    H, N, d = sms // r + 1, 128 * r, 128
+    assert lib.attn_bwd_workspace_size(1, H, N, d, attn.ATTN_DTYPE_BF16) <= 64 << 20
+    _compare_twice(lib, 1, H, N, d, (43, 44))
 
 
 def test_static_workspace_rejects_shapes_beyond_its_size(lib):
