@@ -352,11 +352,23 @@ def _recorded_traffic(workload, kernel):
     return None
 
 
-def _io_model(iomodel, N, d, heads, kept, peaks):
-    """The pages' leading terms, at the kernels' actual tiles (bf16, w = 2 bytes)."""
+def _io_model(iomodel, N, d, heads, kept, peaks, brief=False):
+    """The pages' leading terms, at the kernels' actual tiles (bf16, w = 2 bytes).  brief:
+    the bounds only (leading-term elements, time lower bounds, the sparse bound)."""
     M_smem = 228 * 1024 / 2  # one SM's shared memory in bf16 elements (the pages' M)
     rep = iomodel.report(N, d, heads, 2, M_smem, float(peaks["hbm_gbs"]) * 1e9, float(peaks["bf16_tflops"]) * 1e12,
                          kept)
+    if brief:
+        return {
+            "M_elements_smem": M_smem,
+            "large_cache_regime": rep["large_cache_regime"],
+            "fwd_leading_term_elements": rep["fwd_leading_elements"],
+            "bwd_leading_term_elements": rep["bwd_leading_elements"],
+            "fwd_time_lower_bound_ms": round(rep["fwd_time_lower_bound_s"] * 1e3, 4),
+            "bwd_time_lower_bound_ms": round(rep["bwd_time_lower_bound_s"] * 1e3, 4),
+            **({"sparse_bound_elements": rep["sparse_bound_elements"],
+                "sparse_regime_split_M": rep["sparse_regime_split_M"]} if "sparse_bound_elements" in rep else {}),
+        }
     return {
         "fwd_time_lower_bound_ms": round(rep["fwd_time_lower_bound_s"] * 1e3, 4),
         "bwd_time_lower_bound_ms": round(rep["bwd_time_lower_bound_s"] * 1e3, 4),
@@ -519,7 +531,8 @@ def _workloads(attn, torch, dev, stream, inputs, iomodel, peaks):
         ms = _time(lambda: attn.attn_fwd(q, k, v, w.scale, block_mask=dm, out=o, lse=l, stream=stream), torch, dev,
                    stream)
         r = {"shape": [B, H, N, d], "kept_block_fraction": round(kept, 4), "fwd_ms": round(ms, 4),
-             "fwd_tflops": round(ff / ms / 1e9, 1), "fwd_frac": round(ff / ms / 1e9 / peak, 4)}
+             "fwd_tflops": round(ff / ms / 1e9, 1), "fwd_frac": round(ff / ms / 1e9 / peak, 4),
+             "io_model": _io_model(iomodel, N, d, B * H, kept, peaks, brief=True)}
         if "bwd" in w.passes:
             do = x["do"].to(dev)
             dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
@@ -555,11 +568,11 @@ def _workloads(attn, torch, dev, stream, inputs, iomodel, peaks):
         out[name] = r
         del q, k, v, o, l
         torch.cuda.empty_cache()
-    out["sparse_16k_fine"] = _fine_masks(attn, torch, dev, stream, inputs, iomodel, peak)
+    out["sparse_16k_fine"] = _fine_masks(attn, torch, dev, stream, inputs, iomodel, peaks)
     return out
 
 
-def _fine_masks(attn, torch, dev, stream, inputs, iomodel, peak):
+def _fine_masks(attn, torch, dev, stream, inputs, iomodel, peaks):
     """The block-sparse workload's shape with one mask per head over 64-row blocks (the band and
     random off-band blocks of the 128-block workload, at half the block side): the masked entry
     points, forward and backward, credited the kept-block FLOPs."""
@@ -568,6 +581,7 @@ def _fine_masks(attn, torch, dev, stream, inputs, iomodel, peak):
     x, _ = inputs.workload_inputs(w)
     mask = inputs.band_random_mask_fine(N, B * H, seed=0)
     kept = float(mask.float().mean())
+    peak = float(peaks["bf16_tflops"])
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     dm = mask.to(dev)
     o = torch.empty_like(q)
@@ -582,7 +596,8 @@ def _fine_masks(attn, torch, dev, stream, inputs, iomodel, peak):
                                               workspace=wsp, stream=stream), torch, dev, stream)
     r = {"shape": [B, H, N, d], "mask": "per head, 64-row blocks", "kept_block_fraction": round(kept, 4),
          "fwd_ms": round(ms_f, 4), "fwd_tflops": round(ff / ms_f / 1e9, 1), "fwd_frac": round(ff / ms_f / 1e9 / peak, 4),
-         "bwd_ms": round(ms_b, 4), "bwd_tflops": round(bf / ms_b / 1e9, 1), "bwd_frac": round(bf / ms_b / 1e9 / peak, 4)}
+         "bwd_ms": round(ms_b, 4), "bwd_tflops": round(bf / ms_b / 1e9, 1), "bwd_frac": round(bf / ms_b / 1e9 / peak, 4),
+         "io_model": _io_model(iomodel, N, d, B * H, kept, peaks, brief=True)}
     del q, k, v, do, o, l, dq, dk, dv, wsp, dm
     torch.cuda.empty_cache()
     return r
@@ -619,6 +634,9 @@ def _decode(attn, torch, dev, stream, inputs, peaks):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": f"{w['name']}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} bf16 (K/V cache {2 * B * H * Nk * d * 2 / 2**30:.1f} GiB > L2)",
             "ms": round(ms, 4), "bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": float(peaks["hbm_gbs"]),
+            # the rectangular account: every element of K, V, Q read once and O, LSE written once
+            # is the whole movement, so T >= w L / beta is the bytes over the copy bandwidth
+            "time_lower_bound_ms": round(nbytes / (float(peaks["hbm_gbs"]) * 1e9) * 1e3, 4),
             "frac": round(gbs / float(peaks["hbm_gbs"]), 4), "bound": "hbm"}
 
 

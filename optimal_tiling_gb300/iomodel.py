@@ -142,9 +142,11 @@ def report(N: int, d: int, heads: int, elem_bytes: int, M: float, hbm_bytes_per_
 
     M is the fast-memory capacity in elements (the pages' model); the leading
     terms are per head and multiplied by the head count.  For a block-sparse
-    workload the sparse bound of Theorem 4.5 is evaluated with Z_input = 2 N d
-    (the non-zeros of Q and K, the operands of QK^T) and Z_QK = kept * N^2; the
-    dense forms are scaled by the kept-block fraction.  Time bounds use
+    workload the sparse bound of Theorem 4.5 is evaluated with Z_input = N d
+    (the non-zeros of one dense input matrix: the reading under which the bound
+    reduces to the dense N^2 d^2 / M and its split M = Z_input^2 / Z_QK to the
+    dense d^2, as the page says it does) and Z_QK = kept * N^2; the dense forms
+    are scaled by the kept-block fraction.  Time bounds use
     T >= max(w L / beta, F / P) with L the compulsory elements plus the leading
     term (ideal overlap; no constant is known for the Theta forms).
     """
@@ -164,7 +166,7 @@ def report(N: int, d: int, heads: int, elem_bytes: int, M: float, hbm_bytes_per_
     out["bwd_time_lower_bound_s"] = time_lower_bound(out["bwd_leading_elements"] + heads * 2 * compulsory_io(N, d),
                                                      elem_bytes, hbm_bytes_per_s, out["bwd_flops"], flops_per_s)
     if kept_fraction < 1.0:
-        z_in, z_qk = 2.0 * N * d, kept_fraction * N * N
+        z_in, z_qk = float(N * d), kept_fraction * N * N
         out["sparse_bound_elements"] = heads * sparse_io_bound(z_in, z_qk, M)
         out["sparse_regime_split_M"] = sparse_regime_split(z_in, z_qk)
     return out

@@ -71,7 +71,7 @@ def test_report_at_teaching_example():
     assert r["bwd_leading_elements"] == G["bwd_io_large"]
     assert r["fwd_time_lower_bound_s"] == max(2 * r["fwd_bound_elements"] / 1e12, G["fwd_flops"] / 1e15)
     s = iomodel.report(4096, 64, 1, 2, 65536, 1e12, 1e15, kept_fraction=0.25)
-    assert s["sparse_bound_elements"] == iomodel.sparse_io_bound(2 * 4096 * 64, 0.25 * 4096 ** 2, 65536)
+    assert s["sparse_bound_elements"] == iomodel.sparse_io_bound(4096 * 64, 0.25 * 4096 ** 2, 65536)
 
 
 def test_byte_counts_match_the_buffers_they_describe():
@@ -96,3 +96,15 @@ def test_byte_counts_match_the_buffers_they_describe():
     kv = 2 * x
     assert iomodel.fwd_kv_rescan_bytes(N, d, heads, 2, 128) == kv * (N // 128)
     assert iomodel.fwd_kv_rescan_bytes(N, d, heads, 2, 128, 0.25) == kv * (N // 128) * 0.25
+
+
+def test_report_sparse_bound_uses_the_dense_reduction():
+    """report() evaluates Theorem 4.5 with Z_input = N d and Z_QK = kept N^2: at kept = 1
+    (a mask that keeps everything, still passed as sparse) it equals the dense leading
+    term, and its split sits at d^2 whatever N is."""
+    for N, d, M in ((4096, 64, 65536.0), (16384, 128, 116736.0)):
+        almost_all = 1.0 - 1e-12
+        r = iomodel.report(N, d, 1, 2, M, 1e12, 1e15, almost_all)
+        dense = min(iomodel.fused_stream_io(N, d, M), iomodel.square_tile_io(N, d, M))
+        assert abs(r["sparse_bound_elements"] - dense) <= 1e-6 * dense
+        assert abs(r["sparse_regime_split_M"] - d * d) <= 1e-6 * d * d
