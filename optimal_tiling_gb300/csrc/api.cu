@@ -31,6 +31,7 @@ std::mutex g_mu;
 typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
 CtxGetCurrentFn g_ctx_get_current = nullptr;
 bool g_ctx_looked_up = false;
+std::mutex g_ctx_mu;  // guards the two above only (current_context runs inside g_mu's sections)
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -45,7 +46,7 @@ namespace attn {
 void *current_context() {
     CtxGetCurrentFn fn;
     {
-        std::lock_guard<std::mutex> lk(g_mu);
+        std::lock_guard<std::mutex> lk(g_ctx_mu);
         if (!g_ctx_looked_up) {
             void *f = nullptr;
             cudaDriverEntryPointQueryResult q;
@@ -124,7 +125,7 @@ attn_status check_common(int B, int H, int N, int d, attn_dtype dt) {
 }
 
 bool bf16_fwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128 || d == 256); }
-bool bf16_bwd_shape_ok(int N, int d) { return N % 128 == 0 && d == 128; }
+bool bf16_bwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
 bool bf16_matbwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
 
 attn_status launch_status(cudaError_t e) {

@@ -78,20 +78,29 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct BwdCfg {
-    static_assert(D == 128, "tcgen05 backward is built for d = 128");
-    static constexpr int kKVTile = BKV * D * 2;          // 32 KB
+    static_assert(D == 64 || D == 128, "tcgen05 backward is built for d = 64 and d = 128");
+    static constexpr int kKVTile = BKV * D * 2;          // 16 / 32 KB
     static constexpr int kKVSlab = BKV * 128;            // 16 KB: 64 columns of the K/V tile
-    static constexpr int kQTile = BQ * D * 2;            // 16 KB
+    static constexpr int kQTile = BQ * D * 2;            // 8 / 16 KB
     static constexpr int kQSlab = BQ * 128;              // 8 KB
     static constexpr int kDsTile = BKV * BQ * 2;         // 16 KB: dS^T, 128 rows x 128 B
-    static constexpr int kDqTile = BQ * D * 4;           // 32 KB fp32
+    static constexpr int kDqTile = BQ * D * 4;           // 16 / 32 KB fp32
+    // dQ^T = K^T dS^T has M = d.  At d = 64 it runs as an M = 128 product whose A rows 64..127
+    // (the second 64-element M chunk of the MN-major K^T, one leading byte offset past the
+    // first) are a zeroed region of shared memory: the accumulator then has the known M = 128
+    // layout (lane = row), rows 0..63 holding dQ^T and rows 64..127 zeros.
+    static constexpr int kZeroBytes = D == 64 ? BKV * 128 : 0;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kKVTile;
     static constexpr int kQOff = kVOff + kKVTile;
     static constexpr int kdOOff = kQOff + kStages * kQTile;
     static constexpr int kDsOff = kdOOff + kStages * kQTile;
     static constexpr int kDqOff = kDsOff + 2 * kDsTile;
-    static constexpr int kLdOff = kDqOff + kDqTile;      // per stage: L2[64], D[64]
+    static constexpr int kZeroOff = kDqOff + kDqTile;
+    static constexpr int kLdOff = kZeroOff + kZeroBytes; // per stage: L2[64], D[64]
+    // leading byte offset of K^T's second M chunk: the next 64 columns of K, or the zeros
+    static constexpr uint32_t kDqALbo = D == 64 ? (uint32_t)(kZeroOff - kKOff) : (uint32_t)kKVSlab;
+    static constexpr int kDqM = 128;                     // M of the dQ^T product
     static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
     // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull, dqfree, dpfree, kvdone, drain[3]
     static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3;
@@ -106,6 +115,7 @@ struct BwdCfg {
     // registers at the start of a block's elementwise work); dQ^T of one block
     static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 2 * BQ, kColQ = kColDP + BQ;
     static_assert(kColQ + BQ <= kTmemCols, "tensor memory budget");
+    static_assert(kDqALbo % 16 == 0 && (kDqALbo >> 4) < (1u << 14), "leading byte offset field");
 };
 
 struct BwdBars {
@@ -240,6 +250,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
     }
     if (use_bits) build_visit_bits(vwords, nq, qvisited);
+    if constexpr (C::kZeroBytes > 0) {
+        // the zero rows of the padded K^T operand (read by the tensor core: async proxy)
+        uint4 *z = reinterpret_cast<uint4 *>(sm + C::kZeroOff);
+        for (int i = tid; i < C::kZeroBytes / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -298,7 +314,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (lane == 0 && n > 0) {
             constexpr uint32_t idSP = idesc_bf16_f32(BKV, BQ, false, false);  // S^T, dP^T
             constexpr uint32_t idKV = idesc_bf16_f32(BKV, D, false, true);    // dV, dK
-            constexpr uint32_t idQ = idesc_bf16_f32(D, BQ, true, true);       // dQ^T
+            constexpr uint32_t idQ = idesc_bf16_f32(C::kDqM, BQ, true, true); // dQ^T (M padded to 128)
             bool ok = mbar_wait(bars.kv(), 0, abort_flag, p.dev_status);
             if (role < 2) {
                 // S^T_it (role 0) or dP^T_it (role 1) into buffer it & 1
@@ -352,8 +368,24 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 if (ok) mma_commit(bars.kvdone());
             } else {
+                // 64-row mask blocks: the key halves of this tile kept for query block iq (bit 0:
+                // keys 0-63, bit 1: keys 64-127).  dS is zero over a removed half, so dQ^T skips the
+                // k-steps that contract over it.  Read one block ahead, off the issue path.
+                const bool fine = hm != nullptr && mb == 64;
+                auto halves = [&](int iq) -> uint32_t {
+                    if (!fine) return 3u;
+                    const uint8_t *r = hm + (size_t)iq * mnb + 2 * kvt;
+                    return (uint32_t)(r[0] != 0) | ((uint32_t)(r[1] != 0) << 1);
+                };
+                int iq_next = n > 0 ? next_q(q_lo - 1) : 0;
+                uint32_t h_next = n > 0 ? halves(iq_next) : 3u;
                 for (int it = 0; it < n && ok; ++it) {
                     const int b = it & 1;
+                    const uint32_t h_cur = h_next;
+                    if (it + 1 < n) {
+                        iq_next = next_q(iq_next);
+                        h_next = halves(iq_next);
+                    }
                     if (!(ok = mbar_wait(bars.pfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
                     // one dQ^T buffer: the drain warps must have read dQ^T of block it-1
                     if (it >= 1 && !(ok = mbar_wait(bars.dqfree(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status)))
@@ -361,10 +393,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tc_fence_after();
                     const uint32_t dsb = sDs + b * C::kDsTile;
                     // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous)
+                    bool first = true;
 #pragma unroll
-                    for (int ks = 0; ks < BKV / 16; ++ks)
-                        mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + ks * 2048, C::kKVSlab, 1024),
-                               smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
+                    for (int ks = 0; ks < BKV / 16; ++ks) {
+                        if (!((h_cur >> (ks >> 2)) & 1u)) continue;
+                        mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + ks * 2048, C::kDqALbo, 1024),
+                               smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, first ? 0u : 1u);
+                        first = false;
+                    }
                     mma_commit(bars.dsfree(b));
                     mma_commit(bars.dqfull());
                 }
@@ -523,7 +559,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // Every drain thread runs the same sequence of named barriers whatever happens:
         // after a failed (timed-out) wait the work is skipped but the barriers are kept,
         // and the CTA abort flag makes every later wait return at once.
-        const int t = tid - kDqWarp0 * 32;  // 0..127 = d index (tensor memory lane)
+        const int t = tid - kDqWarp0 * 32;  // 0..127 = d index (tensor memory lane); rows >= D are padding
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         float *dq_gen = reinterpret_cast<float *>(sm + C::kDqOff);
         bool alive = true;
@@ -551,7 +587,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             auto stage = [&](const uint32_t(&r)[32], int hq) {
                 if (t == 0) bulk_wait_read_but_one();
                 named_bar_sync(1, 128);
-                if (ok) {
+                if (ok && t < D) {
                     float *dst = dq_gen + hq * 32 * D;
 #pragma unroll
                     for (int q = 0; q < 32; ++q) dst[q * D + t] = __uint_as_float(r[q]);
@@ -702,6 +738,7 @@ cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O
                             float *kvacc, int split_tiles, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
     switch (p.d) {
+        case 64: return launch_d<64>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, kvacc, split_tiles, st);
         case 128: return launch_d<128>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, kvacc, split_tiles, st);
         default: return cudaErrorNotSupported;
     }

@@ -224,9 +224,27 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 mma_commit(bars.sfull(it & 1));
                 return true;
             };
+            // 64-row mask blocks: the 64-key halves of a visited block that some row of this tile
+            // keeps (bit 0: keys 0-63, bit 1: keys 64-127).  The softmax writes P = 0 over a half
+            // that no row keeps, so PV skips its k-steps (adding those zero products would change
+            // nothing).  Read one block ahead, so that the loads are off the issue path.
+            const bool fine = hm != nullptr && mb == 64;
+            auto halves = [&](int j) -> uint32_t {
+                if (!fine) return 3u;
+                const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
+                return (uint32_t)((r0[0] | r1[0]) != 0) | ((uint32_t)((r0[1] | r1[1]) != 0) << 1);
+            };
+            int j_next = next_block(-1);
+            uint32_t h_next = halves(j_next);
+            bool o_started = false;  // the first PV product initialises O
             if (ok) ok = issue_s(0);
             for (int it = 0; it < n && ok; ++it) {
-                if (it + 1 < n && !(ok = issue_s(it + 1))) break;
+                const uint32_t h_cur = h_next;
+                if (it + 1 < n) {
+                    j_next = next_block(j_next);
+                    h_next = halves(j_next);
+                    if (!(ok = issue_s(it + 1))) break;
+                }
                 const int s = it % S;
                 // V_it was loaded long ago: check it before waiting for P_it, so that only P_it is
                 // waited for on the path from the softmax to PV
@@ -236,9 +254,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
                 const uint32_t vb = sV + s * C::kTileBytes;
 #pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks)
+                for (int ks = 0; ks < BN / 16; ++ks) {
+                    if (!((h_cur >> (ks >> 2)) & 1u)) continue;
                     mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO,
-                           (it > 0 || ks > 0) ? 1u : 0u);
+                           o_started ? 1u : 0u);
+                    o_started = true;
+                }
                 mma_commit(bars.vempty(s));
                 mma_commit(bars.odone());
             }
@@ -767,6 +788,472 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------------------
+// One query tile, two softmax warpgroups ("split key blocks"): the key blocks the
+// tile visits are dealt out in turn, even-numbered visits to warpgroup 0 (warps
+// 0-3) and odd-numbered ones to warpgroup 1 (warps 4-7).  Each warpgroup keeps its
+// own S buffer (128 columns), running max m_x, sum l_x and O accumulator O_x (d
+// columns) in tensor memory, and the two partial states are merged at the end with
+// the online-softmax rule of the page's section "Softmax without storing the score
+// matrix": m = max(m_0, m_1), l = sum_x 2^(m_x - m) l_x, O = sum_x 2^(m_x - m) O_x / l.
+// The MMA order is the two-tile kernel's with "tile X" read as "warpgroup X":
+//     PV_0(i), S_0(i+2), PV_1(i+1), S_1(i+3), ...
+// so the tensor core works on one warpgroup's block while the other warpgroup's
+// softmax runs, whatever the mask (each warpgroup's next S waits only for its K
+// block).  Because one thread's MMAs complete in issue order, "S_x(i+2) done" means
+// "PV_x(i) done", so the softmax may rescale O_x as soon as it sees S_x(i+2).  Each
+// K/V block serves one warpgroup.  Used under block masks and for N % 256 != 0 at
+// d = 64 and 128.
+constexpr int kSplThreads = 320;
+constexpr int kSplTmaWarp = 8;
+constexpr int kSplMmaWarp = 9;
+
+template <int D>
+struct SplCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kStages = D == 64 ? 6 : 3;
+    static constexpr int kTileBytes = BM * D * 2;
+    static constexpr int kChunkBytes = BM * 128;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kTileBytes;
+    static constexpr int kVOff = kKOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone[2], drain (the
+    // two-tile kernel's barrier layout)
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kMaxMaskWords = 256;
+    static constexpr int kBitsOff = kMiscOff + 64;
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;
+    // the merge exchanges (m, l) of both warpgroups through the first K stage, idle by then
+    static constexpr int kStatOff = kKOff;
+    static constexpr uint32_t kOCol0 = 256;
+    static_assert(2 * 2 * BM * 4 <= kTileBytes, "merge statistics fit one K stage");
+    static_assert(kOCol0 + 2 * D <= kTmemCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kSplThreads, 1)
+fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const Problem p, __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
+    using C = SplCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const PPBars bars{smem_addr(sm + C::kBarOff), S};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, head = blockIdx.y;
+    const int nb = p.N / BN;
+    const uint8_t *hm = p.head_mask(head);
+    const int mb = p.mask_block, mnb = p.mask_nb();
+    uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
+    const int nwords = (nb + 31) >> 5;
+    const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
+    const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bars.q(), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bars.kfull(s), 1);
+            mbar_init(bars.kempty(s), 1);
+            mbar_init(bars.vfull(s), 1);
+            mbar_init(bars.vempty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bars.sfull(x), 1);
+            mbar_init(bars.pfull(x), 128);
+            mbar_init(bars.odone(x), 1);
+        }
+        mbar_init(bars.drain(), 1);
+        fence_barrier_init();
+        // the Q tile is needed whatever the mask says: start its load before the mask is read
+        mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
+    }
+    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
+    if (warp == kSplMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const VisitBits vb{vwords, nwords};
+    int n = nb;  // key blocks this query tile visits
+    if (use_bits) {
+        n = vb.count();
+    } else if (hm != nullptr) {  // rows longer than the bit set: read the mask directly
+        n = 0;
+        for (int j = 0; j < nb; ++j) n += visited(hm, mb, mnb, tile, j) ? 1 : 0;
+    }
+    // the visited key block after j (callers ask only while one remains)
+    auto next_block = [&](int j) -> int {
+        if (hm == nullptr) return j + 1;
+        if (use_bits) return vb.next(j);
+        do {
+            ++j;
+        } while (!visited(hm, mb, mnb, tile, j));
+        return j;
+    };
+    const bool fine = hm != nullptr && mb == 64;
+
+    if (warp == kSplTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            int j = -1;
+            for (int it = 0; it < n; ++it) {
+                j = next_block(j);
+                const int s = it % S;
+                const uint32_t ph = (uint32_t)(it / S) & 1u;
+                const int krow = head * p.N + j * BN;
+                if (it >= S && !mbar_wait(bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(bars.kfull(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sK + s * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(s));
+                if (it >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
+            }
+        }
+    } else if (warp == kSplMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
+            const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+            // 64-row mask blocks: the 64-key halves of a visit's block that some row of the tile
+            // keeps (bit 0: keys 0-63, bit 1: keys 64-127); PV skips the k-steps of a half no row
+            // keeps (its P is zero).  hist holds them two bits per visit, newest in the low bits.
+            auto halves = [&](int j) -> uint32_t {
+                if (!fine) return 3u;
+                const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
+                return (uint32_t)((r0[0] | r1[0]) != 0) | ((uint32_t)((r0[1] | r1[1]) != 0) << 1);
+            };
+            int j_s = -1;        // block of the newest S issued
+            uint32_t hist = 0;
+            bool started0 = false, started1 = false;  // the first PV product of a warpgroup initialises O_x
+            // S_x(it) = Q K_it^T into warpgroup x = it & 1's S buffer
+            auto issue_s = [&](int it) -> bool {
+                const int s = it % S, x = it & 1;
+                j_s = next_block(j_s);
+                hist = (hist << 2) | halves(j_s);
+                if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
+                tc_fence_after();
+                const uint32_t kb = sK + s * C::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                    mma_ss(tmem + PPCfg<D>::scol(x), smem_desc_sw128(sQ + off, 16, 1024),
+                           smem_desc_sw128(kb + off, 16, 1024), idS, ks > 0);
+                }
+                mma_commit(bars.kempty(s));
+                mma_commit(bars.sfull(x));
+                return true;
+            };
+            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
+            if (ok) ok = issue_s(0);
+            if (ok && n > 1) ok = issue_s(1);
+            for (int it = 0; it < n && ok; ++it) {
+                const int s = it % S, x = it & 1;
+                // S has been issued for visits 0 .. min(it + 1, n - 1): this visit's halves sit one
+                // field up when the next visit's S is already issued
+                const uint32_t h_cur = (it + 1 < n ? hist >> 2 : hist) & 3u;
+                // V_it and K_{it+2} were loaded long ago: check them before waiting for P, so that
+                // only P_x(it) is waited for on the path from the softmax to PV
+                if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                if (it + 2 < n && !(ok = mbar_wait(bars.kfull((it + 2) % S), (uint32_t)((it + 2) / S) & 1u,
+                                                   abort_flag, p.dev_status)))
+                    break;
+                if (!(ok = mbar_wait(bars.pfull(x), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                const uint32_t vb_ = sV + s * C::kTileBytes;
+#pragma unroll
+                bool started = x ? started1 : started0;
+                for (int ks = 0; ks < BN / 16; ++ks) {
+                    if (!((h_cur >> (ks >> 2)) & 1u)) continue;
+                    mma_ts(tmem + C::kOCol0 + x * D, tmem + PPCfg<D>::scol(x) + ks * 8,
+                           smem_desc_sw128(vb_ + ks * 2048, C::kChunkBytes, 1024), idO, started ? 1u : 0u);
+                    started = true;
+                }
+                if (x) started1 = started;
+                else started0 = started;
+                mma_commit(bars.vempty(s));
+                if (it + 2 < n) {
+                    if (!(ok = issue_s(it + 2))) break;
+                } else {
+                    mma_commit(bars.odone(x));
+                }
+            }
+            if (!ok) {
+                // let every MMA already issued finish before tensor memory is released
+                mma_commit(bars.drain());
+                mbar_wait(bars.drain(), 0, abort_flag, p.dev_status);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax, one warpgroup per parity
+        const int x = warp >> 2;  // visits x, x + 2, x + 4, ...
+        const int r = tid & 127;  // row within the tile == tensor memory lane
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t scol = lane_base + PPCfg<D>::scol(x);
+        const uint32_t ocol = lane_base + C::kOCol0 + x * D;
+        const float sl2 = fabsf(p.scale) * kLog2e;  // S holds sign(s) Q K^T
+        // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each 64-key half of a
+        // visited block is kept or removed for the whole warp
+        const uint8_t *wmask = fine ? hm + (size_t)(2 * tile + (warp & 3) / 2) * mnb : nullptr;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        int vis = -1, jv = -1;  // the visit and block reached so far (fine masks)
+        for (int it = x, lk = 0; it < n; it += 2, ++lk) {
+            bool keep_lo = true, keep_hi = true;
+            if (fine) {
+                while (vis < it) {
+                    jv = next_block(jv);
+                    ++vis;
+                }
+                keep_lo = wmask[2 * jv] != 0;
+                keep_hi = wmask[2 * jv + 1] != 0;
+            }
+            ok = mbar_wait(bars.sfull(x), (uint32_t)lk & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            // S in two 64-column halves, so that only 64 scores are live at a time (as in the
+            // two-tile kernel): the max of each kept half, the exps of the high half while it is
+            // in registers, then the low half loaded again; P of the high half (columns 32..63,
+            // which hold S of keys 32..63) is written only after that reload
+            uint32_t rr[2][32];
+            float mlo = -INFINITY, mhi = -INFINITY;
+            if (keep_lo) {
+                tmem_ld32(scol + 0, rr[0]);
+                tmem_ld32(scol + 32, rr[1]);
+                tmem_wait_ld();
+                reg_fence(rr[0]);
+                reg_fence(rr[1]);
+                float mx4[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
+                    mx4[c] = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+#pragma unroll
+                    for (int t = 1; t < 8; ++t)
+                        mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+                }
+                mlo = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+            }
+            if (keep_hi) {
+                tmem_ld32(scol + 64, rr[0]);
+                tmem_ld32(scol + 96, rr[1]);
+                tmem_wait_ld();
+                reg_fence(rr[0]);
+                reg_fence(rr[1]);
+                float mx4[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
+                    mx4[c] = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+#pragma unroll
+                    for (int t = 1; t < 8; ++t)
+                        mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+                }
+                mhi = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+            }
+            const float mx = fmaxf(mlo, mhi);
+            // a warp with nothing kept so far keeps m_used = -inf
+            const float m_new = mx == -INFINITY ? m_used : fmaxf(m_used, mx * sl2);
+            float alpha = 1.f;
+            if (m_new > m_used + kRescaleThreshold) {
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+            }
+            // O_x is complete up to this warpgroup's previous block (S_x(it) was issued after
+            // PV_x(it - 2)), and PV_x(it) waits for this warpgroup: rescale it here
+            if (lk > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(ocol + c0, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    tmem_st32(ocol + c0, o);
+                }
+            }
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m_used, -m_used);
+            uint64_t sumq[4];
+            uint32_t pkh[2][16];
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                sumq[2 + qq] = f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    if (!keep_hi) {
+                        pkh[qq][t] = 0u;
+                        continue;
+                    }
+                    const uint64_t x2 =
+                        f2_fma(f2_pack(__uint_as_float(rr[qq][2 * t]), __uint_as_float(rr[qq][2 * t + 1])), sl2x2,
+                               negm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[2 + qq] = f2_add(sumq[2 + qq], f2_pack(y0, y1));
+                    pkh[qq][t] = pack_bf16(y0, y1);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) sumq[q] = f2_pack(0.f, 0.f);
+            if (keep_lo && keep_hi) {  // (with the high half removed, rr still holds the low half)
+                tmem_ld32(scol + 0, rr[0]);
+                tmem_ld32(scol + 32, rr[1]);
+                tmem_wait_ld();
+                reg_fence(rr[0]);
+                reg_fence(rr[1]);
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    if (!keep_lo) {
+                        pk[t] = 0u;
+                        continue;
+                    }
+                    const uint64_t x2 =
+                        f2_fma(f2_pack(__uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1])), sl2x2,
+                               negm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[q] = f2_add(sumq[q], f2_pack(y0, y1));
+                    pk[t] = pack_bf16(y0, y1);
+                }
+                tmem_st16(scol + q * 16, pk);
+            }
+            tmem_st16(scol + 32, pkh[0]);
+            tmem_st16(scol + 48, pkh[1]);
+            float rs0, rs1;
+            f2_unpack(f2_add(f2_add(sumq[0], sumq[1]), f2_add(sumq[2], sumq[3])), rs0, rs1);
+            l = l * alpha + (rs0 + rs1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bars.pfull(x));
+        }
+        if (n == 0) {
+            // every key block removed: O = 0, LSE = -inf (warpgroup 0 writes the rows)
+            if (x == 0) {
+                const size_t grow = (size_t)row0 + r;
+                uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
+                for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
+                LSE[grow] = -INFINITY;
+            }
+        } else {
+            // both warpgroups' last PV: after these every MMA of the tile has completed, so the Q
+            // tile and the K ring are idle (a warpgroup with no block of its own, n == 1, must not
+            // touch the K ring while the other's S still reads it)
+            if (ok) {
+                for (int y = 0; y < 2 && ok; ++y)
+                    if (n > y) ok = mbar_wait(bars.odone(y), 0, abort_flag, p.dev_status);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+            }
+            // Merge.  Both warpgroups publish (m_x, l_x) in the idle K ring and meet at a named
+            // barrier (whatever `ok` says, so that no warp waits there for one that gave up).
+            // Warpgroup x then merges columns [x d/2, (x + 1) d/2) of O for its rows into the Q
+            // tile, in the 128-byte-swizzled layout of the 64-column TMA box.
+            float *stat = reinterpret_cast<float *>(sm + C::kStatOff);
+            stat[(2 * x) * BM + r] = m_used;
+            stat[(2 * x + 1) * BM + r] = l;
+            named_bar_sync(1, 256);
+            const float m0 = stat[r], l0 = stat[BM + r], m1 = stat[2 * BM + r], l1 = stat[3 * BM + r];
+            const float m = fmaxf(m0, m1);
+            // a warpgroup with no kept score in this row (or no block at all: n == 1 leaves O_1
+            // unwritten) contributes nothing; select rather than multiply, since O_x is then
+            // undefined
+            const float a0 = l0 > 0.f ? ex2(m0 - m) : 0.f;
+            const float a1 = l1 > 0.f ? ex2(m1 - m) : 0.f;
+            const float lt = a0 * l0 + a1 * l1;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float w0 = a0 * inv, w1 = a1 * inv;
+            uint8_t *stage = sm + C::kQOff;
+            if (ok) {
+                const uint32_t o0col = lane_base + C::kOCol0, o1col = lane_base + C::kOCol0 + D;
+#pragma unroll 1
+                for (int c0 = x * (D / 2); c0 < (x + 1) * (D / 2); c0 += 32) {
+                    uint32_t u0[32], u1[32];
+                    tmem_ld32(o0col + c0, u0);
+                    tmem_ld32(o1col + c0, u1);
+                    tmem_wait_ld();
+                    reg_fence(u0);
+                    reg_fence(u1);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const float v0 = (w0 != 0.f ? w0 * __uint_as_float(u0[2 * t]) : 0.f) +
+                                         (w1 != 0.f ? w1 * __uint_as_float(u1[2 * t]) : 0.f);
+                        const float v1 = (w0 != 0.f ? w0 * __uint_as_float(u0[2 * t + 1]) : 0.f) +
+                                         (w1 != 0.f ? w1 * __uint_as_float(u1[2 * t + 1]) : 0.f);
+                        pk[t] = pack_bf16(v0, v1);
+                    }
+                    uint8_t *slab = stage + (c0 >> 6) * C::kChunkBytes + r * 128;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int u = ((c0 & 63) >> 3) + v;  // 16-byte unit within the 128-byte row
+                        *reinterpret_cast<uint4 *>(slab + ((u ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                if (x == 0) LSE[(size_t)row0 + r] = lt > 0.f ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+                fence_proxy_async_smem();
+            }
+            named_bar_sync(1, 256);
+            if (tid == 0 && !*abort_flag) {
+                const uint32_t src = smem_addr(stage);
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&tmO, c * 64, row0, src + c * C::kChunkBytes);
+                bulk_commit();
+                bulk_wait_all();
+            }
+        }
+    }
+
+    // a tile that visits no key block still received its Q tile: let that copy land first
+    if (n == 0 && tid == 0) mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kSplMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_split(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
+    auto kern = fwd_bf16_split_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SplCfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.N / BM, p.B * p.H);
+    {
+        ProfScope prof_("fwd_bf16", st);
+        kern<<<grid, kSplThreads, SplCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p,
+                                                                static_cast<__nv_bfloat16 *>(O), LSE);
+    }
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_pp(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
     auto kern = fwd_bf16_pp_kernel<D>;
@@ -799,16 +1286,14 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
 
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
-#ifndef ATTN_FWD_NO_PINGPONG
-    // two query tiles per CTA when both tiles visit every key block
-    if (p.mask == nullptr && p.N % (2 * BM) == 0) {
-        if (p.d == 64) return launch_pp<64>(p, maps, O, LSE, st);
-        if (p.d == 128) return launch_pp<128>(p, maps, O, LSE, st);
-    }
-#endif
+    // d = 64, 128: two query tiles per CTA when both visit every key block; otherwise (a block
+    // mask, or N % 256 != 0) one tile per CTA with its visited blocks split between two
+    // warpgroups.  d = 256 (two S buffers and O fill tensor memory): one tile, one warpgroup.
     switch (p.d) {
-        case 64: return launch_d<64>(p, maps, O, LSE, st);
-        case 128: return launch_d<128>(p, maps, O, LSE, st);
+        case 64: return (p.mask == nullptr && p.N % (2 * BM) == 0) ? launch_pp<64>(p, maps, O, LSE, st)
+                                                                  : launch_split<64>(p, maps, O, LSE, st);
+        case 128: return (p.mask == nullptr && p.N % (2 * BM) == 0) ? launch_pp<128>(p, maps, O, LSE, st)
+                                                                   : launch_split<128>(p, maps, O, LSE, st);
         case 256: return launch_d<256>(p, maps, O, LSE, st);
         default: return cudaErrorNotSupported;
     }

@@ -56,7 +56,7 @@ def _s(d: int) -> float:
 # (the throughput target is stated at N=16384, d=128 without a mask).
 WORKLOADS = {
     "fp32_small": Workload("fp32_small", 1, 1, 256, 64, "f32", 1.0, passes=("fwd", "bwd")),
-    "teaching": Workload("teaching", 4, 16, 4096, 64, "bf16", _s(64)),
+    "teaching": Workload("teaching", 4, 16, 4096, 64, "bf16", _s(64), passes=("fwd", "bwd")),
     "dsweep_d64": Workload("dsweep_d64", 2, 16, 8192, 64, "bf16", _s(64), passes=("fwd", "mat")),
     "dsweep_d128": Workload("dsweep_d128", 2, 16, 8192, 128, "bf16", _s(128), passes=("fwd", "mat")),
     "dsweep_d256": Workload("dsweep_d256", 2, 16, 8192, 256, "bf16", _s(256), passes=("fwd", "mat")),

@@ -146,7 +146,7 @@ def test_masked_entry_point_checks(lib):
         assert bwd(block=blk) == attn.ATTN_ERR_INVALID_ARG
     assert fwd(stride=-1) == attn.ATTN_ERR_INVALID_ARG
     assert bwd(stride=-64) == attn.ATTN_ERR_INVALID_ARG
-    assert bwd(d=64) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(d=96) == attn.ATTN_ERR_UNSUPPORTED
     bm = attn.BlockMask(FAKE, 64, 0)
     assert lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 200, 64, 1.0, attn.ATTN_DTYPE_BF16,
                                ctypes.byref(bm), None) == attn.ATTN_ERR_UNSUPPORTED

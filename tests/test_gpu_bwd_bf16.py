@@ -43,17 +43,19 @@ def _check_full(x, scale, oracle_mod, mask=None):
     return dq, dk, dv
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N,BH", [(128, (1, 1)), (256, (1, 3)), (384, (3, 1)), (1024, (1, 2))])
-def test_small_shapes(oracle_mod, N, BH):
+def test_small_shapes(oracle_mod, N, BH, d):
     B, H = BH
-    x = inputs.make_inputs(B, H, N, 128, torch.bfloat16, seed=N + 1)
-    _check_full(x, 1.0 / math.sqrt(128), oracle_mod)
+    x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=N + d + 1)
+    _check_full(x, 1.0 / math.sqrt(d), oracle_mod)
 
 
-def test_block_masks_and_empty_rows(oracle_mod):
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_masks_and_empty_rows(oracle_mod, d):
     N = 768
-    x = inputs.make_inputs(1, 2, N, 128, torch.bfloat16, seed=21)
-    s = 1.0 / math.sqrt(128)
+    x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=21 + d)
+    s = 1.0 / math.sqrt(d)
     _check_full(x, s, oracle_mod, inputs.block_diagonal_mask(N))
     _check_full(x, s, oracle_mod, inputs.random_block_mask(N, seed=6, p=0.3))
     m = torch.zeros((6, 6), dtype=torch.uint8)
@@ -66,11 +68,12 @@ def test_block_masks_and_empty_rows(oracle_mod):
     assert np.all(dk[:, :, 0:128] == 0) and np.all(dv[:, :, 256:512] == 0)
 
 
-def test_gradient_invariants():
+@pytest.mark.parametrize("d", [64, 128])
+def test_gradient_invariants(d):
     """Rows of P sum to one: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i."""
     N = 1024
-    x = inputs.make_inputs(1, 1, N, 128, torch.bfloat16, seed=22)
-    dq, dk, dv = _fwd_bwd(x, 1.0 / math.sqrt(128))
+    x = inputs.make_inputs(1, 1, N, d, torch.bfloat16, seed=22 + d)
+    dq, dk, dv = _fwd_bwd(x, 1.0 / math.sqrt(d))
     dO = x["do"].double().numpy()[0, 0]
     sk = np.abs(dk[0, 0].sum(axis=0))
     assert np.max(sk) <= 2e-2 * np.sqrt(N) * np.sqrt(np.mean(dk ** 2))
@@ -92,7 +95,7 @@ def _sample(n, N, seed):
     return np.unique(np.concatenate([[0, N - 1], r.integers(0, N, n - 2)])).astype(np.int32)
 
 
-@pytest.mark.parametrize("name", ["bwd_d128", "sparse_16k", "dense_16k"])
+@pytest.mark.parametrize("name", ["teaching", "bwd_d128", "sparse_16k", "dense_16k"])
 def test_full_size_workloads_sampled(oracle_mod, name):
     """Full-size workloads in the bench's launch configuration; the oracle computes
     sampled gradient rows of the first and the last head: dQ rows (one query row each)
@@ -117,7 +120,8 @@ def test_full_size_workloads_sampled(oracle_mod, name):
     assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
 
 
-def test_last_wave_split_matches_unsplit(oracle_mod):
+@pytest.mark.parametrize("d", [64, 128])
+def test_last_wave_split_matches_unsplit(oracle_mod, d):
     """A dense shape whose last wave is split into query halves (the SM count does not
     divide the 128-key tiles and the remainder is at most half the SMs).  With r tiles
     per head and r dividing the SM count, the split tiles are exactly the last head.
@@ -126,9 +130,9 @@ def test_last_wave_split_matches_unsplit(oracle_mod):
     to a few bf16 roundings, and with the oracle on sampled rows."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     r = max(t for t in range(1, sms // 4 + 1) if sms % t == 0)
-    H, N, d = sms // r + 1, 128 * r, 128
+    H, N = sms // r + 1, 128 * r
     s = 1.0 / math.sqrt(d)
-    x = inputs.make_inputs(1, H, N, d, torch.bfloat16, seed=31)
+    x = inputs.make_inputs(1, H, N, d, torch.bfloat16, seed=31 + d)
     q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
     o, lse = attn.attn_fwd(q, k, v, s)
     lib = attn.load()

@@ -95,10 +95,11 @@ def test_bf16_forward_per_head_masks(oracle_mod, N, d, block):
     assert np.all(O[np.isneginf(Lr)] == 0)
 
 
-@pytest.mark.parametrize("N,block", [(512, 64), (768, 128), (384, 64)])
-def test_bf16_backward_per_head_masks(oracle_mod, N, block):
-    B, H, d = 1, 2, 128
-    x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=3 * N + block)
+@pytest.mark.parametrize("N,block,d", [(512, 64, 128), (768, 128, 128), (384, 64, 128), (512, 64, 64),
+                                       (768, 128, 64)])
+def test_bf16_backward_per_head_masks(oracle_mod, N, block, d):
+    B, H = 1, 2
+    x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=3 * N + block + d)
     mask = _masks(B * H, N, block, seed=5 * block)
     scale = 1.0 / math.sqrt(d)
     o, lse = _fwd(x, scale, mask, block)
