@@ -60,26 +60,33 @@ struct FwdCfg {
     // K/V ring depth: as deep as the shared memory allows (block-sparse masks scatter the
     // key blocks a tile visits, so their loads miss L2 and need the latency covered)
     static constexpr int kStages = D == 64 ? 6 : (D == 128 ? 3 : 1);
-    // exps per 8 pairs evaluated by the FMA-pipe polynomial instead of MUFU
-#ifdef ATTN_FWD_POLY_PAIRS
-    static constexpr int kPolyPairs = ATTN_FWD_POLY_PAIRS;
-#else
-    static constexpr int kPolyPairs = 0;  // measured: every split above 0 is slower on GB300
-#endif
+    // exps per 8 pairs evaluated by the FMA-pipe polynomial instead of MUFU (measured on this
+    // kernel: every split above 0 was slower)
+    static constexpr int kPolyPairs = 0;
     static constexpr int kTileBytes = BM * D * 2;              // Q tile == K tile == V tile bytes
     static constexpr int kChunkBytes = BM * 128;               // one 64-column slab of a tile
+    // d = 256: one K and one V tile (64 KB each) would fit beside Q, so V of the next block could
+    // load only after the current PV; instead K and V stream through a ring of kPieces 32 KB
+    // pieces, consumed in tensor-core order: K of a block in two d-halves (128 keys x 128
+    // columns), V in two 64-key halves (64 keys x 256 columns)
+    static constexpr bool kRing = D == 256;
+    static constexpr int kPieces = 5;
+    static constexpr int kPieceBytes = 32768;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kTileBytes;
+    static constexpr int kKOff = kQOff + kTileBytes;           // ring base when kRing
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
+    static constexpr int kBarOff = kRing ? kKOff + kPieces * kPieceBytes : kVOff + kStages * kTileBytes;
+    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain (ring: S =
+    // kPieces, and kfull / kempty are a piece's full / empty barriers)
+    static constexpr int kBarStages = kRing ? kPieces : kStages;
+    static constexpr int kNumBars = 1 + 4 * kBarStages + 2 + 2 + 1 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // visited key blocks as a bit set: masks with up to 32 * kMaxMaskWords blocks per row
     static constexpr int kMaxMaskWords = 256;
     static constexpr int kBitsOff = kMiscOff + 64;
     static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
     static_assert(kChunkBytes == 16384, "slab layout");
+    static_assert(!kRing || (BN * 128 * 2 == kPieceBytes && (BN / 2) * D * 2 == kPieceBytes), "piece sizes");
     static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
@@ -108,16 +115,28 @@ __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int 
     return (r0[0] | r0[1] | r1[0] | r1[1]) != 0;
 }
 
+// 2^x of a pair of exponents: pair t of a run takes the FMA-pipe polynomial when t % 8 is
+// below POLY, MUFU ex2 otherwise (POLY = 0: always MUFU).
+template <int POLY>
+__device__ __forceinline__ uint64_t exp2_pair(uint64_t x2, int t) {
+    if (POLY > 0 && (t & 7) < POLY) return exp2_poly_pair(x2);
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    return f2_pack(ex2(x0), ex2(x1));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
-                __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                const __grid_constant__ CUtensorMap tmV64, const Problem p, __nv_bfloat16 *__restrict__ O,
+                float *__restrict__ LSE) {
     using C = FwdCfg<D>;
     constexpr int S = C::kStages;
+    constexpr int NP = C::kPieces;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Bars bars{smem_addr(sm + C::kBarOff), S};
+    const Bars bars{smem_addr(sm + C::kBarOff), C::kBarStages};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
 
@@ -135,7 +154,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(bars.q(), 1);
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < C::kBarStages; ++s) {
             mbar_init(bars.kfull(s), 1);
             mbar_init(bars.kempty(s), 1);
             mbar_init(bars.vfull(s), 1);
@@ -179,7 +198,45 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         return j;
     };
 
-    if (warp == kTmaWarp) {
+    if (warp == kTmaWarp && C::kRing) {
+        // ------------------------------------------------------------ producer (piece ring)
+        // The tensor core's order is S(0), S(1), PV(0), S(2), PV(1), ..., PV(n-1), so pieces are
+        // loaded in the order K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1); piece q
+        // goes to slot q % NP once the MMAs of piece q - NP have released it.
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV64);
+            int q = 0;
+            auto load = [&](bool is_v, int blk) -> bool {
+                const int krow = head * p.N + blk * BN;
+                for (int h = 0; h < 2; ++h, ++q) {
+                    const int slot = q % NP;
+                    if (q >= NP && !mbar_wait(bars.kempty(slot), ((uint32_t)(q / NP) & 1u) ^ 1u, abort_flag,
+                                              p.dev_status))
+                        return false;
+                    const uint32_t full = bars.kfull(slot), dst = sK + slot * C::kPieceBytes;
+                    mbar_arrive_expect_tx(full, C::kPieceBytes);
+                    if (!is_v) {  // K, columns 128 h .. 128 h + 127: two 128-row boxes
+                        for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * C::kChunkBytes, &tmK, (2 * h + c) * 64, krow, full);
+                    } else {      // V, keys 64 h .. 64 h + 63: four 64-row boxes
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_2d(dst + c * (C::kPieceBytes / C::kChunks), &tmV64, c * 64, krow + 64 * h, full);
+                    }
+                }
+                return true;
+            };
+            int jk = next_block(-1), jv = jk;
+            bool ok = load(false, jk);
+            for (int it = 0; it < n && ok; ++it) {
+                if (it + 1 < n) {
+                    jk = next_block(jk);
+                    if (!(ok = load(false, jk))) break;
+                }
+                if (!(ok = load(true, jv))) break;
+                if (it + 1 < n) jv = next_block(jv);
+            }
+        }
+    } else if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmK);
@@ -207,20 +264,39 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
+            int q = 0;  // next piece of the ring (the producer's order)
             // S_it = Q K_it^T into S buffer (it & 1)
             auto issue_s = [&](int it) -> bool {
-                const int s = it % S;
-                if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
-                tc_fence_after();
                 const uint32_t dcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
-                const uint32_t kb = sK + s * C::kTileBytes;
+                if constexpr (C::kRing) {
+                    for (int h = 0; h < 2; ++h, ++q) {  // d-half h of K_it
+                        const int slot = q % NP;
+                        if (!mbar_wait(bars.kfull(slot), (uint32_t)(q / NP) & 1u, abort_flag, p.dev_status))
+                            return false;
+                        tc_fence_after();
+                        const uint32_t kb = sK + slot * C::kPieceBytes;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-                    mma_ss(dcol, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idS,
-                           ks > 0);
+                        for (int k8 = 0; k8 < 8; ++k8) {
+                            const int ks = 8 * h + k8;
+                            mma_ss(dcol, smem_desc_sw128(sQ + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024),
+                                   smem_desc_sw128(kb + (k8 >> 2) * C::kChunkBytes + (k8 & 3) * 32, 16, 1024), idS,
+                                   ks > 0);
+                        }
+                        mma_commit(bars.kempty(slot));
+                    }
+                } else {
+                    const int s = it % S;
+                    if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
+                    tc_fence_after();
+                    const uint32_t kb = sK + s * C::kTileBytes;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                        mma_ss(dcol, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idS,
+                               ks > 0);
+                    }
+                    mma_commit(bars.kempty(s));
                 }
-                mma_commit(bars.kempty(s));
                 mma_commit(bars.sfull(it & 1));
                 return true;
             };
@@ -245,22 +321,51 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     h_next = halves(j_next);
                     if (!(ok = issue_s(it + 1))) break;
                 }
-                const int s = it % S;
-                // V_it was loaded long ago: check it before waiting for P_it, so that only P_it is
-                // waited for on the path from the softmax to PV
-                if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
-                if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
-                tc_fence_after();
                 const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
-                const uint32_t vb = sV + s * C::kTileBytes;
+                if constexpr (C::kRing) {
+                    // V_it's two 64-key halves are pieces q and q + 1; check both before P_it
+                    const int slot0 = q % NP, slot1 = (q + 1) % NP;
+                    if (!(ok = mbar_wait(bars.kfull(slot0), (uint32_t)(q / NP) & 1u, abort_flag, p.dev_status))) break;
+                    if (!(ok = mbar_wait(bars.kfull(slot1), (uint32_t)((q + 1) / NP) & 1u, abort_flag,
+                                         p.dev_status)))
+                        break;
+                    if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status)))
+                        break;
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks) {
-                    if (!((h_cur >> (ks >> 2)) & 1u)) continue;
-                    mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO,
-                           o_started ? 1u : 0u);
-                    o_started = true;
+                    for (int h = 0; h < 2; ++h) {
+                        const int slot = h ? slot1 : slot0;
+                        const uint32_t vb = sK + slot * C::kPieceBytes;  // keys 64 h .. 64 h + 63 of V_it
+                        if ((h_cur >> h) & 1u) {
+#pragma unroll
+                            for (int k4 = 0; k4 < 4; ++k4) {
+                                mma_ts(tmem + kOCol, pcol + (4 * h + k4) * 8,
+                                       smem_desc_sw128(vb + k4 * 2048, C::kPieceBytes / C::kChunks, 1024), idO,
+                                       o_started ? 1u : 0u);
+                                o_started = true;
+                            }
+                        }
+                        mma_commit(bars.kempty(slot));
+                    }
+                    q += 2;
+                } else {
+                    const int s = it % S;
+                    // V_it was loaded long ago: check it before waiting for P_it, so that only P_it
+                    // is waited for on the path from the softmax to PV
+                    if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                    if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t vb = sV + s * C::kTileBytes;
+#pragma unroll
+                    for (int ks = 0; ks < BN / 16; ++ks) {
+                        if (!((h_cur >> (ks >> 2)) & 1u)) continue;
+                        mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024),
+                               idO, o_started ? 1u : 0u);
+                        o_started = true;
+                    }
+                    mma_commit(bars.vempty(s));
                 }
-                mma_commit(bars.vempty(s));
                 mma_commit(bars.odone());
             }
             if (!ok) {
@@ -464,6 +569,9 @@ template <int D>
 struct PPCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kStages = D == 64 ? 4 : 2;
+    // exp pairs of every 8 evaluated by the FMA-pipe polynomial (exp2_poly_pair) instead of
+    // MUFU ex2: at d = 64 a tile's exps take MUFU about as long as its MMAs take the tensor core
+    static constexpr int kPolyPairs = 0;
     static constexpr int kTileBytes = BM * D * 2;
     static constexpr int kChunkBytes = BM * 128;
     static constexpr int kQOff = 0;                                // Q_A, Q_B
@@ -700,10 +808,10 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int t = 0; t < 16; ++t) {
                     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[qq][2 * t]), __uint_as_float(rr[qq][2 * t + 1])),
                                                sl2x2, negm2);
-                    float x0, x1;
-                    f2_unpack(x2, x0, x1);
-                    const float y0 = ex2(x0), y1 = ex2(x1);
-                    sumq[2 + qq] = f2_add(sumq[2 + qq], f2_pack(y0, y1));
+                    const uint64_t y2 = exp2_pair<C::kPolyPairs>(x2, t);
+                    sumq[2 + qq] = f2_add(sumq[2 + qq], y2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
                     pkh[qq][t] = pack_bf16(y0, y1);
                 }
             }
@@ -720,10 +828,10 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int t = 0; t < 16; ++t) {
                     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1])),
                                                sl2x2, negm2);
-                    float x0, x1;
-                    f2_unpack(x2, x0, x1);
-                    const float y0 = ex2(x0), y1 = ex2(x1);
-                    sumq[q] = f2_add(sumq[q], f2_pack(y0, y1));
+                    const uint64_t y2 = exp2_pair<C::kPolyPairs>(x2, t);
+                    sumq[q] = f2_add(sumq[q], y2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
                     pk[t] = pack_bf16(y0, y1);
                 }
                 tmem_st16(scol + q * 16, pk);
@@ -906,24 +1014,28 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     const bool fine = hm != nullptr && mb == 64;
 
     if (warp == kSplTmaWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0 && n > 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+        // ------------------------------------------------------------ producers
+        // Lane 0 loads K, lane 1 loads V, each as soon as its own stage is released: S of a
+        // visit is issued two visits ahead of its PV's turn (after the PV that read the same
+        // warpgroup's S buffer), so K must run ahead of V, which one thread loading K and V of
+        // each block in turn would hold back behind V's later release.
+        if (lane < 2 && n > 0) {
+            const bool is_v = lane == 1;
+            const CUtensorMap *tm = is_v ? &tmV : &tmK;
+            const uint32_t base = is_v ? sV : sK;
+            tma_prefetch_desc(tm);
             int j = -1;
             for (int it = 0; it < n; ++it) {
                 j = next_block(j);
                 const int s = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 const int krow = head * p.N + j * BN;
-                if (it >= S && !mbar_wait(bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
-                mbar_arrive_expect_tx(bars.kfull(s), C::kTileBytes);
+                const uint32_t full = is_v ? bars.vfull(s) : bars.kfull(s);
+                if (it >= S && !mbar_wait(is_v ? bars.vempty(s) : bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status))
+                    break;
+                mbar_arrive_expect_tx(full, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(sK + s * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(s));
-                if (it >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
-                mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
+                    tma_load_2d(base + s * C::kTileBytes + c * C::kChunkBytes, tm, c * 64, krow, full);
             }
         }
     } else if (warp == kSplMmaWarp) {
@@ -969,12 +1081,9 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 // S has been issued for visits 0 .. min(it + 1, n - 1): this visit's halves sit one
                 // field up when the next visit's S is already issued
                 const uint32_t h_cur = (it + 1 < n ? hist >> 2 : hist) & 3u;
-                // V_it and K_{it+2} were loaded long ago: check them before waiting for P, so that
-                // only P_x(it) is waited for on the path from the softmax to PV
+                // V_it was loaded long ago: check it before waiting for P, so that only P_x(it) is
+                // waited for on the path from the softmax to PV (K_{it+2} is waited for after PV)
                 if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
-                if (it + 2 < n && !(ok = mbar_wait(bars.kfull((it + 2) % S), (uint32_t)((it + 2) / S) & 1u,
-                                                   abort_flag, p.dev_status)))
-                    break;
                 if (!(ok = mbar_wait(bars.pfull(x), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
                 tc_fence_after();
                 const uint32_t vb_ = sV + s * C::kTileBytes;
@@ -1276,8 +1385,8 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
     dim3 grid(p.N / BM, p.B * p.H);
     {
         ProfScope prof_("fwd_bf16", st);
-        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, static_cast<__nv_bfloat16 *>(O),
-                                                            LSE);
+        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, m.v64, p,
+                                                            static_cast<__nv_bfloat16 *>(O), LSE);
     }
     return cudaGetLastError();
 }
