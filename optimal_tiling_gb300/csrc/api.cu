@@ -291,8 +291,7 @@ attn_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float
     const uint64_t rows = (uint64_t)B * H * N;
     attn::FwdMaps maps;
     if (!make_map_bf16(&maps.q, Q, d, rows, 128) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
-        !make_map_bf16(&maps.v, V, d, rows, 128) || !make_map_bf16(&maps.o, O, d, rows, 128) ||
-        !make_map_bf16(&maps.v64, V, d, rows, 64))
+        !make_map_bf16(&maps.v, V, d, rows, d == 256 ? 64 : 128) || !make_map_bf16(&maps.o, O, d, rows, 128))
         return ATTN_ERR_CUDA;
     return launch_status(attn::launch_fwd_bf16(p, maps, O, LSE, st));
 }

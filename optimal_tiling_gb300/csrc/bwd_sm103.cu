@@ -377,12 +377,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const uint8_t *r = hm + (size_t)iq * mnb + 2 * kvt;
                     return (uint32_t)(r[0] != 0) | ((uint32_t)(r[1] != 0) << 1);
                 };
-                int iq_next = n > 0 ? next_q(q_lo - 1) : 0;
-                uint32_t h_next = n > 0 ? halves(iq_next) : 3u;
+                int iq_next = (fine && n > 0) ? next_q(q_lo - 1) : 0;
+                uint32_t h_next = halves(iq_next);
                 for (int it = 0; it < n && ok; ++it) {
                     const int b = it & 1;
                     const uint32_t h_cur = h_next;
-                    if (it + 1 < n) {
+                    if (fine && it + 1 < n) {
                         iq_next = next_q(iq_next);
                         h_next = halves(iq_next);
                     }
@@ -393,13 +393,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     tc_fence_after();
                     const uint32_t dsb = sDs + b * C::kDsTile;
                     // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous)
-                    bool first = true;
+                    if (h_cur == 3u) {
 #pragma unroll
-                    for (int ks = 0; ks < BKV / 16; ++ks) {
-                        if (!((h_cur >> (ks >> 2)) & 1u)) continue;
-                        mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + ks * 2048, C::kDqALbo, 1024),
-                               smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, first ? 0u : 1u);
-                        first = false;
+                        for (int ks = 0; ks < BKV / 16; ++ks)
+                            mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + ks * 2048, C::kDqALbo, 1024),
+                                   smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
+                    } else {  // one key half kept for this query block: its four k-steps only
+                        const int k0 = h_cur == 1u ? 0 : 4;
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + (k0 + k4) * 2048, C::kDqALbo, 1024),
+                                   smem_desc_sw128(dsb + (k0 + k4) * 2048, C::kDsTile, 1024), idQ, k4 > 0);
                     }
                     mma_commit(bars.dsfree(b));
                     mma_commit(bars.dqfull());

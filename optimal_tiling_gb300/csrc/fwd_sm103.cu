@@ -115,6 +115,11 @@ __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int 
     return (r0[0] | r0[1] | r1[0] | r1[1]) != 0;
 }
 
+// Instruction descriptors of the S = Q K^T product (128 x 128, both operands K-major), and the
+// same with A negated for a negative score scale.
+constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
+constexpr uint32_t kIdSNeg = kIdS | kIdescNegateA;
+
 // 2^x of a pair of exponents: pair t of a run takes the FMA-pipe polynomial when t % 8 is
 // below POLY, MUFU ex2 otherwise (POLY = 0: always MUFU).
 template <int POLY>
@@ -128,9 +133,8 @@ __device__ __forceinline__ uint64_t exp2_pair(uint64_t x2, int t) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                const __grid_constant__ CUtensorMap tmV64, const Problem p, __nv_bfloat16 *__restrict__ O,
-                float *__restrict__ LSE) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
+                __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
     using C = FwdCfg<D>;
     constexpr int S = C::kStages;
     constexpr int NP = C::kPieces;
@@ -205,7 +209,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // goes to slot q % NP once the MMAs of piece q - NP have released it.
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV64);
+            tma_prefetch_desc(&tmV);
             int q = 0;
             auto load = [&](bool is_v, int blk) -> bool {
                 const int krow = head * p.N + blk * BN;
@@ -218,9 +222,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     mbar_arrive_expect_tx(full, C::kPieceBytes);
                     if (!is_v) {  // K, columns 128 h .. 128 h + 127: two 128-row boxes
                         for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * C::kChunkBytes, &tmK, (2 * h + c) * 64, krow, full);
-                    } else {      // V, keys 64 h .. 64 h + 63: four 64-row boxes
+                    } else {      // V, keys 64 h .. 64 h + 63: four 64-row boxes (V's map at d = 256)
                         for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_2d(dst + c * (C::kPieceBytes / C::kChunks), &tmV64, c * 64, krow + 64 * h, full);
+                            tma_load_2d(dst + c * (C::kPieceBytes / C::kChunks), &tmV, c * 64, krow + 64 * h, full);
                     }
                 }
                 return true;
@@ -261,7 +265,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             // a negative scale: S = (-Q) K^T, scaled by |s| below
-            const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
+            const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
             int q = 0;  // next piece of the ring (the producer's order)
@@ -310,15 +314,16 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
                 return (uint32_t)((r0[0] | r1[0]) != 0) | ((uint32_t)((r0[1] | r1[1]) != 0) << 1);
             };
-            int j_next = next_block(-1);
+            int j_next = fine ? next_block(-1) : 0;
             uint32_t h_next = halves(j_next);
-            bool o_started = false;  // the first PV product initialises O
             if (ok) ok = issue_s(0);
             for (int it = 0; it < n && ok; ++it) {
                 const uint32_t h_cur = h_next;
                 if (it + 1 < n) {
-                    j_next = next_block(j_next);
-                    h_next = halves(j_next);
+                    if (fine) {
+                        j_next = next_block(j_next);
+                        h_next = halves(j_next);
+                    }
                     if (!(ok = issue_s(it + 1))) break;
                 }
                 const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
@@ -332,18 +337,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status)))
                         break;
                     tc_fence_after();
+                    // the first product of the tile initialises O (every visited block issues at
+                    // least one half: a visit keeps some score)
+                    bool first = it == 0;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int slot = h ? slot1 : slot0;
                         const uint32_t vb = sK + slot * C::kPieceBytes;  // keys 64 h .. 64 h + 63 of V_it
                         if ((h_cur >> h) & 1u) {
 #pragma unroll
-                            for (int k4 = 0; k4 < 4; ++k4) {
+                            for (int k4 = 0; k4 < 4; ++k4)
                                 mma_ts(tmem + kOCol, pcol + (4 * h + k4) * 8,
                                        smem_desc_sw128(vb + k4 * 2048, C::kPieceBytes / C::kChunks, 1024), idO,
-                                       o_started ? 1u : 0u);
-                                o_started = true;
-                            }
+                                       (first && k4 == 0) ? 0u : 1u);
+                            first = false;
                         }
                         mma_commit(bars.kempty(slot));
                     }
@@ -357,12 +364,18 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         break;
                     tc_fence_after();
                     const uint32_t vb = sV + s * C::kTileBytes;
+                    if (h_cur == 3u) {
 #pragma unroll
-                    for (int ks = 0; ks < BN / 16; ++ks) {
-                        if (!((h_cur >> (ks >> 2)) & 1u)) continue;
-                        mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024),
-                               idO, o_started ? 1u : 0u);
-                        o_started = true;
+                        for (int ks = 0; ks < BN / 16; ++ks)
+                            mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024),
+                                   idO, (it > 0 || ks > 0) ? 1u : 0u);
+                    } else {  // one key half kept by some row (64-row masks): its four k-steps only
+                        const int k0 = h_cur == 1u ? 0 : 4;
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_ts(tmem + kOCol, pcol + (k0 + k4) * 8,
+                                   smem_desc_sw128(vb + (k0 + k4) * 2048, C::kChunkBytes, 1024), idO,
+                                   (it > 0 || k4 > 0) ? 1u : 0u);
                     }
                     mma_commit(bars.vempty(s));
                 }
@@ -672,7 +685,7 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     } else if (warp == kPPMmaWarp) {
         if (lane == 0) {
             // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
-            const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
+            const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             auto mma_s = [&](int x, int j) {
                 const uint32_t kb = sK + (j % S) * C::kTileBytes, qb = sQ + x * C::kTileBytes;
@@ -1042,7 +1055,7 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
-            const uint32_t idS = idesc_bf16_f32(BM, BN, false, false) | (p.scale < 0.f ? kIdescNegateA : 0u);
+            const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             // 64-row mask blocks: the 64-key halves of a visit's block that some row of the tile
             // keeps (bit 0: keys 0-63, bit 1: keys 64-127); PV skips the k-steps of a half no row
@@ -1052,14 +1065,15 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
                 return (uint32_t)((r0[0] | r1[0]) != 0) | ((uint32_t)((r0[1] | r1[1]) != 0) << 1);
             };
-            int j_s = -1;        // block of the newest S issued
+            int j_s = -1;        // block of the newest S issued (64-row masks)
             uint32_t hist = 0;
-            bool started0 = false, started1 = false;  // the first PV product of a warpgroup initialises O_x
             // S_x(it) = Q K_it^T into warpgroup x = it & 1's S buffer
             auto issue_s = [&](int it) -> bool {
                 const int s = it % S, x = it & 1;
-                j_s = next_block(j_s);
-                hist = (hist << 2) | halves(j_s);
+                if (fine) {
+                    j_s = next_block(j_s);
+                    hist = (hist << 2) | halves(j_s);
+                }
                 if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
                 tc_fence_after();
                 const uint32_t kb = sK + s * C::kTileBytes;
@@ -1080,23 +1094,28 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 const int s = it % S, x = it & 1;
                 // S has been issued for visits 0 .. min(it + 1, n - 1): this visit's halves sit one
                 // field up when the next visit's S is already issued
-                const uint32_t h_cur = (it + 1 < n ? hist >> 2 : hist) & 3u;
+                const uint32_t h_cur = fine ? (it + 1 < n ? hist >> 2 : hist) & 3u : 3u;
                 // V_it was loaded long ago: check it before waiting for P, so that only P_x(it) is
                 // waited for on the path from the softmax to PV (K_{it+2} is waited for after PV)
                 if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
                 if (!(ok = mbar_wait(bars.pfull(x), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
                 tc_fence_after();
                 const uint32_t vb_ = sV + s * C::kTileBytes;
+                // a warpgroup's first visit (it = x < 2) initialises O_x with its first product
+                if (h_cur == 3u) {
 #pragma unroll
-                bool started = x ? started1 : started0;
-                for (int ks = 0; ks < BN / 16; ++ks) {
-                    if (!((h_cur >> (ks >> 2)) & 1u)) continue;
-                    mma_ts(tmem + C::kOCol0 + x * D, tmem + PPCfg<D>::scol(x) + ks * 8,
-                           smem_desc_sw128(vb_ + ks * 2048, C::kChunkBytes, 1024), idO, started ? 1u : 0u);
-                    started = true;
+                    for (int ks = 0; ks < BN / 16; ++ks)
+                        mma_ts(tmem + C::kOCol0 + x * D, tmem + PPCfg<D>::scol(x) + ks * 8,
+                               smem_desc_sw128(vb_ + ks * 2048, C::kChunkBytes, 1024), idO,
+                               (it >= 2 || ks > 0) ? 1u : 0u);
+                } else {  // one key half kept by some row (64-row masks): its four k-steps only
+                    const int k0 = h_cur == 1u ? 0 : 4;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        mma_ts(tmem + C::kOCol0 + x * D, tmem + PPCfg<D>::scol(x) + (k0 + k4) * 8,
+                               smem_desc_sw128(vb_ + (k0 + k4) * 2048, C::kChunkBytes, 1024), idO,
+                               (it >= 2 || k4 > 0) ? 1u : 0u);
                 }
-                if (x) started1 = started;
-                else started0 = started;
                 mma_commit(bars.vempty(s));
                 if (it + 2 < n) {
                     if (!(ok = issue_s(it + 2))) break;
@@ -1385,8 +1404,8 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
     dim3 grid(p.N / BM, p.B * p.H);
     {
         ProfScope prof_("fwd_bf16", st);
-        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, m.v64, p,
-                                                            static_cast<__nv_bfloat16 *>(O), LSE);
+        kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, static_cast<__nv_bfloat16 *>(O),
+                                                            LSE);
     }
     return cudaGetLastError();
 }

@@ -58,8 +58,7 @@ cudaError_t launch_bwd_f32(const Problem &p, const float *Q, const float *K, con
 // ---- bf16 tcgen05 path ------------------------------------------------------
 // Tensor maps are built by the host layer (see tma_desc in api.cu).
 struct FwdMaps {
-    CUtensorMap q, k, v, o;
-    CUtensorMap v64;  // V with 64-row boxes (the d = 256 kernel loads V in 64-key halves)
+    CUtensorMap q, k, v, o;  // 128-row boxes; at d = 256 V has 64-row boxes (loaded in 64-key halves)
 };
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE,
                             cudaStream_t st);
