@@ -5,27 +5,37 @@
 // (the stabilised online update: running max m, sum l, accumulator u, o = u/l)
 // and "Large caches: where FlashAttention's I/O comes from" (a query block and
 // its output state stay on chip while all of K, V is scanned).  The page's
-// schedule is for a generic two-level machine; this kernel is shaped for GB300:
+// schedule is for a generic two-level machine; these kernels are shaped for GB300:
 //
-//   * one CTA per 128-row query tile of one head; K/V are scanned in 128-row
+//   * a CTA owns 128-row query tiles of one head; K/V are scanned in 128-row
 //     blocks through a TMA ring in shared memory (128-byte swizzle);
 //   * both products run on tcgen05 with fp32 accumulators in tensor memory:
-//     S = Q K^T into one of two 128-column S buffers, O += P V into a d-column
-//     O buffer; P (bf16) is written back over its own S buffer and fed to the
-//     second MMA straight from tensor memory;
-//   * warp roles: warps 0-3 own one query row per thread (TMEM lane = row) and
-//     run the softmax, the O rescale and the epilogue; warp 4 issues TMA; warp 5
-//     allocates tensor memory and issues the MMAs from one elected lane;
-//   * S for block j+1 is computed while the softmax of block j runs;
+//     S = Q K^T into a 128-column S buffer, O += P V into a d-column O buffer;
+//     P (bf16) is written back over its own S buffer and fed to the second MMA
+//     straight from tensor memory;
+//   * softmax warps own one query row per thread (TMEM lane = row) and run the
+//     softmax, the O rescale and the epilogue; one warp issues TMA, one lane of
+//     another allocates tensor memory and issues every MMA;
 //   * the running max is kept in the log2 domain (scores scaled by s*log2 e) and
 //     O is rescaled only when a row's max grows by more than 8 (a factor 256):
 //     the final division uses the same reference max, so the result is the same
 //     function and only rounding differs;
-//   * key blocks whose mask entries for this query tile are all zero are never
+//   * key blocks whose mask entries for a query tile are all zero are never
 //     loaded or multiplied; with 64-row mask blocks a visited 128-key block can
 //     still be removed for one half of the keys or one half of the rows, and
 //     the softmax warps drop those 64-column halves (whole 32-column TMEM
-//     chunks, the same for every row of a warp) before the max and the exps.
+//     chunks, the same for every row of a warp) before the max and the exps;
+//   * a negative score scale s sets the instruction descriptor's negate-A bit
+//     of the S product, so the tensor core returns sign(s) Q K^T and the softmax
+//     scales it by |s|.
+// Three kernels:
+//   fwd_bf16_kernel       one query tile per CTA, S double-buffered so that S of
+//                         block j+1 is computed while the softmax of block j runs
+//                         (block masks, or N % 256 != 0; d = 64, 128);
+//   fwd_bf16_pp_kernel    two query tiles per CTA sharing every K/V block, the
+//                         tensor core on one tile while the other's softmax runs
+//                         (no mask, N % 256 == 0; d = 64, 128);
+//   fwd_bf16_ring_kernel  d = 256: K and V stream through a ring of 32 KB pieces.
 // Every mbarrier wait is bounded; an expired wait sets the device status word
 // and the CTA unwinds without touching the GPU's state.
 #include <cuda_bf16.h>
@@ -59,34 +69,21 @@ struct FwdCfg {
     static constexpr int kChunks = D / 64;                     // 64-element (128 B) swizzle atoms per row
     // K/V ring depth: as deep as the shared memory allows (block-sparse masks scatter the
     // key blocks a tile visits, so their loads miss L2 and need the latency covered)
-    static constexpr int kStages = D == 64 ? 6 : (D == 128 ? 3 : 1);
-    // exps per 8 pairs evaluated by the FMA-pipe polynomial instead of MUFU (measured on this
-    // kernel: every split above 0 was slower)
-    static constexpr int kPolyPairs = 0;
+    static constexpr int kStages = D == 64 ? 6 : 3;
     static constexpr int kTileBytes = BM * D * 2;              // Q tile == K tile == V tile bytes
     static constexpr int kChunkBytes = BM * 128;               // one 64-column slab of a tile
-    // d = 256: one K and one V tile (64 KB each) would fit beside Q, so V of the next block could
-    // load only after the current PV; instead K and V stream through a ring of kPieces 32 KB
-    // pieces, consumed in tensor-core order: K of a block in two d-halves (128 keys x 128
-    // columns), V in two 64-key halves (64 keys x 256 columns)
-    static constexpr bool kRing = D == 256;
-    static constexpr int kPieces = 5;
-    static constexpr int kPieceBytes = 32768;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + kTileBytes;           // ring base when kRing
+    static constexpr int kKOff = kQOff + kTileBytes;
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kRing ? kKOff + kPieces * kPieceBytes : kVOff + kStages * kTileBytes;
-    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain (ring: S =
-    // kPieces, and kfull / kempty are a piece's full / empty barriers)
-    static constexpr int kBarStages = kRing ? kPieces : kStages;
-    static constexpr int kNumBars = 1 + 4 * kBarStages + 2 + 2 + 1 + 1;
+    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // visited key blocks as a bit set: masks with up to 32 * kMaxMaskWords blocks per row
     static constexpr int kMaxMaskWords = 256;
     static constexpr int kBitsOff = kMiscOff + 64;
     static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
     static_assert(kChunkBytes == 16384, "slab layout");
-    static_assert(!kRing || (BN * 128 * 2 == kPieceBytes && (BN / 2) * D * 2 == kPieceBytes), "piece sizes");
     static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
@@ -120,16 +117,6 @@ __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int 
 constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
 constexpr uint32_t kIdSNeg = kIdS | kIdescNegateA;
 
-// 2^x of a pair of exponents: pair t of a run takes the FMA-pipe polynomial when t % 8 is
-// below POLY, MUFU ex2 otherwise (POLY = 0: always MUFU).
-template <int POLY>
-__device__ __forceinline__ uint64_t exp2_pair(uint64_t x2, int t) {
-    if (POLY > 0 && (t & 7) < POLY) return exp2_poly_pair(x2);
-    float x0, x1;
-    f2_unpack(x2, x0, x1);
-    return f2_pack(ex2(x0), ex2(x1));
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -137,10 +124,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
     using C = FwdCfg<D>;
     constexpr int S = C::kStages;
-    constexpr int NP = C::kPieces;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Bars bars{smem_addr(sm + C::kBarOff), C::kBarStages};
+    const Bars bars{smem_addr(sm + C::kBarOff), S};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
 
@@ -158,7 +144,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(bars.q(), 1);
-        for (int s = 0; s < C::kBarStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(bars.kfull(s), 1);
             mbar_init(bars.kempty(s), 1);
             mbar_init(bars.vfull(s), 1);
@@ -202,45 +188,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         return j;
     };
 
-    if (warp == kTmaWarp && C::kRing) {
-        // ------------------------------------------------------------ producer (piece ring)
-        // The tensor core's order is S(0), S(1), PV(0), S(2), PV(1), ..., PV(n-1), so pieces are
-        // loaded in the order K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1); piece q
-        // goes to slot q % NP once the MMAs of piece q - NP have released it.
-        if (lane == 0 && n > 0) {
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            int q = 0;
-            auto load = [&](bool is_v, int blk) -> bool {
-                const int krow = head * p.N + blk * BN;
-                for (int h = 0; h < 2; ++h, ++q) {
-                    const int slot = q % NP;
-                    if (q >= NP && !mbar_wait(bars.kempty(slot), ((uint32_t)(q / NP) & 1u) ^ 1u, abort_flag,
-                                              p.dev_status))
-                        return false;
-                    const uint32_t full = bars.kfull(slot), dst = sK + slot * C::kPieceBytes;
-                    mbar_arrive_expect_tx(full, C::kPieceBytes);
-                    if (!is_v) {  // K, columns 128 h .. 128 h + 127: two 128-row boxes
-                        for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * C::kChunkBytes, &tmK, (2 * h + c) * 64, krow, full);
-                    } else {      // V, keys 64 h .. 64 h + 63: four 64-row boxes (V's map at d = 256)
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_2d(dst + c * (C::kPieceBytes / C::kChunks), &tmV, c * 64, krow + 64 * h, full);
-                    }
-                }
-                return true;
-            };
-            int jk = next_block(-1), jv = jk;
-            bool ok = load(false, jk);
-            for (int it = 0; it < n && ok; ++it) {
-                if (it + 1 < n) {
-                    jk = next_block(jk);
-                    if (!(ok = load(false, jk))) break;
-                }
-                if (!(ok = load(true, jv))) break;
-                if (it + 1 < n) jv = next_block(jv);
-            }
-        }
-    } else if (warp == kTmaWarp) {
+    if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmK);
@@ -264,121 +212,43 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
-            // a negative scale: S = (-Q) K^T, scaled by |s| below
+            // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
             const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
             bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
-            int q = 0;  // next piece of the ring (the producer's order)
             // S_it = Q K_it^T into S buffer (it & 1)
             auto issue_s = [&](int it) -> bool {
+                const int s = it % S;
+                if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
+                tc_fence_after();
                 const uint32_t dcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
-                if constexpr (C::kRing) {
-                    for (int h = 0; h < 2; ++h, ++q) {  // d-half h of K_it
-                        const int slot = q % NP;
-                        if (!mbar_wait(bars.kfull(slot), (uint32_t)(q / NP) & 1u, abort_flag, p.dev_status))
-                            return false;
-                        tc_fence_after();
-                        const uint32_t kb = sK + slot * C::kPieceBytes;
+                const uint32_t kb = sK + s * C::kTileBytes;
 #pragma unroll
-                        for (int k8 = 0; k8 < 8; ++k8) {
-                            const int ks = 8 * h + k8;
-                            mma_ss(dcol, smem_desc_sw128(sQ + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024),
-                                   smem_desc_sw128(kb + (k8 >> 2) * C::kChunkBytes + (k8 & 3) * 32, 16, 1024), idS,
-                                   ks > 0);
-                        }
-                        mma_commit(bars.kempty(slot));
-                    }
-                } else {
-                    const int s = it % S;
-                    if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
-                    tc_fence_after();
-                    const uint32_t kb = sK + s * C::kTileBytes;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-                        mma_ss(dcol, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idS,
-                               ks > 0);
-                    }
-                    mma_commit(bars.kempty(s));
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                    mma_ss(dcol, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), idS,
+                           ks > 0);
                 }
+                mma_commit(bars.kempty(s));
                 mma_commit(bars.sfull(it & 1));
                 return true;
             };
-            // 64-row mask blocks: the 64-key halves of a visited block that some row of this tile
-            // keeps (bit 0: keys 0-63, bit 1: keys 64-127).  The softmax writes P = 0 over a half
-            // that no row keeps, so PV skips its k-steps (adding those zero products would change
-            // nothing).  Read one block ahead, so that the loads are off the issue path.
-            const bool fine = hm != nullptr && mb == 64;
-            auto halves = [&](int j) -> uint32_t {
-                if (!fine) return 3u;
-                const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
-                return (uint32_t)((r0[0] | r1[0]) != 0) | ((uint32_t)((r0[1] | r1[1]) != 0) << 1);
-            };
-            int j_next = fine ? next_block(-1) : 0;
-            uint32_t h_next = halves(j_next);
             if (ok) ok = issue_s(0);
             for (int it = 0; it < n && ok; ++it) {
-                const uint32_t h_cur = h_next;
-                if (it + 1 < n) {
-                    if (fine) {
-                        j_next = next_block(j_next);
-                        h_next = halves(j_next);
-                    }
-                    if (!(ok = issue_s(it + 1))) break;
-                }
+                if (it + 1 < n && !(ok = issue_s(it + 1))) break;
+                const int s = it % S;
+                // V_it was loaded long ago: check it before waiting for P_it, so that only P_it is
+                // waited for on the path from the softmax to PV
+                if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                tc_fence_after();
                 const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
-                if constexpr (C::kRing) {
-                    // V_it's two 64-key halves are pieces q and q + 1; check both before P_it
-                    const int slot0 = q % NP, slot1 = (q + 1) % NP;
-                    if (!(ok = mbar_wait(bars.kfull(slot0), (uint32_t)(q / NP) & 1u, abort_flag, p.dev_status))) break;
-                    if (!(ok = mbar_wait(bars.kfull(slot1), (uint32_t)((q + 1) / NP) & 1u, abort_flag,
-                                         p.dev_status)))
-                        break;
-                    if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status)))
-                        break;
-                    tc_fence_after();
-                    // the first product of the tile initialises O (every visited block issues at
-                    // least one half: a visit keeps some score)
-                    bool first = it == 0;
+                const uint32_t vb = sV + s * C::kTileBytes;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int slot = h ? slot1 : slot0;
-                        const uint32_t vb = sK + slot * C::kPieceBytes;  // keys 64 h .. 64 h + 63 of V_it
-                        if ((h_cur >> h) & 1u) {
-#pragma unroll
-                            for (int k4 = 0; k4 < 4; ++k4)
-                                mma_ts(tmem + kOCol, pcol + (4 * h + k4) * 8,
-                                       smem_desc_sw128(vb + k4 * 2048, C::kPieceBytes / C::kChunks, 1024), idO,
-                                       (first && k4 == 0) ? 0u : 1u);
-                            first = false;
-                        }
-                        mma_commit(bars.kempty(slot));
-                    }
-                    q += 2;
-                } else {
-                    const int s = it % S;
-                    // V_it was loaded long ago: check it before waiting for P_it, so that only P_it
-                    // is waited for on the path from the softmax to PV
-                    if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
-                    if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t vb = sV + s * C::kTileBytes;
-                    if (h_cur == 3u) {
-#pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks)
-                            mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024),
-                                   idO, (it > 0 || ks > 0) ? 1u : 0u);
-                    } else {  // one key half kept by some row (64-row masks): its four k-steps only
-                        const int k0 = h_cur == 1u ? 0 : 4;
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4)
-                            mma_ts(tmem + kOCol, pcol + (k0 + k4) * 8,
-                                   smem_desc_sw128(vb + (k0 + k4) * 2048, C::kChunkBytes, 1024), idO,
-                                   (it > 0 || k4 > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bars.vempty(s));
-                }
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO,
+                           (it > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bars.vempty(s));
                 mma_commit(bars.odone());
             }
             if (!ok) {
@@ -439,8 +309,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 alpha = ex2(m_used - m_new);
                 m_used = m_new;
             }
-            // p = 2^(s log2e S - m): pairs on the packed FMA path; kPolyPairs of every 8
-            // pairs take the FMA-pipe polynomial, the rest the MUFU ex2.
+            // p = 2^(s log2e S - m): pairs on the packed FMA path, exps on MUFU
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t negm2 = f2_pack(-m_used, -m_used);
             uint64_t sumq[4];  // four independent row-sum chains
@@ -459,14 +328,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int t = 0; t < 16; ++t) {
                     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1])),
                                                sl2x2, negm2);
-                    uint64_t y2;
-                    if ((t & 7) < C::kPolyPairs) {
-                        y2 = exp2_poly_pair(x2);
-                    } else {
-                        float x0, x1;
-                        f2_unpack(x2, x0, x1);
-                        y2 = f2_pack(ex2(x0), ex2(x1));
-                    }
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const uint64_t y2 = f2_pack(ex2(x0), ex2(x1));
                     sumq[q] = f2_add(sumq[q], y2);
                     float y0, y1;
                     f2_unpack(y2, y0, y1);
@@ -582,9 +446,6 @@ template <int D>
 struct PPCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kStages = D == 64 ? 4 : 2;
-    // exp pairs of every 8 evaluated by the FMA-pipe polynomial (exp2_poly_pair) instead of
-    // MUFU ex2: at d = 64 a tile's exps take MUFU about as long as its MMAs take the tensor core
-    static constexpr int kPolyPairs = 0;
     static constexpr int kTileBytes = BM * D * 2;
     static constexpr int kChunkBytes = BM * 128;
     static constexpr int kQOff = 0;                                // Q_A, Q_B
@@ -821,10 +682,10 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int t = 0; t < 16; ++t) {
                     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[qq][2 * t]), __uint_as_float(rr[qq][2 * t + 1])),
                                                sl2x2, negm2);
-                    const uint64_t y2 = exp2_pair<C::kPolyPairs>(x2, t);
-                    sumq[2 + qq] = f2_add(sumq[2 + qq], y2);
-                    float y0, y1;
-                    f2_unpack(y2, y0, y1);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[2 + qq] = f2_add(sumq[2 + qq], f2_pack(y0, y1));
                     pkh[qq][t] = pack_bf16(y0, y1);
                 }
             }
@@ -841,10 +702,10 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int t = 0; t < 16; ++t) {
                     const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1])),
                                                sl2x2, negm2);
-                    const uint64_t y2 = exp2_pair<C::kPolyPairs>(x2, t);
-                    sumq[q] = f2_add(sumq[q], y2);
-                    float y0, y1;
-                    f2_unpack(y2, y0, y1);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[q] = f2_add(sumq[q], f2_pack(y0, y1));
                     pk[t] = pack_bf16(y0, y1);
                 }
                 tmem_st16(scol + q * 16, pk);
@@ -910,60 +771,58 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// One query tile, two softmax warpgroups ("split key blocks"): the key blocks the
-// tile visits are dealt out in turn, even-numbered visits to warpgroup 0 (warps
-// 0-3) and odd-numbered ones to warpgroup 1 (warps 4-7).  Each warpgroup keeps its
-// own S buffer (128 columns), running max m_x, sum l_x and O accumulator O_x (d
-// columns) in tensor memory, and the two partial states are merged at the end with
-// the online-softmax rule of the page's section "Softmax without storing the score
-// matrix": m = max(m_0, m_1), l = sum_x 2^(m_x - m) l_x, O = sum_x 2^(m_x - m) O_x / l.
-// The MMA order is the two-tile kernel's with "tile X" read as "warpgroup X":
-//     PV_0(i), S_0(i+2), PV_1(i+1), S_1(i+3), ...
-// so the tensor core works on one warpgroup's block while the other warpgroup's
-// softmax runs, whatever the mask (each warpgroup's next S waits only for its K
-// block).  Because one thread's MMAs complete in issue order, "S_x(i+2) done" means
-// "PV_x(i) done", so the softmax may rescale O_x as soon as it sees S_x(i+2).  Each
-// K/V block serves one warpgroup.  Used under block masks and for N % 256 != 0 at
-// d = 64 and 128.
-constexpr int kSplThreads = 320;
-constexpr int kSplTmaWarp = 8;
-constexpr int kSplMmaWarp = 9;
-
+// d = 256, one query tile per CTA.  The Q tile takes 64 KB; one K and one V tile
+// (64 KB each) fit beside it, but then V of block j+1 can load only after PV of
+// block j, and the pass waits for that load every block.  Instead K and V stream
+// through a ring of five 32 KB pieces, loaded and consumed in the tensor core's
+// order: K of a block as two d-halves (128 keys x 128 columns, the k-steps
+// 0..7 and 8..15 of S = Q K^T) and V as two 64-key halves (64 keys x 256
+// columns, the k-steps 0..3 and 4..7 of O += P V), so the next block's pieces
+// load while the current products run.  Otherwise the single-tile scheme.
 template <int D>
-struct SplCfg {
-    static constexpr int kChunks = D / 64;
-    static constexpr int kStages = D == 64 ? 6 : 3;
-    static constexpr int kTileBytes = BM * D * 2;
-    static constexpr int kChunkBytes = BM * 128;
+struct RingCfg {
+    static_assert(D == 256, "the piece ring is laid out for d = 256");
+    static constexpr int kChunks = D / 64;                     // 64-column slabs of a row
+    static constexpr int kTileBytes = BM * D * 2;              // the Q tile: 64 KB
+    static constexpr int kChunkBytes = BM * 128;               // one 64-column slab of a 128-row tile
+    static constexpr int kPieces = 5;
+    static constexpr int kPieceBytes = 32768;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kTileBytes;
-    static constexpr int kVOff = kKOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone[2], drain (the
-    // two-tile kernel's barrier layout)
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kRingOff = kQOff + kTileBytes;
+    static constexpr int kBarOff = kRingOff + kPieces * kPieceBytes;
+    // q, full[P], empty[P], sfull[2], pfull[2], odone, drain
+    static constexpr int kNumBars = 1 + 2 * kPieces + 2 + 2 + 1 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kMaxMaskWords = 256;
     static constexpr int kBitsOff = kMiscOff + 64;
-    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;
-    // the merge exchanges (m, l) of both warpgroups through the first K stage, idle by then
-    static constexpr int kStatOff = kKOff;
-    static constexpr uint32_t kOCol0 = 256;
-    static_assert(2 * 2 * BM * 4 <= kTileBytes, "merge statistics fit one K stage");
-    static_assert(kOCol0 + 2 * D <= kTmemCols, "tensor memory budget");
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
+    static_assert(BN * 128 * 2 == kPieceBytes && (BN / 2) * D * 2 == kPieceBytes, "piece sizes");
+    static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
+struct RingBars {
+    uint32_t base;
+    static constexpr int P = RingCfg<256>::kPieces;
+    __device__ uint32_t q() const { return base; }
+    __device__ uint32_t full(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t empty(int s) const { return base + 8u * (1 + P + s); }
+    __device__ uint32_t sfull(int b) const { return base + 8u * (1 + 2 * P + b); }
+    __device__ uint32_t pfull(int b) const { return base + 8u * (3 + 2 * P + b); }
+    __device__ uint32_t odone() const { return base + 8u * (5 + 2 * P); }
+    __device__ uint32_t drain() const { return base + 8u * (6 + 2 * P); }
+};
+
 template <int D>
-__global__ void __launch_bounds__(kSplThreads, 1)
-fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                      const Problem p, __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
-    using C = SplCfg<D>;
-    constexpr int S = C::kStages;
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
+                     __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
+    using C = RingCfg<D>;
+    constexpr int NP = C::kPieces;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const PPBars bars{smem_addr(sm + C::kBarOff), S};
+    const RingBars bars{smem_addr(sm + C::kBarOff)};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
 
@@ -976,22 +835,20 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     const int nwords = (nb + 31) >> 5;
     const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
     const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
-    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sR = smem_addr(sm + C::kRingOff);
 
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(bars.q(), 1);
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bars.kfull(s), 1);
-            mbar_init(bars.kempty(s), 1);
-            mbar_init(bars.vfull(s), 1);
-            mbar_init(bars.vempty(s), 1);
+        for (int s = 0; s < NP; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.empty(s), 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(bars.sfull(x), 1);
-            mbar_init(bars.pfull(x), 128);
-            mbar_init(bars.odone(x), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.sfull(b), 1);
+            mbar_init(bars.pfull(b), 4 * 32);
         }
+        mbar_init(bars.odone(), 1);
         mbar_init(bars.drain(), 1);
         fence_barrier_init();
         // the Q tile is needed whatever the mask says: start its load before the mask is read
@@ -999,7 +856,7 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
     }
     if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
-    if (warp == kSplMmaWarp) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -1024,104 +881,97 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         } while (!visited(hm, mb, mnb, tile, j));
         return j;
     };
-    const bool fine = hm != nullptr && mb == 64;
 
-    if (warp == kSplTmaWarp) {
-        // ------------------------------------------------------------ producers
-        // Lane 0 loads K, lane 1 loads V, each as soon as its own stage is released: S of a
-        // visit is issued two visits ahead of its PV's turn (after the PV that read the same
-        // warpgroup's S buffer), so K must run ahead of V, which one thread loading K and V of
-        // each block in turn would hold back behind V's later release.
-        if (lane < 2 && n > 0) {
-            const bool is_v = lane == 1;
-            const CUtensorMap *tm = is_v ? &tmV : &tmK;
-            const uint32_t base = is_v ? sV : sK;
-            tma_prefetch_desc(tm);
-            int j = -1;
-            for (int it = 0; it < n; ++it) {
-                j = next_block(j);
-                const int s = it % S;
-                const uint32_t ph = (uint32_t)(it / S) & 1u;
-                const int krow = head * p.N + j * BN;
-                const uint32_t full = is_v ? bars.vfull(s) : bars.kfull(s);
-                if (it >= S && !mbar_wait(is_v ? bars.vempty(s) : bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status))
-                    break;
-                mbar_arrive_expect_tx(full, C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(base + s * C::kTileBytes + c * C::kChunkBytes, tm, c * 64, krow, full);
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer (piece ring)
+        // The tensor core's order is S(0), S(1), PV(0), S(2), PV(1), ..., PV(n-1), so pieces are
+        // loaded in the order K(0), K(1), V(0), K(2), V(1), ..., K(n-1), V(n-2), V(n-1); piece q
+        // goes to slot q % NP once the MMAs of piece q - NP have released it.
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            int q = 0;
+            auto load = [&](bool is_v, int blk) -> bool {
+                const int krow = head * p.N + blk * BN;
+                for (int h = 0; h < 2; ++h, ++q) {
+                    const int slot = q % NP;
+                    if (q >= NP && !mbar_wait(bars.empty(slot), ((uint32_t)(q / NP) & 1u) ^ 1u, abort_flag,
+                                              p.dev_status))
+                        return false;
+                    const uint32_t full = bars.full(slot), dst = sR + slot * C::kPieceBytes;
+                    mbar_arrive_expect_tx(full, C::kPieceBytes);
+                    if (!is_v) {  // K, columns 128 h .. 128 h + 127: two 128-row boxes
+                        for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * C::kChunkBytes, &tmK, (2 * h + c) * 64, krow, full);
+                    } else {      // V, keys 64 h .. 64 h + 63: four 64-row boxes (V's map at d = 256)
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_2d(dst + c * (C::kPieceBytes / C::kChunks), &tmV, c * 64, krow + 64 * h, full);
+                    }
+                }
+                return true;
+            };
+            int jk = next_block(-1), jv = jk;
+            bool ok = load(false, jk);
+            for (int it = 0; it < n && ok; ++it) {
+                if (it + 1 < n) {
+                    jk = next_block(jk);
+                    if (!(ok = load(false, jk))) break;
+                }
+                if (!(ok = load(true, jv))) break;
+                if (it + 1 < n) jv = next_block(jv);
             }
         }
-    } else if (warp == kSplMmaWarp) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
             const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
-            // 64-row mask blocks: the 64-key halves of a visit's block that some row of the tile
-            // keeps (bit 0: keys 0-63, bit 1: keys 64-127); PV skips the k-steps of a half no row
-            // keeps (its P is zero).  hist holds them two bits per visit, newest in the low bits.
-            auto halves = [&](int j) -> uint32_t {
-                if (!fine) return 3u;
-                const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
-                return (uint32_t)((r0[0] | r1[0]) != 0) | ((uint32_t)((r0[1] | r1[1]) != 0) << 1);
-            };
-            int j_s = -1;        // block of the newest S issued (64-row masks)
-            uint32_t hist = 0;
-            // S_x(it) = Q K_it^T into warpgroup x = it & 1's S buffer
+            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
+            int q = 0;  // next piece of the ring (the producer's order)
+            // S_it = Q K_it^T into S buffer (it & 1)
             auto issue_s = [&](int it) -> bool {
-                const int s = it % S, x = it & 1;
-                if (fine) {
-                    j_s = next_block(j_s);
-                    hist = (hist << 2) | halves(j_s);
-                }
-                if (!mbar_wait(bars.kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status)) return false;
-                tc_fence_after();
-                const uint32_t kb = sK + s * C::kTileBytes;
+                const uint32_t dcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
+                for (int h = 0; h < 2; ++h, ++q) {  // d-half h of K_it
+                    const int slot = q % NP;
+                    if (!mbar_wait(bars.full(slot), (uint32_t)(q / NP) & 1u, abort_flag, p.dev_status)) return false;
+                    tc_fence_after();
+                    const uint32_t kb = sR + slot * C::kPieceBytes;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-                    mma_ss(tmem + PPCfg<D>::scol(x), smem_desc_sw128(sQ + off, 16, 1024),
-                           smem_desc_sw128(kb + off, 16, 1024), idS, ks > 0);
+                    for (int k8 = 0; k8 < 8; ++k8) {
+                        const int ks = 8 * h + k8;
+                        mma_ss(dcol, smem_desc_sw128(sQ + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024),
+                               smem_desc_sw128(kb + (k8 >> 2) * C::kChunkBytes + (k8 & 3) * 32, 16, 1024), idS, ks > 0);
+                    }
+                    mma_commit(bars.empty(slot));
                 }
-                mma_commit(bars.kempty(s));
-                mma_commit(bars.sfull(x));
+                mma_commit(bars.sfull(it & 1));
                 return true;
             };
-            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
             if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
             for (int it = 0; it < n && ok; ++it) {
-                const int s = it % S, x = it & 1;
-                // S has been issued for visits 0 .. min(it + 1, n - 1): this visit's halves sit one
-                // field up when the next visit's S is already issued
-                const uint32_t h_cur = fine ? (it + 1 < n ? hist >> 2 : hist) & 3u : 3u;
-                // V_it was loaded long ago: check it before waiting for P, so that only P_x(it) is
-                // waited for on the path from the softmax to PV (K_{it+2} is waited for after PV)
-                if (!(ok = mbar_wait(bars.vfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
-                if (!(ok = mbar_wait(bars.pfull(x), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
+                if (it + 1 < n && !(ok = issue_s(it + 1))) break;
+                const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
+                // V_it's two 64-key halves are pieces q and q + 1: check both before waiting for P_it,
+                // so that only P_it is waited for on the path from the softmax to PV
+                const int slot0 = q % NP, slot1 = (q + 1) % NP;
+                if (!(ok = mbar_wait(bars.full(slot0), (uint32_t)(q / NP) & 1u, abort_flag, p.dev_status))) break;
+                if (!(ok = mbar_wait(bars.full(slot1), (uint32_t)((q + 1) / NP) & 1u, abort_flag, p.dev_status)))
+                    break;
+                if (!(ok = mbar_wait(bars.pfull(it & 1), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status))) break;
                 tc_fence_after();
-                const uint32_t vb_ = sV + s * C::kTileBytes;
-                // a warpgroup's first visit (it = x < 2) initialises O_x with its first product
-                if (h_cur == 3u) {
 #pragma unroll
-                    for (int ks = 0; ks < BN / 16; ++ks)
-                        mma_ts(tmem + C::kOCol0 + x * D, tmem + PPCfg<D>::scol(x) + ks * 8,
-                               smem_desc_sw128(vb_ + ks * 2048, C::kChunkBytes, 1024), idO,
-                               (it >= 2 || ks > 0) ? 1u : 0u);
-                } else {  // one key half kept by some row (64-row masks): its four k-steps only
-                    const int k0 = h_cur == 1u ? 0 : 4;
+                for (int h = 0; h < 2; ++h) {
+                    const int slot = h ? slot1 : slot0;
+                    const uint32_t vb = sR + slot * C::kPieceBytes;  // keys 64 h .. 64 h + 63 of V_it
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4)
-                        mma_ts(tmem + C::kOCol0 + x * D, tmem + PPCfg<D>::scol(x) + (k0 + k4) * 8,
-                               smem_desc_sw128(vb_ + (k0 + k4) * 2048, C::kChunkBytes, 1024), idO,
-                               (it >= 2 || k4 > 0) ? 1u : 0u);
+                        mma_ts(tmem + kOCol, pcol + (4 * h + k4) * 8,
+                               smem_desc_sw128(vb + k4 * 2048, C::kPieceBytes / C::kChunks, 1024), idO,
+                               (it > 0 || h > 0 || k4 > 0) ? 1u : 0u);
+                    mma_commit(bars.empty(slot));
                 }
-                mma_commit(bars.vempty(s));
-                if (it + 2 < n) {
-                    if (!(ok = issue_s(it + 2))) break;
-                } else {
-                    mma_commit(bars.odone(x));
-                }
+                q += 2;
+                mma_commit(bars.odone());
             }
             if (!ok) {
                 // let every MMA already issued finish before tensor memory is released
@@ -1130,74 +980,50 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             }
         }
     } else {
-        // ------------------------------------------------------------ softmax, one warpgroup per parity
-        const int x = warp >> 2;  // visits x, x + 2, x + 4, ...
-        const int r = tid & 127;  // row within the tile == tensor memory lane
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const uint32_t scol = lane_base + PPCfg<D>::scol(x);
-        const uint32_t ocol = lane_base + C::kOCol0 + x * D;
+        // ------------------------------------------------------------ softmax warps 0-3
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const float sl2 = fabsf(p.scale) * kLog2e;  // S holds sign(s) Q K^T
-        // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each 64-key half of a
-        // visited block is kept or removed for the whole warp
-        const uint8_t *wmask = fine ? hm + (size_t)(2 * tile + (warp & 3) / 2) * mnb : nullptr;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        int vis = -1, jv = -1;  // the visit and block reached so far (fine masks)
-        for (int it = x, lk = 0; it < n; it += 2, ++lk) {
-            bool keep_lo = true, keep_hi = true;
+        // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each
+        // 64-key half of a visited block is kept or removed for the whole warp.
+        const bool fine = hm != nullptr && mb == 64;
+        const uint8_t *wmask = fine ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
+        int j = -1;  // key block of iteration it (tracked only for fine masks)
+        for (int it = 0; it < n; ++it) {
+            const int b = it & 1;
+            bool half_kept[2] = {true, true};
             if (fine) {
-                while (vis < it) {
-                    jv = next_block(jv);
-                    ++vis;
-                }
-                keep_lo = wmask[2 * jv] != 0;
-                keep_hi = wmask[2 * jv + 1] != 0;
+                j = next_block(j);
+                half_kept[0] = wmask[2 * j] != 0;
+                half_kept[1] = wmask[2 * j + 1] != 0;
             }
-            ok = mbar_wait(bars.sfull(x), (uint32_t)lk & 1u, abort_flag, p.dev_status);
+            ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // S in two 64-column halves, so that only 64 scores are live at a time (as in the
-            // two-tile kernel): the max of each kept half, the exps of the high half while it is
-            // in registers, then the low half loaded again; P of the high half (columns 32..63,
-            // which hold S of keys 32..63) is written only after that reload
-            uint32_t rr[2][32];
-            float mlo = -INFINITY, mhi = -INFINITY;
-            if (keep_lo) {
-                tmem_ld32(scol + 0, rr[0]);
-                tmem_ld32(scol + 32, rr[1]);
-                tmem_wait_ld();
-                reg_fence(rr[0]);
-                reg_fence(rr[1]);
-                float mx4[4];
+            const uint32_t scol = lane_base + (b ? kSCol1 : kSCol0);
+            uint32_t r[4][32];
+            tmem_ld32(scol + 0, r[0]);
+            tmem_ld32(scol + 32, r[1]);
+            tmem_ld32(scol + 64, r[2]);
+            tmem_ld32(scol + 96, r[3]);
+            tmem_wait_ld();
+            reg_fence(r[0]);
+            reg_fence(r[1]);
+            reg_fence(r[2]);
+            reg_fence(r[3]);
+            // row max: four independent chains (one per 32-column chunk), then combined
+            float mxq[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
-                    mx4[c] = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            for (int q = 0; q < 4; ++q) {
+                mxq[q] = fmaxf(__uint_as_float(r[q][0]), __uint_as_float(r[q][1]));
 #pragma unroll
-                    for (int t = 1; t < 8; ++t)
-                        mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
-                }
-                mlo = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                for (int t = 1; t < 16; ++t)
+                    mxq[q] = fmax3(mxq[q], __uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1]));
+                if (!half_kept[q >> 1]) mxq[q] = -INFINITY;
             }
-            if (keep_hi) {
-                tmem_ld32(scol + 64, rr[0]);
-                tmem_ld32(scol + 96, rr[1]);
-                tmem_wait_ld();
-                reg_fence(rr[0]);
-                reg_fence(rr[1]);
-                float mx4[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
-                    mx4[c] = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
-#pragma unroll
-                    for (int t = 1; t < 8; ++t)
-                        mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
-                }
-                mhi = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-            }
-            const float mx = fmaxf(mlo, mhi);
+            const float mx = fmaxf(fmax3(mxq[0], mxq[1], mxq[2]), mxq[3]);
             // a warp with nothing kept so far keeps m_used = -inf
             const float m_new = mx == -INFINITY ? m_used : fmaxf(m_used, mx * sl2);
             float alpha = 1.f;
@@ -1205,156 +1031,112 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 alpha = ex2(m_used - m_new);
                 m_used = m_new;
             }
-            // O_x is complete up to this warpgroup's previous block (S_x(it) was issued after
-            // PV_x(it - 2)), and PV_x(it) waits for this warpgroup: rescale it here
-            if (lk > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(ocol + c0, o);
-                    tmem_wait_ld();
-                    reg_fence(o);
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-                    tmem_st32(ocol + c0, o);
-                }
-            }
+            // p = 2^(s log2e S - m): pairs on the packed FMA path, exps on MUFU
             const uint64_t sl2x2 = f2_pack(sl2, sl2);
             const uint64_t negm2 = f2_pack(-m_used, -m_used);
-            uint64_t sumq[4];
-            uint32_t pkh[2][16];
+            uint64_t sumq[4];  // four independent row-sum chains
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-                sumq[2 + qq] = f2_pack(0.f, 0.f);
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    if (!keep_hi) {
-                        pkh[qq][t] = 0u;
-                        continue;
-                    }
-                    const uint64_t x2 =
-                        f2_fma(f2_pack(__uint_as_float(rr[qq][2 * t]), __uint_as_float(rr[qq][2 * t + 1])), sl2x2,
-                               negm2);
-                    float x0, x1;
-                    f2_unpack(x2, x0, x1);
-                    const float y0 = ex2(x0), y1 = ex2(x1);
-                    sumq[2 + qq] = f2_add(sumq[2 + qq], f2_pack(y0, y1));
-                    pkh[qq][t] = pack_bf16(y0, y1);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) sumq[q] = f2_pack(0.f, 0.f);
-            if (keep_lo && keep_hi) {  // (with the high half removed, rr still holds the low half)
-                tmem_ld32(scol + 0, rr[0]);
-                tmem_ld32(scol + 32, rr[1]);
-                tmem_wait_ld();
-                reg_fence(rr[0]);
-                reg_fence(rr[1]);
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int q = 0; q < 4; ++q) {
+                sumq[q] = f2_pack(0.f, 0.f);
                 uint32_t pk[16];
+                if (!half_kept[q >> 1]) {
+                    // removed half: P = 0, nothing added to the row sum
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) pk[t] = 0u;
+                    tmem_st16(scol + q * 16, pk);
+                    continue;
+                }
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    if (!keep_lo) {
-                        pk[t] = 0u;
-                        continue;
-                    }
-                    const uint64_t x2 =
-                        f2_fma(f2_pack(__uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1])), sl2x2,
-                               negm2);
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[q][2 * t]), __uint_as_float(r[q][2 * t + 1])),
+                                               sl2x2, negm2);
                     float x0, x1;
                     f2_unpack(x2, x0, x1);
-                    const float y0 = ex2(x0), y1 = ex2(x1);
-                    sumq[q] = f2_add(sumq[q], f2_pack(y0, y1));
+                    const uint64_t y2 = f2_pack(ex2(x0), ex2(x1));
+                    sumq[q] = f2_add(sumq[q], y2);
+                    float y0, y1;
+                    f2_unpack(y2, y0, y1);
                     pk[t] = pack_bf16(y0, y1);
                 }
                 tmem_st16(scol + q * 16, pk);
             }
-            tmem_st16(scol + 32, pkh[0]);
-            tmem_st16(scol + 48, pkh[1]);
             float rs0, rs1;
             f2_unpack(f2_add(f2_add(sumq[0], sumq[1]), f2_add(sumq[2], sumq[3])), rs0, rs1);
-            l = l * alpha + (rs0 + rs1);
+            const float rs = rs0 + rs1;
+            l = l * alpha + rs;
             tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bars.pfull(x));
-        }
-        if (n == 0) {
-            // every key block removed: O = 0, LSE = -inf (warpgroup 0 writes the rows)
-            if (x == 0) {
-                const size_t grow = (size_t)row0 + r;
-                uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
-                for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
-                LSE[grow] = -INFINITY;
-            }
-        } else {
-            // both warpgroups' last PV: after these every MMA of the tile has completed, so the Q
-            // tile and the K ring are idle (a warpgroup with no block of its own, n == 1, must not
-            // touch the K ring while the other's S still reads it)
-            if (ok) {
-                for (int y = 0; y < 2 && ok; ++y)
-                    if (n > y) ok = mbar_wait(bars.odone(y), 0, abort_flag, p.dev_status);
+            if (it > 0) {
+                ok = mbar_wait(bars.odone(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status);
                 ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
                 tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + kOCol + c0, o);
+                        tmem_wait_ld();
+                        reg_fence(o);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                        tmem_st32(lane_base + kOCol + c0, o);
+                    }
+                    tmem_wait_st();
+                }
             }
-            // Merge.  Both warpgroups publish (m_x, l_x) in the idle K ring and meet at a named
-            // barrier (whatever `ok` says, so that no warp waits there for one that gave up).
-            // Warpgroup x then merges columns [x d/2, (x + 1) d/2) of O for its rows into the Q
-            // tile, in the 128-byte-swizzled layout of the 64-column TMA box.
-            float *stat = reinterpret_cast<float *>(sm + C::kStatOff);
-            stat[(2 * x) * BM + r] = m_used;
-            stat[(2 * x + 1) * BM + r] = l;
-            named_bar_sync(1, 256);
-            const float m0 = stat[r], l0 = stat[BM + r], m1 = stat[2 * BM + r], l1 = stat[3 * BM + r];
-            const float m = fmaxf(m0, m1);
-            // a warpgroup with no kept score in this row (or no block at all: n == 1 leaves O_1
-            // unwritten) contributes nothing; select rather than multiply, since O_x is then
-            // undefined
-            const float a0 = l0 > 0.f ? ex2(m0 - m) : 0.f;
-            const float a1 = l1 > 0.f ? ex2(m1 - m) : 0.f;
-            const float lt = a0 * l0 + a1 * l1;
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
-            const float w0 = a0 * inv, w1 = a1 * inv;
+            tc_fence_before();
+            mbar_arrive(bars.pfull(b));
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && n > 0) {
+            ok = mbar_wait(bars.odone(), (uint32_t)(n - 1) & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        const size_t grow = (size_t)row0 + tid;
+        if (n > 0) {
+            // O leaves through the Q tile (the last MMA that read it completed before odone):
+            // rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
+            // stores the tile.  The four warps meet at the named barrier whatever `ok` says.
             uint8_t *stage = sm + C::kQOff;
             if (ok) {
-                const uint32_t o0col = lane_base + C::kOCol0, o1col = lane_base + C::kOCol0 + D;
+                // a row whose every visited score was removed (64-row masks) has l = 0:
+                // O = 0 and LSE = -inf, with the tensor-memory loads still warp-wide
+                const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-                for (int c0 = x * (D / 2); c0 < (x + 1) * (D / 2); c0 += 32) {
-                    uint32_t u0[32], u1[32];
-                    tmem_ld32(o0col + c0, u0);
-                    tmem_ld32(o1col + c0, u1);
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kOCol + c0, o);
                     tmem_wait_ld();
-                    reg_fence(u0);
-                    reg_fence(u1);
+                    reg_fence(o);
                     uint32_t pk[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const float v0 = (w0 != 0.f ? w0 * __uint_as_float(u0[2 * t]) : 0.f) +
-                                         (w1 != 0.f ? w1 * __uint_as_float(u1[2 * t]) : 0.f);
-                        const float v1 = (w0 != 0.f ? w0 * __uint_as_float(u0[2 * t + 1]) : 0.f) +
-                                         (w1 != 0.f ? w1 * __uint_as_float(u1[2 * t + 1]) : 0.f);
-                        pk[t] = pack_bf16(v0, v1);
-                    }
-                    uint8_t *slab = stage + (c0 >> 6) * C::kChunkBytes + r * 128;
+                    for (int t = 0; t < 16; ++t)
+                        pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                    uint8_t *slab = stage + (c0 >> 6) * C::kChunkBytes + tid * 128;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int u = ((c0 & 63) >> 3) + v;  // 16-byte unit within the 128-byte row
-                        *reinterpret_cast<uint4 *>(slab + ((u ^ (r & 7)) << 4)) =
+                        *reinterpret_cast<uint4 *>(slab + ((u ^ (tid & 7)) << 4)) =
                             make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                     }
                 }
-                if (x == 0) LSE[(size_t)row0 + r] = lt > 0.f ? (m + __log2f(lt)) * kLn2 : -INFINITY;
+                LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
                 fence_proxy_async_smem();
             }
-            named_bar_sync(1, 256);
-            if (tid == 0 && !*abort_flag) {
+            named_bar_sync(1, 128);
+            if (tid == 0 && ok) {
                 const uint32_t src = smem_addr(stage);
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&tmO, c * 64, row0, src + c * C::kChunkBytes);
                 bulk_commit();
                 bulk_wait_all();
             }
+        } else {
+            // every key block removed: O = 0, LSE = -inf
+            uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
+            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
+            LSE[grow] = -INFINITY;
         }
     }
 
@@ -1362,25 +1144,12 @@ fwd_bf16_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     if (n == 0 && tid == 0) mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
-    if (warp == kSplMmaWarp) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int D>
-cudaError_t launch_split(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
-    auto kern = fwd_bf16_split_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SplCfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    dim3 grid(p.N / BM, p.B * p.H);
-    {
-        ProfScope prof_("fwd_bf16", st);
-        kern<<<grid, kSplThreads, SplCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p,
-                                                                static_cast<__nv_bfloat16 *>(O), LSE);
-    }
-    return cudaGetLastError();
-}
 
 template <int D>
 cudaError_t launch_pp(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
@@ -1410,19 +1179,29 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
     return cudaGetLastError();
 }
 
+cudaError_t launch_ring(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
+    auto kern = fwd_bf16_ring_kernel<256>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RingCfg<256>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.N / BM, p.B * p.H);
+    {
+        ProfScope prof_("fwd_bf16", st);
+        kern<<<grid, kThreads, RingCfg<256>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p,
+                                                               static_cast<__nv_bfloat16 *>(O), LSE);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
-    // d = 64, 128: two query tiles per CTA when both visit every key block; otherwise (a block
-    // mask, or N % 256 != 0) one tile per CTA with its visited blocks split between two
-    // warpgroups.  d = 256 (two S buffers and O fill tensor memory): one tile, one warpgroup.
+    // two query tiles per CTA when both tiles visit every key block
+    const bool pp = p.mask == nullptr && p.N % (2 * BM) == 0;
     switch (p.d) {
-        case 64: return (p.mask == nullptr && p.N % (2 * BM) == 0) ? launch_pp<64>(p, maps, O, LSE, st)
-                                                                  : launch_split<64>(p, maps, O, LSE, st);
-        case 128: return (p.mask == nullptr && p.N % (2 * BM) == 0) ? launch_pp<128>(p, maps, O, LSE, st)
-                                                                   : launch_split<128>(p, maps, O, LSE, st);
-        case 256: return launch_d<256>(p, maps, O, LSE, st);
+        case 64: return pp ? launch_pp<64>(p, maps, O, LSE, st) : launch_d<64>(p, maps, O, LSE, st);
+        case 128: return pp ? launch_pp<128>(p, maps, O, LSE, st) : launch_d<128>(p, maps, O, LSE, st);
+        case 256: return launch_ring(p, maps, O, LSE, st);
         default: return cudaErrorNotSupported;
     }
 }

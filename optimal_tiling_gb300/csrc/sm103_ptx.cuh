@@ -315,35 +315,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// 2^x for a pair, evaluated on the FMA pipe instead of MUFU.  Cody-Waite split
-// x = n + f, n = round(x) (the 1.5 * 2^23 rounding constant), f in [-1/2, 1/2];
-// 2^f by a degree-3 polynomial minimising the relative error on [-1/2, 1/2]
-// (coefficients from csrc/gen_exp2_poly.py, max relative error 7.5e-5); 2^n is
-// added into the exponent field: the bits of the rounded sum are 0x4B400000 + n,
-// and (0x4B400000 << 23) vanishes mod 2^32, so bits(t) << 23 == n << 23.
-// Inputs below -125 are clamped there (the result is then < 2^-124, a weight that
-// rounds away in every sum it enters).
-__device__ __forceinline__ uint64_t exp2_poly_pair(uint64_t x) {
-    float x0, x1;
-    f2_unpack(x, x0, x1);
-    x = f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-    const uint64_t kRound = f2_pack(12582912.f, 12582912.f);
-    const uint64_t kNegRound = f2_pack(-12582912.f, -12582912.f);
-    const uint64_t kNegOne = f2_pack(-1.f, -1.f);
-    const uint64_t t = f2_add(x, kRound);
-    const uint64_t n = f2_add(t, kNegRound);
-    const uint64_t f = f2_fma(n, kNegOne, x);
-    uint64_t pz = f2_fma(f2_pack(5.517166853e-02f, 5.517166853e-02f), f, f2_pack(2.426111251e-01f, 2.426111251e-01f));
-    pz = f2_fma(pz, f, f2_pack(6.932609677e-01f, 6.932609677e-01f));
-    pz = f2_fma(pz, f, f2_pack(9.999280572e-01f, 9.999280572e-01f));
-    float p0, p1, t0, t1;
-    f2_unpack(pz, p0, p1);
-    f2_unpack(t, t0, t1);
-    const float y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-    const float y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-    return f2_pack(y0, y1);
-}
-
 // Pack two fp32 into one 32-bit word of bf16 (lo in bits 0-15), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;

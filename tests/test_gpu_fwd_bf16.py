@@ -64,11 +64,10 @@ def test_many_key_blocks_and_large_scale(oracle_mod, d):
 @pytest.mark.parametrize("d", [64, 128])
 def test_all_ones_mask_matches_no_mask(oracle_mod, d):
     """An all-ones mask removes nothing.  Without a mask (N % 256 == 0) two query tiles
-    share a CTA; with one, a single tile's key blocks are split between two warpgroups
-    whose partial states are merged at the end, so the two differ only in rounding: both
-    against the oracle, and against each other within the same bound.  Two masks that
-    keep the same scores (128-blocks, and the same pattern as 64-blocks) take the same
-    path and agree bit for bit."""
+    share a CTA; with one, each tile has a CTA of its own, so the two differ only in
+    rounding: both against the oracle, and against each other within the same bound.
+    Two masks that keep the same scores (128-blocks, and the same pattern as 64-blocks)
+    take the same path and agree bit for bit."""
     x = inputs.make_inputs(1, 2, 512, d, torch.bfloat16, seed=11 + d, with_do=False)
     O1, L1 = _check_full(x, 0.1, oracle_mod)
     ones = torch.ones((4, 4), dtype=torch.uint8)
@@ -81,10 +80,9 @@ def test_all_ones_mask_matches_no_mask(oracle_mod, d):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("blocks", [1, 2, 3, 5])
-def test_split_key_blocks_few_visits(oracle_mod, d, blocks):
-    """Query tiles that visit 1, 2, 3 or 5 key blocks under a mask: with one block the
-    second warpgroup has nothing to do and its (undefined) accumulator must not enter
-    the merge; with an odd count the warpgroups end on different blocks."""
+def test_few_visited_key_blocks(oracle_mod, d, blocks):
+    """Query tiles that visit 1, 2, 3 or 5 key blocks under a mask, so that the double
+    buffered S and the K/V ring run with fewer blocks than buffers and stages."""
     N = 128 * 6
     x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=100 + blocks + d, with_do=False)
     m = torch.zeros((6, 6), dtype=torch.uint8)
