@@ -206,11 +206,12 @@ def run_cuda(args):
 
     def step():
         attn.attn_fwd(q, k, v, w.scale, block_mask=dmask, out=o, lse=lse, stream=stream)
-        attn.attn_bwd(q, k, v, o, do, lse, w.scale, block_mask=dmask, dq=dq, dk=dk, dv=dv, workspace=wspace,
-                      stream=stream)
+        if not args.fwd_only:
+            attn.attn_bwd(q, k, v, o, do, lse, w.scale, block_mask=dmask, dq=dq, dk=dk, dv=dv, workspace=wspace,
+                          stream=stream)
 
     fwd_flops = iomodel.fwd_flops(N, d, heads) * kept
-    bwd_flops = iomodel.bwd_flops(N, d, heads) * kept
+    bwd_flops = 0.0 if args.fwd_only else iomodel.bwd_flops(N, d, heads) * kept
     step_flops = fwd_flops + bwd_flops
 
     for _ in range(args.warmup):
@@ -272,7 +273,7 @@ def run_cuda(args):
     gpu_launches = sum(n for (n, t) in prof.values())
 
     # ---------------------------------------------------------------- end to end (host buffers)
-    e2e = _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist)
+    e2e = _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only=args.fwd_only)
 
     result = {
         "metric": METRIC,
@@ -287,7 +288,8 @@ def run_cuda(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{w.name}: fused fwd+bwd, B={B} H={H} N={N} d={d}, s=1/sqrt(d), "
+        "config": {"workload": f"{w.name}: fused {'fwd' if args.fwd_only else 'fwd+bwd'}, B={B} H={H} N={N} d={d}, "
+                               f"s=1/sqrt(d), "
                                f"{'block mask (band + 10% random)' if mask is not None else 'no mask'}",
                    "B": B, "H": H, "N": N, "d": d, "kept_block_fraction": round(kept, 5),
                    "parallelism": f"heads independent per GPU x{ws} (no collective)",
@@ -295,10 +297,11 @@ def run_cuda(args):
                          % (4 * q.numel() * 2 // 2 ** 20)},
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 1),
                 "frac_of_peak": round(fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak, 4)},
-        "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 1),
-                "frac_of_peak": round(bwd_flops / (bwd_ms * 1e-3) / 1e12 / peak, 4),
-                "kernels_ms": {"bwd_pre": round(pre_ms, 4), "bwd_main": round(main_ms, 4),
-                               "bwd_kv_finish": round(fin_ms, 4), "bwd_dq_convert": round(conv_ms, 4)}},
+        "bwd": None if args.fwd_only else {
+            "ms": round(bwd_ms, 4), "tflops": round(bwd_flops / (bwd_ms * 1e-3) / 1e12, 1),
+            "frac_of_peak": round(bwd_flops / (bwd_ms * 1e-3) / 1e12 / peak, 4),
+            "kernels_ms": {"bwd_pre": round(pre_ms, 4), "bwd_main": round(main_ms, 4),
+                           "bwd_kv_finish": round(fin_ms, 4), "bwd_dq_convert": round(conv_ms, 4)}},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
@@ -383,7 +386,7 @@ def _io_model(iomodel, N, d, heads, kept, peaks, brief=False):
     }
 
 
-def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist):
+def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only=False):
     """Same metric through the public API with host buffers.  Every step copies its
     inputs (Q, K, V, dO) host -> device from pinned memory, runs fwd + bwd, and
     copies every result (O, LSE, dQ, dK, dV) device -> host, all inside the timed
@@ -392,12 +395,13 @@ def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist):
     step i's results are copied back on a third stream while step i+1 computes
     (two device buffer sets, ordered with CUDA events)."""
     B, H, N, d = w.shape
-    names = ("q", "k", "v", "do")
+    names = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
+    n_out = 1 if fwd_only else 4   # O (and dQ, dK, dV), then LSE
     host_in = [{n: x[n].contiguous().pin_memory() for n in names} for _ in range(2)]
-    host_out = [[torch.empty(x["q"].shape, dtype=x["q"].dtype).pin_memory() for _ in range(4)] +
+    host_out = [[torch.empty(x["q"].shape, dtype=x["q"].dtype).pin_memory() for _ in range(n_out)] +
                 [torch.empty((B, H, N), dtype=torch.float32).pin_memory()] for _ in range(2)]
     dev_in = [{n: torch.empty_like(x[n], device=dev) for n in names} for _ in range(2)]
-    dev_out = [[torch.empty_like(x["q"], device=dev) for _ in range(4)] +
+    dev_out = [[torch.empty_like(x["q"], device=dev) for _ in range(n_out)] +
                [torch.empty((B, H, N), device=dev, dtype=torch.float32)] for _ in range(2)]
     ws_bytes = attn.attn_bwd_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16)
     wsp = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8)
@@ -417,9 +421,10 @@ def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist):
         stream.wait_event(ev_in[b])
         stream.wait_event(ev_out[b])     # the previous results of this set were copied out
         di, do_ = dev_in[b], dev_out[b]
-        attn.attn_fwd(di["q"], di["k"], di["v"], w.scale, block_mask=dmask, out=do_[0], lse=do_[4], stream=stream)
-        attn.attn_bwd(di["q"], di["k"], di["v"], do_[0], di["do"], do_[4], w.scale, block_mask=dmask,
-                      dq=do_[1], dk=do_[2], dv=do_[3], workspace=wsp, stream=stream)
+        attn.attn_fwd(di["q"], di["k"], di["v"], w.scale, block_mask=dmask, out=do_[0], lse=do_[-1], stream=stream)
+        if not fwd_only:
+            attn.attn_bwd(di["q"], di["k"], di["v"], do_[0], di["do"], do_[-1], w.scale, block_mask=dmask,
+                          dq=do_[1], dk=do_[2], dv=do_[3], workspace=wsp, stream=stream)
         ev_done[b].record(stream)
 
     def d2h(b):
@@ -732,6 +737,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-comparison", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time the forward pass alone (for profiling one forward kernel; the step is fwd + bwd)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "cuda":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
