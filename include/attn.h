@@ -42,7 +42,7 @@
  *               that attn_device_status() reports as ATTN_ERR_TIMEOUT.
  *   Shapes      fp32: any N >= 1, 1 <= d <= 256 (SIMT kernels).
  *               bf16: N a multiple of 128; forward d in {64, 128, 256};
- *               backward d = 128; materialising forward d in {64, 128, 256};
+ *               backward d in {64, 128}; materialising forward d in {64, 128, 256};
  *               materialising backward d in {64, 128}.  All: B * H <= 65535
  *               and B * H * N <= 2^31.  Anything else returns ATTN_ERR_UNSUPPORTED.
  *   Scale       Any finite s, of either sign (a non-finite s is
