@@ -12,8 +12,9 @@
 // function:  E = exp(s Q K^T - c),  l = rowsum E,  O = E V / l,  LSE = c + ln l.
 //
 // Kernels (caller's stream): mat_init (zero l and the per-head key-norm max),
-// mat_norms (|q_i| and the per-head max |k_j|), mat_scores (tcgen05 S tile ->
-// E tile, bf16, TMA-stored; row sums of the stored values added into l),
+// mat_norms (|q_i| and the per-head max |k_j|), mat_scores (per query tile, the
+// kept key tiles' S on tcgen05 -> E tiles, bf16, TMA-stored; l = the row sums of
+// the stored values),
 // mat_output (the shared block GEMM of gemm_sm103.cuh: O = E V over the kept
 // key blocks, then O / l and LSE).
 // Key blocks removed by the block mask are neither written nor read.
@@ -31,6 +32,10 @@ using namespace ptx;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int BT = 128;  // tile rows / columns
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __global__ void mat_init_kernel(float *__restrict__ rowl, float *__restrict__ kmax, size_t rows, int heads) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows; i += (size_t)gridDim.x * blockDim.x)
@@ -68,110 +73,211 @@ __global__ void __launch_bounds__(256) mat_norms_kernel(const __nv_bfloat16 *__r
 
 template <int D>
 struct ScoreCfg {
-    static constexpr int kTile = BT * D * 2;       // Q or K tile
-    static constexpr int kSlab = BT * 128;
-    static constexpr int kQOff = 0, kKOff = kTile, kBarOff = 2 * kTile;
-    // at most four CTAs per SM, so that their 128 tensor-memory columns always fit
-    static constexpr int kSmemBytes = (2 * kTile + 64 + 1024) > 59 * 1024 ? (2 * kTile + 64 + 1024) : 59 * 1024;
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTile = BT * D * 2;           // a Q or K tile
+    static constexpr int kSlab = BT * 128;             // one 64-column slab of a 128-row tile
+    static constexpr int kStages = D == 256 ? 2 : 3;   // K ring depth (as deep as shared memory allows at d = 256)
+    static constexpr int kETile = BT * BT * 2;         // one bf16 E tile: two 64-column slabs
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kTile;
+    static constexpr int kEOff = kKOff + kStages * kTile;
+    static constexpr int kBarOff = kEOff + kETile;
+    // q, kfull[S], kempty[S], sfull[2], sfree[2], drain
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // kept key blocks of the CTA's mask row as a bit set, up to 32 * kMaxMaskWords blocks
+    static constexpr int kMaxMaskWords = 256;
+    static constexpr int kBitsOff = kMiscOff + 64;
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
-// One CTA per (key tile, query tile, head): S = Q K^T on tcgen05, then
-// E = exp(s S - c) as bf16 through shared memory to HBM with a TMA store.
+// One CTA per (query tile, head), 192 threads: warps 0-3 epilogue (row = tensor memory lane),
+// warp 4 TMA, warp 5 MMA.  The Q tile stays in shared memory while the kept key tiles stream
+// through a K ring; S = Q K^T alternates between two 128-column tensor-memory buffers, so the
+// next tile's product runs while the epilogue turns this one into E = exp(s S - c) (bf16) and
+// stores it with tensor stores from one staging tile.  Each row's sum of the stored values is
+// kept in a register and written once.  (One CTA per score tile, the earlier form, left one CTA
+// per SM at d = 256, whose loads, product, exps and store then ran one after another.)
 template <int D>
-__global__ void __launch_bounds__(128) mat_scores_kernel(const __grid_constant__ CUtensorMap tmQ,
-                                                         const __grid_constant__ CUtensorMap tmK,
-                                                         const __grid_constant__ CUtensorMap tmE, const Problem p,
-                                                         const float *__restrict__ qnorm,
-                                                         const float *__restrict__ kmax, float *__restrict__ rowl) {
+__global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                            const __grid_constant__ CUtensorMap tmK,
+                                                            const __grid_constant__ CUtensorMap tmE, const Problem p,
+                                                            const float *__restrict__ qnorm,
+                                                            const float *__restrict__ kmax, float *__restrict__ rowl) {
     using C = ScoreCfg<D>;
-    const int kt = blockIdx.x, qt = blockIdx.y, head = blockIdx.z;
-    const int nb = p.N / BT;
-    if (p.mask && p.mask[(size_t)qt * nb + kt] == 0) return;  // removed block: never written, never read
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t bar_ld = smem_addr(sm + C::kBarOff), bar_mma = bar_ld + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kBarOff + 16);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kBarOff + 24);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff);
-    const int q0 = head * p.N + qt * BT, k0 = head * p.N + kt * BT;
+    const uint32_t bar0 = smem_addr(sm + C::kBarOff);
+    auto kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto kempty = [&](int s) { return bar0 + 8u * (1 + S + s); };
+    auto sfull = [&](int b) { return bar0 + 8u * (1 + 2 * S + b); };
+    auto sfree = [&](int b) { return bar0 + 8u * (3 + 2 * S + b); };
+    const uint32_t bar_q = bar0, bar_drain = bar0 + 8u * (5 + 2 * S);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qt = blockIdx.x, head = blockIdx.y;
+    const int nb = p.N / BT;
+    const int q0 = head * p.N + qt * BT;
+    uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
+    const int nwords = (nb + 31) >> 5;
+    const bool use_bits = p.mask != nullptr && nwords <= C::kMaxMaskWords;
+    auto kept = [&](int k) { return p.mask == nullptr || p.mask[(size_t)qt * nb + k] != 0; };
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sE = smem_addr(sm + C::kEOff);
+
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(kfull(s), 1);
+            mbar_init(kempty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sfull(b), 1);
+            mbar_init(sfree(b), 128);
+        }
+        mbar_init(bar_drain, 1);
         fence_barrier_init();
+        // the Q tile is needed whatever the mask says: start its load before the mask is read
+        mbar_arrive_expect_tx(bar_q, C::kTile);
+        for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kSlab, &tmQ, c * 64, q0, bar_q);
     }
-    if (warp == 0) {
-        tmem_alloc(smem_addr(tmem_slot), 128);
+    if (use_bits) build_visit_bits(vwords, nb, kept);
+    if (warp == 5) {
+        tmem_alloc(smem_addr(tmem_slot), 256);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_ld, 2 * C::kTile);
-        for (int c = 0; c < D / 64; ++c) {
-            tma_load_2d(sQ + c * C::kSlab, &tmQ, c * 64, q0, bar_ld);
-            tma_load_2d(sK + c * C::kSlab, &tmK, c * 64, k0, bar_ld);
-        }
+    const VisitBits vb{vwords, nwords};
+    int n = nb;  // kept key tiles of this query tile
+    if (use_bits) {
+        n = vb.count();
+    } else if (p.mask != nullptr) {  // rows longer than the bit set: read the mask directly
+        n = 0;
+        for (int k = 0; k < nb; ++k) n += kept(k) ? 1 : 0;
     }
-    bool ok = mbar_wait(bar_ld, 0, abort_flag, p.dev_status);
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        constexpr uint32_t id = idesc_bf16_f32(BT, BT, false, false);
+    auto next_block = [&](int k) -> int {
+        if (p.mask == nullptr) return k + 1;
+        if (use_bits) return vb.next(k);
+        do {
+            ++k;
+        } while (!kept(k));
+        return k;
+    };
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tmK);
+            int k = -1;
+            for (int it = 0; it < n; ++it) {
+                k = next_block(k);
+                const int s = it % S;
+                if (it >= S && !mbar_wait(kempty(s), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, p.dev_status)) break;
+                mbar_arrive_expect_tx(kfull(s), C::kTile);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sK + s * C::kTile + c * C::kSlab, &tmK, c * 64, head * p.N + k * BT, kfull(s));
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t id = idesc_bf16_f32(BT, BT, false, false);
+            bool ok = mbar_wait(bar_q, 0, abort_flag, p.dev_status);
+            for (int it = 0; it < n && ok; ++it) {
+                const int s = it % S, b = it & 1;
+                if (!(ok = mbar_wait(kfull(s), (uint32_t)(it / S) & 1u, abort_flag, p.dev_status))) break;
+                // the epilogue has read S of tile it - 2 out of this buffer
+                if (it >= 2 && !(ok = mbar_wait(sfree(b), (uint32_t)((it - 2) >> 1) & 1u, abort_flag, p.dev_status)))
+                    break;
+                tc_fence_after();
+                const uint32_t kb = sK + s * C::kTile;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::kSlab + (ks & 3) * 32;
-            mma_ss(tmem, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), id, ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::kSlab + (ks & 3) * 32;
+                    mma_ss(tmem + b * BT, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), id,
+                           ks > 0);
+                }
+                mma_commit(kempty(s));
+                mma_commit(sfull(b));
+            }
+            if (!ok) {
+                // let every MMA already issued finish before tensor memory is released
+                mma_commit(bar_drain);
+                mbar_wait(bar_drain, 0, abort_flag, p.dev_status);
+            }
         }
-        mma_commit(bar_mma);
-    }
-    ok = ok && mbar_wait(bar_mma, 0, abort_flag, p.dev_status);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    if (ok) {
+    } else {
+        // ------------------------------------------------------------ epilogue warps 0-3
+        // Every epilogue thread meets the named barriers of every tile whatever happens: after a
+        // failed (timed-out) wait the work is skipped but the barriers are kept.
         const float sl2 = p.scale * kLog2e;
         const float c2 = fabsf(p.scale) * qnorm[q0 + tid] * kmax[head] * kLog2e;  // row bound, log2 domain
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        uint8_t *stage = sm + C::kQOff;  // the Q tile is no longer read: stage E there (two 64-column slabs)
+        uint8_t *stage = sm + C::kEOff;
         float rs = 0.f;
+        bool ok = true;
+        int k = -1;
+        for (int it = 0; it < n; ++it) {
+            k = next_block(k);
+            const int b = it & 1;
+            ok = ok && mbar_wait(sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            // the staging tile is free once the previous tile's tensor stores have read it
+            if (tid == 0) bulk_wait_read_all();
+            named_bar_sync(1, 128);
+            if (ok) {
+                tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < BT; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + c0, r);
-            tmem_wait_ld();
-            reg_fence(r);
-            uint32_t pk[16];
+                for (int c0 = 0; c0 < BT; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + b * BT + c0, r);
+                    tmem_wait_ld();
+                    reg_fence(r);
+                    uint32_t pk[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                pk[t] = pack_bf16(ex2(fmaf(__uint_as_float(r[2 * t]), sl2, -c2)),
-                                  ex2(fmaf(__uint_as_float(r[2 * t + 1]), sl2, -c2)));
-                const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[t]));
-                rs += back.x + back.y;  // the row sum of the values actually stored
+                    for (int t = 0; t < 16; ++t) {
+                        pk[t] = pack_bf16(ex2(fmaf(__uint_as_float(r[2 * t]), sl2, -c2)),
+                                          ex2(fmaf(__uint_as_float(r[2 * t + 1]), sl2, -c2)));
+                        const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[t]));
+                        rs += back.x + back.y;  // the row sum of the values actually stored
+                    }
+                    const int slab = c0 / 64;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int chunk = ((c0 % 64) / 8) + v;  // 16-byte chunk within the 128-byte row
+                        const uint32_t off = slab * C::kSlab + tid * 128 + ((chunk ^ (tid & 7)) * 16);
+                        *reinterpret_cast<uint4 *>(stage + off) =
+                            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(sfree(b));
+                fence_proxy_async_smem();
             }
-            const int slab = c0 / 64;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int chunk = ((c0 % 64) / 8) + v;  // 16-byte chunk within the 128-byte row
-                const uint32_t off = slab * C::kSlab + tid * 128 + ((chunk ^ (tid & 7)) * 16);
-                *reinterpret_cast<uint4 *>(stage + off) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            named_bar_sync(1, 128);
+            if (tid == 0 && ok) {
+                tma_store_2d(&tmE, k * BT, q0, sE);
+                tma_store_2d(&tmE, k * BT + 64, q0, sE + C::kSlab);
+                bulk_commit();
             }
         }
-        atomicAdd(rowl + q0 + tid, rs);
-        fence_proxy_async_smem();
+        if (ok) rowl[q0 + tid] = rs;  // 0 for a row whose every key tile is removed
+        if (tid == 0) bulk_wait_all();
     }
+
+    // a tile that visits no key tile still received its Q tile: let that copy land first
+    if (n == 0 && tid == 0) mbar_wait(bar_q, 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok) {
-        tma_store_2d(&tmE, kt * BT, q0, sQ);
-        tma_store_2d(&tmE, kt * BT + 64, q0, sQ + C::kSlab);
-        bulk_commit();
-        bulk_wait_all();
-    }
-    if (warp == 0) {
+    if (warp == 5) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -220,7 +326,7 @@ cudaError_t launch_d(const Problem &p, const MatMaps &m, const void *Q, const vo
         return e;
     {
         ProfScope prof_("mat_scores", st);
-        ks<<<dim3(p.N / BT, p.N / BT, heads), 128, ScoreCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.e, p, qnorm, kmax, rowl);
+        ks<<<dim3(p.N / BT, heads), 192, ScoreCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.e, p, qnorm, kmax, rowl);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return gemm::launch_block_gemm<D, false>(
