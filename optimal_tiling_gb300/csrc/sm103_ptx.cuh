@@ -134,8 +134,6 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float *dst, uint32_t src, ui
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Every committed bulk group has finished reading shared memory (its writes may still be in flight).
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // All but the most recent committed bulk group have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_but_one() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
