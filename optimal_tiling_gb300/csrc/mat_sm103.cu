@@ -47,30 +47,45 @@ __global__ void mat_init_kernel(float *__restrict__ rowl, float *__restrict__ km
         for (int h = threadIdx.x; h < heads; h += blockDim.x) kmax[h] = 0.f;
 }
 
-// One warp per row: |q_row| into qnorm, max over the head's |k_row| into kmax.
+// |q_row| into qnorm and the max over the head's |k_row| into kmax.  A block of 8 warps takes
+// kNormRows consecutive rows of one head (N is a multiple of 128), a warp one row at a time; the
+// block's maximum goes into kmax with one atomic (one atomic per row put all rows of a head on
+// one address, and those atomics, not the reads, set the kernel's time).
+constexpr int kNormRows = 128;
+
 template <int D>
 __global__ void __launch_bounds__(256) mat_norms_kernel(const __nv_bfloat16 *__restrict__ Q,
                                                         const __nv_bfloat16 *__restrict__ K,
                                                         float *__restrict__ qnorm, float *__restrict__ kmax,
                                                         size_t rows, int N) {
-    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    float aq = 0.f, ak = 0.f;
-    for (int c = lane * 2; c < D; c += 64) {
-        const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(Q + row * D + c));
-        const float2 k = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(K + row * D + c));
-        aq = fmaf(q.x, q.x, fmaf(q.y, q.y, aq));
-        ak = fmaf(k.x, k.x, fmaf(k.y, k.y, ak));
+    __shared__ float wmax[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t row0 = (size_t)blockIdx.x * kNormRows;
+    float kmx = 0.f;
+    for (int rr = warp; rr < kNormRows; rr += 8) {
+        const size_t row = row0 + rr;
+        if (row >= rows) break;
+        float aq = 0.f, ak = 0.f;
+        for (int c = lane * 2; c < D; c += 64) {
+            const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(Q + row * D + c));
+            const float2 k = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(K + row * D + c));
+            aq = fmaf(q.x, q.x, fmaf(q.y, q.y, aq));
+            ak = fmaf(k.x, k.x, fmaf(k.y, k.y, ak));
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+            aq += __shfl_xor_sync(0xffffffffu, aq, off);
+            ak += __shfl_xor_sync(0xffffffffu, ak, off);
+        }
+        if (lane == 0) qnorm[row] = sqrtf(aq);
+        kmx = fmaxf(kmx, sqrtf(ak));
     }
-    for (int off = 16; off > 0; off >>= 1) {
-        aq += __shfl_xor_sync(0xffffffffu, aq, off);
-        ak += __shfl_xor_sync(0xffffffffu, ak, off);
-    }
-    if (lane == 0) {
-        qnorm[row] = sqrtf(aq);
+    if (lane == 0) wmax[warp] = kmx;
+    __syncthreads();
+    if (threadIdx.x == 0 && row0 < rows) {
+        float m = wmax[0];
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
         // norms are non-negative, so their bit patterns order like the values
-        atomicMax(reinterpret_cast<int *>(kmax) + row / N, __float_as_int(sqrtf(ak)));
+        atomicMax(reinterpret_cast<int *>(kmax) + row0 / N, __float_as_int(m));
     }
 }
 
@@ -81,10 +96,13 @@ struct ScoreCfg {
     static constexpr int kSlab = BT * 128;             // one 64-column slab of a 128-row tile
     static constexpr int kStages = D == 256 ? 2 : 3;   // K ring depth (as deep as shared memory allows at d = 256)
     static constexpr int kETile = BT * BT * 2;         // one bf16 E tile: two 64-column slabs
+    // staging tiles for E: two where they fit beside Q and the K ring without costing a CTA per
+    // SM (d = 128), so that a tile's epilogue need not wait for the previous tile's store to read
+    static constexpr int kEStages = D == 128 ? 2 : 1;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kTile;
     static constexpr int kEOff = kKOff + kStages * kTile;
-    static constexpr int kBarOff = kEOff + kETile;
+    static constexpr int kBarOff = kEOff + kEStages * kETile;
     // q, kfull[S], kempty[S], sfull[2], sfree[2], drain
     static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -95,15 +113,16 @@ struct ScoreCfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
-// One CTA per (query tile, head), 192 threads: warps 0-3 epilogue (row = tensor memory lane),
-// warp 4 TMA, warp 5 MMA.  The Q tile stays in shared memory while the kept key tiles stream
+// One CTA per (query tile, head), 320 threads: warps 0-7 epilogue (warp w: rows of tensor memory
+// lane quarter w % 4, score columns 64 (w / 4) .. + 63), warp 8 TMA, warp 9 MMA.  The Q tile stays in shared memory while the kept key tiles stream
 // through a K ring; S = Q K^T alternates between two 128-column tensor-memory buffers, so the
 // next tile's product runs while the epilogue turns this one into E = exp(s S - c) (bf16) and
-// stores it with tensor stores from one staging tile.  Each row's sum of the stored values is
-// kept in a register and written once.  (One CTA per score tile, the earlier form, left one CTA
+// stores it with tensor stores from one staging tile.  Each thread keeps its half of a row's sum
+// of the stored values in a register and adds it into l once.  (With one CTA per SM at d >= 128,
+// four epilogue warps, one thread per row, set the pace.)  (One CTA per score tile, the earlier form, left one CTA
 // per SM at d = 256, whose loads, product, exps and store then ran one after another.)
 template <int D>
-__global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constant__ CUtensorMap tmQ,
+__global__ void __launch_bounds__(320, D == 64 ? 2 : 1) mat_scores_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                             const __grid_constant__ CUtensorMap tmK,
                                                             const __grid_constant__ CUtensorMap tmE, const Problem p,
                                                             const float *__restrict__ qnorm,
@@ -139,7 +158,7 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sfull(b), 1);
-            mbar_init(sfree(b), 128);
+            mbar_init(sfree(b), 256);
         }
         mbar_init(bar_drain, 1);
         fence_barrier_init();
@@ -148,7 +167,7 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
         for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kSlab, &tmQ, c * 64, q0, bar_q);
     }
     if (use_bits) build_visit_bits(vwords, nb, kept);
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_addr(tmem_slot), 256);
         tmem_relinquish();
     }
@@ -173,7 +192,7 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
         return k;
     };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmK);
@@ -187,7 +206,7 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
                     tma_load_2d(sK + s * C::kTile + c * C::kSlab, &tmK, c * 64, head * p.N + k * BT, kfull(s));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             constexpr uint32_t id = idesc_bf16_f32(BT, BT, false, false);
@@ -216,13 +235,13 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue warps 0-3
+        // ------------------------------------------------------------ epilogue warps 0-7
         // Every epilogue thread meets the named barriers of every tile whatever happens: after a
         // failed (timed-out) wait the work is skipped but the barriers are kept.
+        const int hc = warp >> 2, row = tid & 127;  // score columns 64 hc .. 64 hc + 63 of this row
         const float sl2 = p.scale * kLog2e;
-        const float c2 = fabsf(p.scale) * qnorm[q0 + tid] * kmax[head] * kLog2e;  // row bound, log2 domain
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        uint8_t *stage = sm + C::kEOff;
+        const float c2 = fabsf(p.scale) * qnorm[q0 + row] * kmax[head] * kLog2e;  // row bound, log2 domain
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         float rs = 0.f;
         bool ok = true;
         int k = -1;
@@ -231,13 +250,19 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
             const int b = it & 1;
             ok = ok && mbar_wait(sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
-            // the staging tile is free once the previous tile's tensor stores have read it
-            if (tid == 0) bulk_wait_read_all();
-            named_bar_sync(1, 128);
+            // this tile's staging tile is free once the stores issued from it kEStages tiles ago
+            // have read it
+            uint8_t *stage = sm + C::kEOff + (it % C::kEStages) * C::kETile;
+            const uint32_t sEs = sE + (it % C::kEStages) * C::kETile;
+            if (tid == 0) {
+                if (C::kEStages == 2) bulk_wait_read_but_one();
+                else bulk_wait_read_all();
+            }
+            named_bar_sync(1, 256);
             if (ok) {
                 tc_fence_after();
 #pragma unroll 1
-                for (int c0 = 0; c0 < BT; c0 += 32) {
+                for (int c0 = 64 * hc; c0 < 64 * hc + 64; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(lane_base + b * BT + c0, r);
                     tmem_wait_ld();
@@ -254,7 +279,7 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
                         const int chunk = ((c0 % 64) / 8) + v;  // 16-byte chunk within the 128-byte row
-                        const uint32_t off = slab * C::kSlab + tid * 128 + ((chunk ^ (tid & 7)) * 16);
+                        const uint32_t off = slab * C::kSlab + row * 128 + ((chunk ^ (row & 7)) * 16);
                         *reinterpret_cast<uint4 *>(stage + off) =
                             make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                     }
@@ -263,14 +288,14 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
                 mbar_arrive(sfree(b));
                 fence_proxy_async_smem();
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(1, 256);
             if (tid == 0 && ok) {
-                tma_store_2d(&tmE, k * BT, q0, sE);
-                tma_store_2d(&tmE, k * BT + 64, q0, sE + C::kSlab);
+                tma_store_2d(&tmE, k * BT, q0, sEs);
+                tma_store_2d(&tmE, k * BT + 64, q0, sEs + C::kSlab);
                 bulk_commit();
             }
         }
-        if (ok) rowl[q0 + tid] = rs;  // 0 for a row whose every key tile is removed
+        if (ok && n > 0) atomicAdd(rowl + q0 + row, rs);  // l stays 0 for a row whose every key tile is removed
         if (tid == 0) bulk_wait_all();
     }
 
@@ -278,7 +303,7 @@ __global__ void __launch_bounds__(192, 1) mat_scores_kernel(const __grid_constan
     if (n == 0 && tid == 0) mbar_wait(bar_q, 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
     }
@@ -318,9 +343,8 @@ cudaError_t launch_d(const Problem &p, const MatMaps &m, const void *Q, const vo
     if (e != cudaSuccess) return e;
     {
         ProfScope prof_("mat_norms", st);
-        mat_norms_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(Q),
-                                                                         static_cast<const __nv_bfloat16 *>(K), qnorm,
-                                                                         kmax, rows, p.N);
+        mat_norms_kernel<D><<<(unsigned)((rows + kNormRows - 1) / kNormRows), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(Q), static_cast<const __nv_bfloat16 *>(K), qnorm, kmax, rows, p.N);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     auto ks = mat_scores_kernel<D>;
@@ -329,7 +353,7 @@ cudaError_t launch_d(const Problem &p, const MatMaps &m, const void *Q, const vo
         return e;
     {
         ProfScope prof_("mat_scores", st);
-        ks<<<dim3(p.N / BT, heads), 192, ScoreCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.e, p, qnorm, kmax, rowl);
+        ks<<<dim3(p.N / BT, heads), 320, ScoreCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.e, p, qnorm, kmax, rowl);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return gemm::launch_block_gemm<D, false>(
