@@ -771,6 +771,393 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
+// Two query tiles per CTA under a block mask shared by every head: tile A is query tile t of
+// head 2g and tile B the same query tile of head 2g + 1, so both visit the same key blocks and
+// alternate on the tensor core exactly as in the two-tile kernel above (MMA order per visited
+// block i: PV_A(i), S_A(i+1), PV_B(i), S_B(i+1); one issuing thread).  Their K and V differ, so
+// the K and V tiles of both heads stream through one ring of tile-sized pieces, loaded and
+// consumed in that order: K_A(0), K_B(0), then V_A(i), K_A(i+1), V_B(i), K_B(i+1) for every
+// visited block.  Used for 128 x 128 block masks shared by all heads (B * H even, d = 64, 128),
+// where pairing two tiles of one head would give them different visit lists.
+template <int D>
+struct PP2Cfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTileBytes = BM * D * 2;                  // a Q, K or V tile
+    static constexpr int kChunkBytes = BM * 128;
+    static constexpr int kPieces = D == 64 ? 10 : 5;               // ring of K / V tiles of either head
+    static constexpr int kQOff = 0;                                // Q_A, Q_B
+    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kRingOff + kPieces * kTileBytes;
+    // q, full[P], empty[P], sfull[2], pfull[2], odone[2], drain
+    static constexpr int kNumBars = 1 + 2 * kPieces + 2 + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    // visited key blocks as a bit set: masks with up to 32 * kMaxMaskWords blocks per row
+    static constexpr int kMaxMaskWords = 256;
+    static constexpr int kBitsOff = kMiscOff + 64;
+    static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
+    static constexpr uint32_t kOCol0 = 256;
+    static __device__ __forceinline__ uint32_t scol(int x) { return x ? 128u : 0u; }
+    static_assert(kOCol0 + 2 * D <= kTmemCols, "tensor memory budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+};
+
+struct PP2Bars {
+    uint32_t base;
+    int pieces;
+    __device__ uint32_t q() const { return base; }
+    __device__ uint32_t full(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t empty(int s) const { return base + 8u * (1 + pieces + s); }
+    __device__ uint32_t sfull(int x) const { return base + 8u * (1 + 2 * pieces + x); }
+    __device__ uint32_t pfull(int x) const { return base + 8u * (3 + 2 * pieces + x); }
+    __device__ uint32_t odone(int x) const { return base + 8u * (5 + 2 * pieces + x); }
+    __device__ uint32_t drain() const { return base + 8u * (7 + 2 * pieces); }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPPThreads, 1)
+fwd_bf16_pp2h_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const Problem p, __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
+    using C = PP2Cfg<D>;
+    constexpr int P = C::kPieces;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const PP2Bars bars{smem_addr(sm + C::kBarOff), P};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = blockIdx.x, pair = blockIdx.y;  // heads 2 pair and 2 pair + 1
+    const int nb = p.N / BN;
+    const uint8_t *hm = p.mask;                      // one 128-block mask for every head
+    const int mnb = p.mask_nb();
+    uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
+    const int nwords = (nb + 31) >> 5;
+    const bool use_bits = nwords <= C::kMaxMaskWords;
+    auto kept = [&](int j) { return visited(hm, 128, mnb, tile, j); };
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sR = smem_addr(sm + C::kRingOff);
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bars.q(), 1);
+        for (int s = 0; s < P; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bars.sfull(x), 1);
+            mbar_init(bars.pfull(x), 128);
+            mbar_init(bars.odone(x), 1);
+        }
+        mbar_init(bars.drain(), 1);
+        fence_barrier_init();
+        // the Q tiles are needed whatever the mask says: start their loads before the mask is read
+        mbar_arrive_expect_tx(bars.q(), 2 * C::kTileBytes);
+        for (int x = 0; x < 2; ++x)
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(sQ + x * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * 64,
+                            (2 * pair + x) * p.N + tile * BM, bars.q());
+    }
+    if (use_bits) build_visit_bits(vwords, nb, kept);
+    if (warp == kPPMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const VisitBits vb{vwords, nwords};
+    int n = 0;  // key blocks this query tile visits (in both heads)
+    if (use_bits) {
+        n = vb.count();
+    } else {  // rows longer than the bit set: read the mask directly
+        for (int j = 0; j < nb; ++j) n += kept(j) ? 1 : 0;
+    }
+    // the visited key block after j (callers ask only while one remains)
+    auto next_block = [&](int j) -> int {
+        if (use_bits) return vb.next(j);
+        do {
+            ++j;
+        } while (!kept(j));
+        return j;
+    };
+
+    if (warp == kPPTmaWarp) {
+        // ------------------------------------------------------------ producer (piece ring)
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            int q = 0;
+            // piece q (the K or V tile of head 2 pair + x at key block blk) into slot q % P, once
+            // the MMAs of piece q - P have released it
+            auto load = [&](int x, bool is_v, int blk) -> bool {
+                const int slot = q % P;
+                if (q >= P && !mbar_wait(bars.empty(slot), ((uint32_t)(q / P) & 1u) ^ 1u, abort_flag, p.dev_status))
+                    return false;
+                mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+                const int krow = (2 * pair + x) * p.N + blk * BN;
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_2d(sR + slot * C::kTileBytes + c * C::kChunkBytes, is_v ? &tmV : &tmK, c * 64, krow,
+                                bars.full(slot));
+                ++q;
+                return true;
+            };
+            int jk = next_block(-1), jv = jk;
+            bool ok = load(0, false, jk) && load(1, false, jk);
+            for (int i = 0; i < n && ok; ++i) {
+                const bool more = i + 1 < n;
+                if (more) jk = next_block(jk);
+                ok = load(0, true, jv) && (!more || load(0, false, jk)) && load(1, true, jv) &&
+                     (!more || load(1, false, jk));
+                jv = jk;
+            }
+        }
+    } else if (warp == kPPMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
+            const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
+            constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
+            auto wait_piece = [&](int qq) {
+                return mbar_wait(bars.full(qq % P), (uint32_t)(qq / P) & 1u, abort_flag, p.dev_status);
+            };
+            auto piece = [&](int qq) { return sR + (qq % P) * C::kTileBytes; };
+            auto mma_s = [&](int x, int qq) {
+                const uint32_t kb = piece(qq), qb = sQ + x * C::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+                    mma_ss(tmem + C::scol(x), smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                           idS, ks > 0);
+                }
+                mma_commit(bars.empty(qq % P));
+                mma_commit(bars.sfull(x));
+            };
+            auto mma_pv = [&](int x, int qq, bool first) {
+                const uint32_t vb = piece(qq);
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                    mma_ts(tmem + C::kOCol0 + x * D, tmem + C::scol(x) + ks * 8,
+                           smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO, (!first || ks > 0) ? 1u : 0u);
+                mma_commit(bars.empty(qq % P));
+            };
+            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status) && wait_piece(0);
+            if (ok) {
+                tc_fence_after();
+                mma_s(0, 0);
+                ok = wait_piece(1);
+            }
+            if (ok) {
+                tc_fence_after();
+                mma_s(1, 1);
+            }
+            int q = 2;
+            for (int i = 0; i < n && ok; ++i) {
+                const bool more = i + 1 < n;
+                const uint32_t ph = (uint32_t)i & 1u;
+                const int qa_v = q, qa_k = q + 1, qb_v = more ? q + 2 : q + 1, qb_k = q + 3;
+                q += more ? 4 : 2;
+                // V_A(i) and K_A(i+1) were loaded long ago: check them while tile A's softmax still
+                // runs, so that only P_A(i) is waited for on the path from softmax to PV
+                if (!(ok = wait_piece(qa_v))) break;
+                if (more && !(ok = wait_piece(qa_k))) break;
+                if (!(ok = mbar_wait(bars.pfull(0), ph, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                mma_pv(0, qa_v, i == 0);
+                if (more) mma_s(0, qa_k);
+                else mma_commit(bars.odone(0));
+                if (!(ok = wait_piece(qb_v))) break;
+                if (more && !(ok = wait_piece(qb_k))) break;
+                if (!(ok = mbar_wait(bars.pfull(1), ph, abort_flag, p.dev_status))) break;
+                tc_fence_after();
+                mma_pv(1, qb_v, i == 0);
+                if (more) mma_s(1, qb_k);
+                else mma_commit(bars.odone(1));
+            }
+            if (!ok) {
+                mma_commit(bars.drain());
+                mbar_wait(bars.drain(), 0, abort_flag, p.dev_status);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax, one tile per warpgroup
+        const int x = warp >> 2;  // 0: tile A (head 2g), 1: tile B (head 2g + 1)
+        const int r = tid & 127;  // row within the tile == tensor memory lane
+        const int rowx0 = (2 * pair + x) * p.N + tile * BM;  // first row of this warpgroup's tile
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t scol = lane_base + C::scol(x);
+        const uint32_t ocol = lane_base + C::kOCol0 + x * D;
+        const float sl2 = fabsf(p.scale) * kLog2e;  // S holds sign(s) Q K^T
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = mbar_wait(bars.sfull(x), (uint32_t)j & 1u, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            // S in two 64-column halves, so that only 64 scores are live at a time: the max over
+            // both halves, the exps of the high half (still in registers), then the low half
+            // loaded again; P of the high half (columns 32..63, which hold S of keys 32..63) is
+            // written only after that reload
+            uint32_t rr[2][32];
+            tmem_ld32(scol + 0, rr[0]);
+            tmem_ld32(scol + 32, rr[1]);
+            tmem_wait_ld();
+            reg_fence(rr[0]);
+            reg_fence(rr[1]);
+            // row max in four independent chains of 16-column runs (a single chain through the
+            // second half made the max a long dependent sequence)
+            float mx4[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
+                mx4[c] = fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1]));
+#pragma unroll
+                for (int t = 1; t < 8; ++t) mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+            }
+            tmem_ld32(scol + 64, rr[0]);
+            tmem_ld32(scol + 96, rr[1]);
+            tmem_wait_ld();
+            reg_fence(rr[0]);
+            reg_fence(rr[1]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t *v = &rr[c >> 1][16 * (c & 1)];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) mx4[c] = fmax3(mx4[c], __uint_as_float(v[2 * t]), __uint_as_float(v[2 * t + 1]));
+            }
+            const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+            const float m_new = fmaxf(m_used, mx * sl2);
+            float alpha = 1.f;
+            if (m_new > m_used + kRescaleThreshold) {
+                alpha = ex2(m_used - m_new);
+                m_used = m_new;
+            }
+            // O_X is complete up to block j-1 (S_X(j) was issued after PV_X(j-1)), and
+            // PV_X(j) waits for this warpgroup: rescale it here when a row's max moved.
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(ocol + c0, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    tmem_st32(ocol + c0, o);
+                }
+            }
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m_used, -m_used);
+            uint64_t sumq[4];
+            uint32_t pkh[2][16];
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+                sumq[2 + qq] = f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[qq][2 * t]), __uint_as_float(rr[qq][2 * t + 1])),
+                                               sl2x2, negm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[2 + qq] = f2_add(sumq[2 + qq], f2_pack(y0, y1));
+                    pkh[qq][t] = pack_bf16(y0, y1);
+                }
+            }
+            tmem_ld32(scol + 0, rr[0]);
+            tmem_ld32(scol + 32, rr[1]);
+            tmem_wait_ld();
+            reg_fence(rr[0]);
+            reg_fence(rr[1]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                sumq[q] = f2_pack(0.f, 0.f);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[q][2 * t]), __uint_as_float(rr[q][2 * t + 1])),
+                                               sl2x2, negm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float y0 = ex2(x0), y1 = ex2(x1);
+                    sumq[q] = f2_add(sumq[q], f2_pack(y0, y1));
+                    pk[t] = pack_bf16(y0, y1);
+                }
+                tmem_st16(scol + q * 16, pk);
+            }
+            tmem_st16(scol + 32, pkh[0]);
+            tmem_st16(scol + 48, pkh[1]);
+            float rs0, rs1;
+            f2_unpack(f2_add(f2_add(sumq[0], sumq[1]), f2_add(sumq[2], sumq[3])), rs0, rs1);
+            l = l * alpha + (rs0 + rs1);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bars.pfull(x));
+        }
+        if (n == 0) {
+            // every key block removed for this query tile: O = 0, LSE = -inf
+            const size_t grow = (size_t)rowx0 + r;
+            uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
+            for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
+            LSE[grow] = -INFINITY;
+            ok = false;
+        }
+        if (ok) {
+            ok = mbar_wait(bars.odone(x), 0, abort_flag, p.dev_status);
+            ok = __all_sync(0xffffffffu, ok);
+            tc_fence_after();
+        }
+        // O leaves through this tile's Q region (the last MMA that read Q_X completed before
+        // odone): rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
+        // stores the tile.  The tile's four warps meet at the named barrier whatever `ok` says.
+        uint8_t *stage = sm + C::kQOff + x * C::kTileBytes;
+        if (ok) {
+            const size_t grow = (size_t)rowx0 + r;
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(ocol + c0, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                uint8_t *slab = stage + (c0 >> 6) * C::kChunkBytes + r * 128;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int u = ((c0 & 63) >> 3) + v;  // 16-byte unit within the 128-byte row
+                    *reinterpret_cast<uint4 *>(slab + ((u ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            LSE[grow] = (m_used + __log2f(l)) * kLn2;
+            fence_proxy_async_smem();
+        }
+        named_bar_sync(1 + x, 128);
+        if (r == 0 && ok && n > 0) {
+            const uint32_t src = smem_addr(stage);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) tma_store_2d(&tmO, c * 64, rowx0, src + c * C::kChunkBytes);
+            bulk_commit();
+            bulk_wait_all();
+        }
+    }
+
+    // a tile pair that visits no key block still received its Q tiles: let those copies land first
+    if (n == 0 && tid == 0) mbar_wait(bars.q(), 0, abort_flag, p.dev_status);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kPPMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // d = 256, one query tile per CTA.  The Q tile takes 64 KB; one K and one V tile
 // (64 KB each) fit beside it, but then V of block j+1 can load only after PV of
 // block j, and the pass waits for that load every block.  Instead K and V stream
@@ -1179,6 +1566,20 @@ cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cu
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_pp2h(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
+    auto kern = fwd_bf16_pp2h_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PP2Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.N / BM, p.B * p.H / 2);
+    {
+        ProfScope prof_("fwd_bf16", st);
+        kern<<<grid, kPPThreads, PP2Cfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p,
+                                                               static_cast<__nv_bfloat16 *>(O), LSE);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_ring(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
     auto kern = fwd_bf16_ring_kernel<256>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RingCfg<256>::kSmemBytes);
@@ -1198,9 +1599,17 @@ cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, floa
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
     // two query tiles per CTA when both tiles visit every key block
     const bool pp = p.mask == nullptr && p.N % (2 * BM) == 0;
+    // or when both are the same query tile of two heads under one 128-block mask for every head
+    const bool pp2h = p.mask != nullptr && p.mask_stride == 0 && p.mask_block == 128 && (p.B * p.H) % 2 == 0;
     switch (p.d) {
-        case 64: return pp ? launch_pp<64>(p, maps, O, LSE, st) : launch_d<64>(p, maps, O, LSE, st);
-        case 128: return pp ? launch_pp<128>(p, maps, O, LSE, st) : launch_d<128>(p, maps, O, LSE, st);
+        case 64:
+            return pp     ? launch_pp<64>(p, maps, O, LSE, st)
+                   : pp2h ? launch_pp2h<64>(p, maps, O, LSE, st)
+                          : launch_d<64>(p, maps, O, LSE, st);
+        case 128:
+            return pp     ? launch_pp<128>(p, maps, O, LSE, st)
+                   : pp2h ? launch_pp2h<128>(p, maps, O, LSE, st)
+                          : launch_d<128>(p, maps, O, LSE, st);
         case 256: return launch_ring(p, maps, O, LSE, st);
         default: return cudaErrorNotSupported;
     }

@@ -64,10 +64,11 @@ def test_many_key_blocks_and_large_scale(oracle_mod, d):
 @pytest.mark.parametrize("d", [64, 128])
 def test_all_ones_mask_matches_no_mask(oracle_mod, d):
     """An all-ones mask removes nothing.  Without a mask (N % 256 == 0) two query tiles
-    share a CTA; with one, each tile has a CTA of its own, so the two differ only in
-    rounding: both against the oracle, and against each other within the same bound.
-    Two masks that keep the same scores (128-blocks, and the same pattern as 64-blocks)
-    take the same path and agree bit for bit."""
+    of one head share a CTA; with one 128-block mask for both heads, the same query tile
+    of the two heads shares one; with 64-blocks, each tile has a CTA of its own.  The
+    three differ only in rounding: each against the oracle, and against each other
+    within the same bound.  A 64-block mask and a per-head copy of the 128-block mask
+    keep the same scores and take the same kernel: they agree bit for bit."""
     x = inputs.make_inputs(1, 2, 512, d, torch.bfloat16, seed=11 + d, with_do=False)
     O1, L1 = _check_full(x, 0.1, oracle_mod)
     ones = torch.ones((4, 4), dtype=torch.uint8)
@@ -75,7 +76,11 @@ def test_all_ones_mask_matches_no_mask(oracle_mod, d):
     assert max_abs(O1, O2) <= TOL_BF16_O_ABS and lse_rel(L1, L2) <= TOL_BF16_LSE_REL
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     o3, l3 = attn.attn_fwd_masked(q, k, v, 0.1, mask=torch.ones((8, 8), dtype=torch.uint8, device=DEV), block=64)
-    assert np.array_equal(O2, o3.float().cpu().numpy()) and np.array_equal(L2, l3.cpu().numpy())
+    O3, L3 = o3.float().cpu().numpy(), l3.cpu().numpy()
+    assert max_abs(O2, O3) <= TOL_BF16_O_ABS and lse_rel(L2, L3) <= TOL_BF16_LSE_REL
+    o4, l4 = attn.attn_fwd_masked(q, k, v, 0.1, mask=torch.ones((1, 2, 4, 4), dtype=torch.uint8, device=DEV),
+                                  block=128)
+    assert np.array_equal(O3, o4.float().cpu().numpy()) and np.array_equal(L3, l4.cpu().numpy())
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -92,10 +97,14 @@ def test_few_visited_key_blocks(oracle_mod, d, blocks):
     _check_full(x, 1.0 / math.sqrt(d), oracle_mod, m)
 
 
+@pytest.mark.parametrize("BH", [(2, 1), (1, 3)])
 @pytest.mark.parametrize("d", [64, 128])
-def test_block_masks(oracle_mod, d):
+def test_block_masks(oracle_mod, d, BH):
+    """One mask for every head: with an even number of heads the same query tile of two
+    heads shares a CTA, with an odd number each tile has its own.  Block-diagonal, random,
+    and a single kept block (every other query tile visits nothing: O = 0, LSE = -inf)."""
     N = 768
-    x = inputs.make_inputs(2, 1, N, d, torch.bfloat16, seed=12, with_do=False)
+    x = inputs.make_inputs(*BH, N, d, torch.bfloat16, seed=12, with_do=False)
     s = 1.0 / math.sqrt(d)
     _check_full(x, s, oracle_mod, inputs.block_diagonal_mask(N))
     _check_full(x, s, oracle_mod, inputs.random_block_mask(N, seed=4, p=0.3))
@@ -166,11 +175,13 @@ def test_full_size_workloads_sampled(oracle_mod, name):
 def test_negative_scale(oracle_mod, d):
     """A negative score scale (the softmax of the first page's definition takes any real
     scores): the two-tile kernel (no mask, N % 256 == 0), the single-tile kernel (N = 384,
-    and under a block mask) against the oracle; and s Q K^T = |s| (-Q) K^T exactly, so the
-    call with -s equals the call with -Q and +s bit for bit."""
+    and under a block mask with an odd number of heads), the head-pair kernel (one block
+    mask, two heads) against the oracle; and s Q K^T = |s| (-Q) K^T exactly, so the call
+    with -s equals the call with -Q and +s bit for bit."""
     s = -1.0 / math.sqrt(d)
-    for N, mask in ((512, None), (384, None), (512, inputs.random_block_mask(512, seed=3, p=0.5))):
-        x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=N + d + 1, with_do=False)
+    m = inputs.random_block_mask(512, seed=3, p=0.5)
+    for N, H, mask in ((512, 2, None), (384, 2, None), (512, 2, m), (512, 3, m)):
+        x = inputs.make_inputs(1, H, N, d, torch.bfloat16, seed=N + d + H, with_do=False)
         O, L = _check_full(x, s, oracle_mod, mask)
         flipped = dict(x, q=-x["q"])
         O2, L2 = _fwd(flipped, -s, mask)
