@@ -41,10 +41,17 @@
  *               wait is bounded, and an expired wait sets a device status word
  *               that attn_device_status() reports as ATTN_ERR_TIMEOUT.
  *   Shapes      fp32: any N >= 1, 1 <= d <= 256 (SIMT kernels).
- *               bf16: N a multiple of 128; forward d in {64, 128, 256};
- *               backward d in {64, 128}; materialising forward d in {64, 128, 256};
- *               materialising backward d in {64, 128}.  All: B * H <= 65535
- *               and B * H * N <= 2^31.  Anything else returns ATTN_ERR_UNSUPPORTED.
+ *               bf16: fused forward any N >= 1, d in {64, 128, 256}; fused
+ *               backward any N >= 1, d in {64, 128}; materialising forward
+ *               (N a multiple of 128) d in {64, 128, 256}; materialising
+ *               backward (N a multiple of 128) d in {64, 128}.  When 128 does
+ *               not divide N, the last 128-row tile of each head is partial:
+ *               the kernels read the rows past N (the next head's, or zeros
+ *               past the end of the array) and give them no weight, and write
+ *               nothing past row N of any head.  All: B * H <= 65535 and
+ *               B * H * N <= 2^31 (bf16 backward: B * H * N' <= 2^31, N' = N
+ *               rounded up to a multiple of 64).  Anything else returns
+ *               ATTN_ERR_UNSUPPORTED.
  *   Scale       Any finite s, of either sign (a non-finite s is
  *               ATTN_ERR_INVALID_ARG).
  */
@@ -132,9 +139,11 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype d
  * Out: dQ, dK, dV [B,H,N,d] (dtype).
  * workspace: device scratch of at least attn_bwd_workspace_size() bytes
  *      (16-byte aligned, contents on entry ignored); it holds D and, for bf16,
- *      LSE log2(e) and the fp32 dQ accumulator.  For bf16 without a mask, when the current
- *      device's SM count does not divide the 128-key tiles and the last wave of
- *      tiles would be at most half full, the size also covers fp32 dK and dV of
+ *      LSE log2(e) and the fp32 dQ accumulator (these three with N rounded up
+ *      to a multiple of 64 rows per head).  For bf16 without a mask, when 128
+ *      divides N, the current device's SM count does not divide the 128-key
+ *      tiles and the last wave of tiles would be at most half full, the size
+ *      also covers fp32 dK and dV of
  *      that wave's tiles, which are then split into two query halves each (so
  *      that the wave takes half a tile's time); the size therefore depends on
  *      the current device.  A workspace that holds only those row terms and
@@ -166,8 +175,9 @@ ATTN_API attn_status attn_bwd_masked(const void *Q, const void *K, const void *V
  * Same arguments and results as attn_bwd, without the workspace: the scratch
  * comes from a fixed 64 MiB array compiled into the library, held in device
  * memory of every GPU that loads the library until the process exits.
- *   - Shapes whose row-term and dQ scratch exceeds 64 MiB (B*H*N rows of 4
- *     bytes, 8 + 4d bytes for bf16, each part rounded up to 256 bytes) return
+ *   - Shapes whose row-term and dQ scratch exceeds 64 MiB (fp32: B*H*N rows
+ *     of 4 bytes; bf16: B*H*N' rows of 8 + 4d bytes, N' = N rounded up to a
+ *     multiple of 64; each part rounded up to 256 bytes) return
  *     ATTN_ERR_WORKSPACE and launch nothing (bf16, d = 128: B*H*N up to
  *     about 129,000 rows; fp32: B*H*N up to 16 million rows).  The last-wave
  *     split of attn_bwd is used when its scratch fits as well.

@@ -124,8 +124,9 @@ attn_status check_common(int B, int H, int N, int d, attn_dtype dt) {
     return ATTN_OK;
 }
 
-bool bf16_fwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128 || d == 256); }
-bool bf16_bwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
+bool bf16_fwd_shape_ok(int N, int d) { return N >= 1 && (d == 64 || d == 128 || d == 256); }
+bool bf16_bwd_shape_ok(int N, int d) { return N >= 1 && (d == 64 || d == 128); }
+bool bf16_matfwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128 || d == 256); }
 bool bf16_matbwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
 
 attn_status launch_status(cudaError_t e) {
@@ -191,7 +192,8 @@ ProfScope::~ProfScope() {
 }
 
 size_t bwd_base_bytes(int B, int H, int N, int d, bool bf16) {
-    const size_t rows = (size_t)B * H * N;
+    // bf16: rows padded per head to the 64-row query block
+    const size_t rows = (size_t)B * H * (bf16 ? bwd_rows_per_head(N) : N);
     // D (and, for bf16, LSE log2(e) after it)
     size_t bytes = ((bf16 ? 2 : 1) * rows * sizeof(float) + 255) / 256 * 256;
     if (bf16) bytes += (rows * (size_t)d * sizeof(float) + 255) / 256 * 256;   // dQ accumulator
@@ -342,6 +344,9 @@ attn_status bwd_args_status(const void *Q, const void *K, const void *V, const v
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (dtype == ATTN_DTYPE_F32 && d > 256) return ATTN_ERR_UNSUPPORTED;
     if (dtype == ATTN_DTYPE_BF16 && !bf16_bwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    // the padded rows of the bf16 row terms and dQ accumulator are indexed in 32 bits too
+    if (dtype == ATTN_DTYPE_BF16 && (uint64_t)B * H * bwd_rows_per_head(N) > (1ull << 31))
+        return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -369,8 +374,9 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
             static_cast<const float *>(O), static_cast<const float *>(dO), LSE, static_cast<float *>(dQ),
             static_cast<float *>(dK), static_cast<float *>(dV), D, st));
     }
-    // D, LSE log2(e), then the fp32 dQ accumulator
-    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(2 * rows * sizeof(float), 256));
+    // D, LSE log2(e), then the fp32 dQ accumulator, each with N rounded up to 64 rows per head
+    const size_t prows = (size_t)B * H * attn::bwd_rows_per_head(N);
+    float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(2 * prows * sizeof(float), 256));
     // split the last wave (dense problems) when the workspace also holds the partial dK, dV
     int split = mask == nullptr ? attn::bwd_split_tiles(B, H, N) : 0;
     if (split > 0 && workspace_bytes < need + attn::bwd_split_bytes(split, d)) split = 0;
@@ -424,7 +430,7 @@ attn_status attn_fwd_materialized(const void *Q, const void *K, const void *V, v
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
         return ATTN_ERR_INVALID_ARG;
     if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (dtype != ATTN_DTYPE_BF16 || !bf16_fwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
+    if (dtype != ATTN_DTYPE_BF16 || !bf16_matfwd_shape_ok(N, d)) return ATTN_ERR_UNSUPPORTED;
     const size_t need = attn_fwd_materialized_workspace_size(B, H, N, d, dtype);
     if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
     int *status = device_status_ptr();

@@ -56,6 +56,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
@@ -141,34 +142,47 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // D_i = sum_t dO_it O_it and L2_i = LSE_i log2(e) (the row's log-sum-exp in the base-2 units of
 // the exponentials below); the dQ accumulator row is zeroed.  One warp per row.
 // The split tiles' partial dK, dV (kv4: kv_n4 float4) are zeroed grid-stride.
-template <int D>
+// D, L2 and the accumulator hold npad rows per head (N rounded up to the 64-row query block;
+// npad = N when 64 divides N, PAD = false): the rows from N on get D = 0 and L2 = +inf, so that
+// their probabilities, and with them their dS, are exactly zero in the main kernel.
+template <int D, bool PAD>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       float *__restrict__ Dv, float *__restrict__ dQacc,
                                                       size_t rows, float4 *__restrict__ kv4, size_t kv_n4,
-                                                      const float *__restrict__ LSE, float *__restrict__ L2) {
+                                                      const float *__restrict__ LSE, float *__restrict__ L2, int N,
+                                                      int npad) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < kv_n4; i += (size_t)gridDim.x * blockDim.x)
         kv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const size_t prow = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // row of the padded layout
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    constexpr int E = D / 32;  // elements per lane (2 or 4)
-    const __nv_bfloat16 *o = O + row * D + lane * E;
-    const __nv_bfloat16 *g = dO + row * D + lane * E;
+    if (prow >= rows) return;
+    size_t row = prow;  // row of O, dO and LSE
+    bool pad = false;
+    if constexpr (PAD) {
+        const size_t hh = prow / (size_t)npad, q = prow - hh * (size_t)npad;
+        pad = q >= (size_t)N;
+        row = hh * (size_t)N + q;
+    }
     float acc = 0.f;
+    if (!pad) {
+        constexpr int E = D / 32;  // elements per lane (2 or 4)
+        const __nv_bfloat16 *o = O + row * D + lane * E;
+        const __nv_bfloat16 *g = dO + row * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + e));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + e));
-        acc = fmaf(a.x, b.x, acc);
-        acc = fmaf(a.y, b.y, acc);
+        for (int e = 0; e < E; e += 2) {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + e));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + e));
+            acc = fmaf(a.x, b.x, acc);
+            acc = fmaf(a.y, b.y, acc);
+        }
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     }
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
-        Dv[row] = acc;
-        L2[row] = LSE[row] * kLog2e;
+        Dv[prow] = acc;
+        L2[prow] = pad ? INFINITY : LSE[row] * kLog2e;
     }
-    float4 *z = reinterpret_cast<float4 *>(dQacc + row * D);
+    float4 *z = reinterpret_cast<float4 *>(dQacc + prow * D);
     for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
@@ -177,7 +191,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
 // after split_from (in the order head * (N / 128) + x) belongs to the split last wave and its
 // CTA returns at once.  HALVES = true: grid 2 * (tiles - split_from), two CTAs per split tile,
 // each taking one half of the query blocks and adding fp32 partial dK, dV into kvacc.
-template <int D, bool HALVES>
+// TAIL (N % 128 != 0, never split): grid (ceil(N / 128), B * H).  The last key tile and query
+// block of a head are partial, and the rows past N that their loads bring in belong to the next
+// head (or read as zeros past the end).  Keys from N on get P = dS = 0 here; queries from N on
+// get P = 0 from L2 = +inf (bwd_pre), so their dQ rows are zero and land in the padding rows of
+// the accumulator; dK and dV rows from N on are not stored.
+template <int D, bool HALVES, bool TAIL>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -186,6 +205,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 float *__restrict__ dQacc, __nv_bfloat16 *__restrict__ dK, __nv_bfloat16 *__restrict__ dV,
                 const int split_from, float *__restrict__ kvacc) {
     using C = BwdCfg<D>;
+    static_assert(!(HALVES && TAIL), "a partial tile is never split");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const BwdBars bars{smem_addr(sm + C::kBarOff)};
@@ -193,7 +213,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nq = p.N / BQ;                   // 64-row query blocks
+    const int nq = TAIL ? (p.N + BQ - 1) / BQ : p.N / BQ;  // 64-row query blocks
+    const int npad = TAIL ? nq * BQ : p.N;     // rows per head of D, L2 and the dQ accumulator
     int kvt, head, q_lo;                       // key tile, head, first query block
     if constexpr (HALVES) {
         const int tile = split_from + (int)(blockIdx.x >> 1);
@@ -217,6 +238,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (hm == nullptr) return true;
         if (mb == 128) return hm[(size_t)(iq >> 1) * mnb + kvt] != 0;
         const uint8_t *r = hm + (size_t)iq * mnb + 2 * kvt;
+        if constexpr (TAIL) return (r[0] | (2 * kvt + 1 < mnb ? r[1] : 0)) != 0;  // last column may be absent
         return (r[0] | r[1]) != 0;
     };
     uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
@@ -299,13 +321,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     !mbar_wait(bars.qempty(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, abort_flag, p.dev_status))
                     break;
                 const int q0 = head * p.N + iq * BQ;
+                const int ql = TAIL ? head * npad + iq * BQ : q0;  // the block's rows of L2 and D
                 mbar_arrive_expect_tx(bars.qfull(s), 2 * C::kQTile + 2 * BQ * 4);
                 for (int c = 0; c < D / 64; ++c) {
                     tma_load_2d(sQ + s * C::kQTile + c * C::kQSlab, &tmQ, c * 64, q0, bars.qfull(s));
                     tma_load_2d(sdO + s * C::kQTile + c * C::kQSlab, &tmdO, c * 64, q0, bars.qfull(s));
                 }
-                bulk_load(sLd + s * 2 * BQ * 4, L2 + q0, BQ * 4, bars.qfull(s));
-                bulk_load(sLd + s * 2 * BQ * 4 + BQ * 4, Dv + q0, BQ * 4, bars.qfull(s));
+                bulk_load(sLd + s * 2 * BQ * 4, L2 + ql, BQ * 4, bars.qfull(s));
+                bulk_load(sLd + s * 2 * BQ * 4 + BQ * 4, Dv + ql, BQ * 4, bars.qfull(s));
             }
         }
     } else if (warp >= kMmaWarp) {
@@ -375,7 +398,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 auto halves = [&](int iq) -> uint32_t {
                     if (!fine) return 3u;
                     const uint8_t *r = hm + (size_t)iq * mnb + 2 * kvt;
-                    return (uint32_t)(r[0] != 0) | ((uint32_t)(r[1] != 0) << 1);
+                    const bool has1 = !TAIL || 2 * kvt + 1 < mnb;
+                    return (uint32_t)(r[0] != 0) | ((uint32_t)(has1 && r[1] != 0) << 1);
                 };
                 int iq_next = (fine && n > 0) ? next_q(q_lo - 1) : 0;
                 uint32_t h_next = halves(iq_next);
@@ -428,6 +452,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         uint8_t *ds_gen = sm + C::kDsOff;
         // 64-row mask blocks: this warp's 32 keys lie in one key half of the tile
         const bool fine = hm != nullptr && mb == 64;
+        // TAIL: keys from N on (rows of the next head) get P = dS = 0
+        const bool key_ok = !TAIL || kvt * BKV + key < p.N;
         int iq = q_lo - 1;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
@@ -435,7 +461,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             bool row_kept = true;
             if (fine) {
                 iq = next_q(iq);
-                row_kept = hm[(size_t)iq * mnb + 2 * kvt + ((warp & 3) >> 1)] != 0;
+                if constexpr (TAIL) {  // the tile's second key half may have no mask column
+                    const int kcol = 2 * kvt + ((warp & 3) >> 1);
+                    row_kept = kcol < mnb && hm[(size_t)iq * mnb + kcol] != 0;
+                } else {
+                    row_kept = hm[(size_t)iq * mnb + 2 * kvt + ((warp & 3) >> 1)] != 0;
+                }
             }
             ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             if (ok && it >= 2)
@@ -474,6 +505,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
                     pk[t] = pack_bf16(p0, p1);
                     dk[t] = pack_bf16(d0, d1);
+                }
+                if constexpr (TAIL) {
+                    if (!key_ok) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) pk[t] = dk[t] = 0u;
+                    }
                 }
             }
             // P^T as bf16 pairs over the first 16 of this half's own 32 S columns
@@ -518,6 +555,27 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                               make_float4(__uint_as_float(a[4 * q]) * mul, __uint_as_float(a[4 * q + 1]) * mul,
                                           __uint_as_float(a[4 * q + 2]) * mul, __uint_as_float(a[4 * q + 3]) * mul));
             }
+        } else if (TAIL && n > 0 && (kvt + 1) * BKV > p.N) {
+            // the last tile of a head with N % 128 != 0: the rows past N belong to the next head,
+            // so each thread stores its own row, if it exists, instead of one tensor store
+            if (ok) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(acc + c0, a);
+                    tmem_wait_ld();
+                    reg_fence(a);
+                    uint32_t pa[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * mul, __uint_as_float(a[2 * t + 1]) * mul);
+                    if (key_ok) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            orow[c0 / 8 + q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                    }
+                }
+            }
         } else if (!HALVES && n > 0) {
             // Stage the bf16 tile (dK in the Q ring, dV in the dO ring: every MMA that reads them
             // completed before kvdone) in the 128-byte-swizzled layout of a 64-column TMA box, then
@@ -555,7 +613,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 bulk_commit();
                 bulk_wait_all();
             }
-        } else if (n == 0) {
+        } else if (n == 0 && key_ok) {
             for (int q = 0; q < D / 8; ++q) orow[q] = make_uint4(0, 0, 0, 0);
         }
     } else if (warp < kTmaWarp) {
@@ -587,7 +645,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // Two halves (queries 0-31 from r0, 32-63 from r1), each with its own 16 KB of the
             // staging tile and its own bulk reduction: before a half is rewritten only the
             // reduction of the same half one block back must have read it, not the one just issued.
-            const size_t q0 = (size_t)head * p.N + (size_t)iq * BQ;
+            const size_t q0 = (size_t)head * npad + (size_t)iq * BQ;  // the block's accumulator rows
             auto stage = [&](const uint32_t(&r)[32], int hq) {
                 if (t == 0) bulk_wait_read_but_one();
                 named_bar_sync(1, 128);
@@ -640,6 +698,27 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__rest
     }
 }
 
+// dQ = bf16(s * accumulator) when the accumulator has npad > N rows per head: dQ row
+// head * N + q comes from accumulator row head * npad + q.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_rows_kernel(const float *__restrict__ acc,
+                                                                   __nv_bfloat16 *__restrict__ dQ, float scale,
+                                                                   size_t n8, int N, int npad) {
+    constexpr int U = D / 8;  // 8-element units per row
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / U, hh = row / (size_t)N;
+        const size_t src = ((hh * (size_t)npad + (row - hh * (size_t)N)) * U + i % U) * 2;
+        const float4 a = reinterpret_cast<const float4 *>(acc)[src];
+        const float4 b = reinterpret_cast<const float4 *>(acc)[src + 1];
+        uint4 o;
+        o.x = pack_bf16(a.x * scale, a.y * scale);
+        o.y = pack_bf16(a.z * scale, a.w * scale);
+        o.z = pack_bf16(b.x * scale, b.y * scale);
+        o.w = pack_bf16(b.z * scale, b.w * scale);
+        reinterpret_cast<uint4 *>(dQ)[i] = o;
+    }
+}
+
 // ------------------------------------------------------------------------- 4
 // Split tiles: dK and dV rows are bf16 of the fp32 sum of the two query halves (dK is
 // already scaled).  One CTA per (split tile, dK or dV).
@@ -663,19 +742,43 @@ template <int D>
 cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const void *dO, const float *LSE,
                      void *dQ, void *dK, void *dV, float *Dv, float *dQacc, float *kvacc, int split,
                      cudaStream_t st) {
-    const size_t rows = (size_t)p.B * p.H * p.N;
+    const bool tail = p.N % BKV != 0;
+    const int npad = bwd_rows_per_head(p.N);
+    const size_t rows = (size_t)p.B * p.H * p.N, prows = (size_t)p.B * p.H * npad;
     const int tiles = (p.N / BKV) * p.B * p.H;
-    if (kvacc == nullptr) split = 0;
+    if (kvacc == nullptr || tail) split = 0;
     {
         ProfScope prof_("bwd_pre", st);
-        bwd_pre_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-            static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dv, dQacc, rows,
-            reinterpret_cast<float4 *>(kvacc), bwd_split_bytes(split, D) / sizeof(float4), LSE, Dv + rows);
+        auto pre = npad != p.N ? bwd_pre_kernel<D, true> : bwd_pre_kernel<D, false>;
+        pre<<<(unsigned)((prows + 7) / 8), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dv, dQacc, prows,
+            reinterpret_cast<float4 *>(kvacc), bwd_split_bytes(split, D) / sizeof(float4), LSE, Dv + prows, p.N,
+            npad);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto kern = bwd_main_kernel<D, false>;
-    auto kh = bwd_main_kernel<D, true>;
+    if (tail) {
+        auto kt = bwd_main_kernel<D, false, true>;
+        e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        {
+            ProfScope prof_("bwd_main", st);
+            kt<<<dim3((p.N + BKV - 1) / BKV, p.B * p.H), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
+                m.q, m.k, m.v, m.dO, m.dk, m.dv, p, Dv + prows, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
+                static_cast<__nv_bfloat16 *>(dV), INT_MAX, nullptr);
+        }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const size_t n8 = rows * D / 8;
+        {
+            ProfScope prof_("bwd_dq_convert", st);
+            bwd_dq_convert_rows_kernel<D><<<(unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16), 256, 0, st>>>(
+                dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8, p.N, npad);
+        }
+        return cudaGetLastError();
+    }
+    auto kern = bwd_main_kernel<D, false, false>;
+    auto kh = bwd_main_kernel<D, true, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
     if (e == cudaSuccess && split > 0)
         e = cudaFuncSetAttribute(kh, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
@@ -728,7 +831,10 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
 
 }  // namespace
 
+int bwd_rows_per_head(int N) { return (N + BQ - 1) / BQ * BQ; }
+
 int bwd_split_tiles(int B, int H, int N) {
+    if (N % BKV != 0) return 0;  // partial tiles are never split
     const long long tiles = (long long)B * H * (N / BKV);
     const int sms = device_sm_count();
     const long long r = tiles % sms;

@@ -105,10 +105,17 @@ struct Bars {
 // Key block j (128 keys) is visited by query tile t when any mask entry that
 // covers the 128 x 128 square (t, j) is kept: one entry for 128-blocks, four
 // for 64-blocks.  hm is this head's [mnb][mnb] mask (nullptr: no mask).
+// TAIL (N % 128 != 0): the last tile or key block may cover a single 64-row mask row or column,
+// the last one of the mask; the entries past it do not exist and are not read.
+template <bool TAIL = false>
 __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int t, int j) {
     if (hm == nullptr) return true;
     if (mb == 128) return hm[(size_t)t * mnb + j] != 0;
     const uint8_t *r0 = hm + (size_t)(2 * t) * mnb + 2 * j, *r1 = r0 + mnb;
+    if constexpr (TAIL) {
+        const bool j1 = 2 * j + 1 < mnb, t1 = 2 * t + 1 < mnb;
+        return (r0[0] | (j1 ? r0[1] : 0) | (t1 ? r1[0] : 0) | (t1 && j1 ? r1[1] : 0)) != 0;
+    }
     return (r0[0] | r0[1] | r1[0] | r1[1]) != 0;
 }
 
@@ -117,7 +124,7 @@ __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int 
 constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
 constexpr uint32_t kIdSNeg = kIdS | kIdescNegateA;
 
-template <int D>
+template <int D, bool TAIL>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
@@ -132,7 +139,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, head = blockIdx.y;
-    const int nb = p.N / BN;
+    const int nb = TAIL ? (p.N + BN - 1) / BN : p.N / BN;  // key blocks (the last one partial under TAIL)
     const uint8_t *hm = p.head_mask(head);
     const int mb = p.mask_block, mnb = p.mask_nb();
     uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
@@ -161,7 +168,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
     }
-    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
+    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited<TAIL>(hm, mb, mnb, tile, j); });
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -176,7 +183,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         n = vb.count();
     } else if (hm != nullptr) {  // rows longer than the bit set: read the mask directly
         n = 0;
-        for (int j = 0; j < nb; ++j) n += visited(hm, mb, mnb, tile, j) ? 1 : 0;
+        for (int j = 0; j < nb; ++j) n += visited<TAIL>(hm, mb, mnb, tile, j) ? 1 : 0;
     }
     // the visited key block after j (callers ask only while one remains)
     auto next_block = [&](int j) -> int {
@@ -184,7 +191,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (use_bits) return vb.next(j);
         do {
             ++j;
-        } while (!visited(hm, mb, mnb, tile, j));
+        } while (!visited<TAIL>(hm, mb, mnb, tile, j));
         return j;
     };
 
@@ -266,15 +273,31 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each
         // 64-key half of a visited block is kept or removed for the whole warp.
         const bool fine = hm != nullptr && mb == 64;
-        const uint8_t *wmask = fine ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
-        int j = -1;  // key block of iteration it (tracked only for fine masks)
+        // TAIL: rows 64-127 of the last tile may all lie past N, below the mask's last row
+        const bool wrow = !TAIL || 2 * tile + warp / 2 < mnb;
+        const uint8_t *wmask = fine && wrow ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
+        int j = -1;  // key block of iteration it (tracked for fine masks and under TAIL)
         for (int it = 0; it < n; ++it) {
             const int b = it & 1;
             bool half_kept[2] = {true, true};
             if (fine) {
                 j = next_block(j);
-                half_kept[0] = wmask[2 * j] != 0;
-                half_kept[1] = wmask[2 * j + 1] != 0;
+                if (wmask != nullptr) {
+                    half_kept[0] = wmask[2 * j] != 0;
+                    half_kept[1] = (!TAIL || 2 * j + 1 < mnb) && wmask[2 * j + 1] != 0;
+                } else {  // rows past N only (TAIL)
+                    half_kept[0] = half_kept[1] = false;
+                }
+            } else if (TAIL) {
+                j = next_block(j);
+            }
+            // TAIL: keys of the last block from N on do not exist (their rows in the K and V tiles
+            // belong to the next head, or read as zeros past the end): their scores are -inf, and a
+            // half with no key below N counts as removed
+            int lim = BN;
+            if constexpr (TAIL) {
+                if (j == nb - 1) lim = p.N - j * BN;
+                if (lim <= BN / 2) half_kept[1] = false;
             }
             ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
@@ -291,6 +314,15 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             reg_fence(r[1]);
             reg_fence(r[2]);
             reg_fence(r[3]);
+            if constexpr (TAIL) {
+                if (lim < BN) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (32 * q + t >= lim) r[q][t] = 0xff800000u;  // -inf
+                }
+            }
             // row max: four independent chains (one per 32-column chunk), then combined
             float mxq[4];
 #pragma unroll
@@ -372,7 +404,32 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after();
         }
         const size_t grow = (size_t)row0 + tid;
-        if (n > 0) {
+        // rows of this tile below N (TAIL: the last tile of a head is partial)
+        const int valid = TAIL ? min(BM, p.N - tile * BM) : BM;
+        if (TAIL && n > 0 && valid < BM) {
+            // the rows past N belong to the next head: each thread stores its own row, if it
+            // exists, instead of one tensor store of the whole tile
+            if (ok) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kOCol + c0, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                    if (tid < valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(O + grow * D + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                if (tid < valid) LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (n > 0) {
             // O leaves through the Q tile (the last MMA that read it completed before odone):
             // rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
             // stores the tile.  The four warps meet at the named barrier whatever `ok` says.
@@ -410,7 +467,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 bulk_commit();
                 bulk_wait_all();
             }
-        } else {
+        } else if (tid < valid) {
             // every key block removed: O = 0, LSE = -inf
             uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
             for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
@@ -1200,7 +1257,7 @@ struct RingBars {
     __device__ uint32_t drain() const { return base + 8u * (6 + 2 * P); }
 };
 
-template <int D>
+template <int D, bool TAIL>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
@@ -1215,7 +1272,7 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tile = blockIdx.x, head = blockIdx.y;
-    const int nb = p.N / BN;
+    const int nb = TAIL ? (p.N + BN - 1) / BN : p.N / BN;  // key blocks (the last one partial under TAIL)
     const uint8_t *hm = p.head_mask(head);
     const int mb = p.mask_block, mnb = p.mask_nb();
     uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
@@ -1242,7 +1299,7 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
     }
-    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited(hm, mb, mnb, tile, j); });
+    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited<TAIL>(hm, mb, mnb, tile, j); });
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -1257,7 +1314,7 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         n = vb.count();
     } else if (hm != nullptr) {  // rows longer than the bit set: read the mask directly
         n = 0;
-        for (int j = 0; j < nb; ++j) n += visited(hm, mb, mnb, tile, j) ? 1 : 0;
+        for (int j = 0; j < nb; ++j) n += visited<TAIL>(hm, mb, mnb, tile, j) ? 1 : 0;
     }
     // the visited key block after j (callers ask only while one remains)
     auto next_block = [&](int j) -> int {
@@ -1265,7 +1322,7 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (use_bits) return vb.next(j);
         do {
             ++j;
-        } while (!visited(hm, mb, mnb, tile, j));
+        } while (!visited<TAIL>(hm, mb, mnb, tile, j));
         return j;
     };
 
@@ -1375,15 +1432,31 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each
         // 64-key half of a visited block is kept or removed for the whole warp.
         const bool fine = hm != nullptr && mb == 64;
-        const uint8_t *wmask = fine ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
-        int j = -1;  // key block of iteration it (tracked only for fine masks)
+        // TAIL: rows 64-127 of the last tile may all lie past N, below the mask's last row
+        const bool wrow = !TAIL || 2 * tile + warp / 2 < mnb;
+        const uint8_t *wmask = fine && wrow ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
+        int j = -1;  // key block of iteration it (tracked for fine masks and under TAIL)
         for (int it = 0; it < n; ++it) {
             const int b = it & 1;
             bool half_kept[2] = {true, true};
             if (fine) {
                 j = next_block(j);
-                half_kept[0] = wmask[2 * j] != 0;
-                half_kept[1] = wmask[2 * j + 1] != 0;
+                if (wmask != nullptr) {
+                    half_kept[0] = wmask[2 * j] != 0;
+                    half_kept[1] = (!TAIL || 2 * j + 1 < mnb) && wmask[2 * j + 1] != 0;
+                } else {  // rows past N only (TAIL)
+                    half_kept[0] = half_kept[1] = false;
+                }
+            } else if (TAIL) {
+                j = next_block(j);
+            }
+            // TAIL: keys of the last block from N on do not exist (their rows in the K and V tiles
+            // belong to the next head, or read as zeros past the end): their scores are -inf, and a
+            // half with no key below N counts as removed
+            int lim = BN;
+            if constexpr (TAIL) {
+                if (j == nb - 1) lim = p.N - j * BN;
+                if (lim <= BN / 2) half_kept[1] = false;
             }
             ok = mbar_wait(bars.sfull(b), (uint32_t)(it >> 1) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
@@ -1400,6 +1473,15 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             reg_fence(r[1]);
             reg_fence(r[2]);
             reg_fence(r[3]);
+            if constexpr (TAIL) {
+                if (lim < BN) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            if (32 * q + t >= lim) r[q][t] = 0xff800000u;  // -inf
+                }
+            }
             // row max: four independent chains (one per 32-column chunk), then combined
             float mxq[4];
 #pragma unroll
@@ -1481,7 +1563,32 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             tc_fence_after();
         }
         const size_t grow = (size_t)row0 + tid;
-        if (n > 0) {
+        // rows of this tile below N (TAIL: the last tile of a head is partial)
+        const int valid = TAIL ? min(BM, p.N - tile * BM) : BM;
+        if (TAIL && n > 0 && valid < BM) {
+            // the rows past N belong to the next head: each thread stores its own row, if it
+            // exists, instead of one tensor store of the whole tile
+            if (ok) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + kOCol + c0, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        pk[t] = pack_bf16(__uint_as_float(o[2 * t]) * inv, __uint_as_float(o[2 * t + 1]) * inv);
+                    if (tid < valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(O + grow * D + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                if (tid < valid) LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (n > 0) {
             // O leaves through the Q tile (the last MMA that read it completed before odone):
             // rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
             // stores the tile.  The four warps meet at the named barrier whatever `ok` says.
@@ -1519,7 +1626,7 @@ fwd_bf16_ring_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                 bulk_commit();
                 bulk_wait_all();
             }
-        } else {
+        } else if (tid < valid) {
             // every key block removed: O = 0, LSE = -inf
             uint4 *orow = reinterpret_cast<uint4 *>(O + grow * D);
             for (int v = 0; v < D / 8; ++v) orow[v] = make_uint4(0, 0, 0, 0);
@@ -1552,12 +1659,12 @@ cudaError_t launch_pp(const Problem &p, const FwdMaps &m, void *O, float *LSE, c
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool TAIL>
 cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
-    auto kern = fwd_bf16_kernel<D>;
+    auto kern = fwd_bf16_kernel<D, TAIL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.N / BM, p.B * p.H);
+    dim3 grid((p.N + BM - 1) / BM, p.B * p.H);
     {
         ProfScope prof_("fwd_bf16", st);
         kern<<<grid, kThreads, FwdCfg<D>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, static_cast<__nv_bfloat16 *>(O),
@@ -1580,11 +1687,12 @@ cudaError_t launch_pp2h(const Problem &p, const FwdMaps &m, void *O, float *LSE,
     return cudaGetLastError();
 }
 
+template <bool TAIL>
 cudaError_t launch_ring(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
-    auto kern = fwd_bf16_ring_kernel<256>;
+    auto kern = fwd_bf16_ring_kernel<256, TAIL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RingCfg<256>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.N / BM, p.B * p.H);
+    dim3 grid((p.N + BM - 1) / BM, p.B * p.H);
     {
         ProfScope prof_("fwd_bf16", st);
         kern<<<grid, kThreads, RingCfg<256>::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p,
@@ -1597,20 +1705,25 @@ cudaError_t launch_ring(const Problem &p, const FwdMaps &m, void *O, float *LSE,
 
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;
+    // N % 128 != 0: one query tile per CTA, the last tile and key block partial
+    const bool tail = p.N % BM != 0;
     // two query tiles per CTA when both tiles visit every key block
     const bool pp = p.mask == nullptr && p.N % (2 * BM) == 0;
     // or when both are the same query tile of two heads under one 128-block mask for every head
-    const bool pp2h = p.mask != nullptr && p.mask_stride == 0 && p.mask_block == 128 && (p.B * p.H) % 2 == 0;
+    const bool pp2h =
+        !tail && p.mask != nullptr && p.mask_stride == 0 && p.mask_block == 128 && (p.B * p.H) % 2 == 0;
     switch (p.d) {
         case 64:
             return pp     ? launch_pp<64>(p, maps, O, LSE, st)
                    : pp2h ? launch_pp2h<64>(p, maps, O, LSE, st)
-                          : launch_d<64>(p, maps, O, LSE, st);
+                   : tail ? launch_d<64, true>(p, maps, O, LSE, st)
+                          : launch_d<64, false>(p, maps, O, LSE, st);
         case 128:
             return pp     ? launch_pp<128>(p, maps, O, LSE, st)
                    : pp2h ? launch_pp2h<128>(p, maps, O, LSE, st)
-                          : launch_d<128>(p, maps, O, LSE, st);
-        case 256: return launch_ring(p, maps, O, LSE, st);
+                   : tail ? launch_d<128, true>(p, maps, O, LSE, st)
+                          : launch_d<128, false>(p, maps, O, LSE, st);
+        case 256: return tail ? launch_ring<true>(p, maps, O, LSE, st) : launch_ring<false>(p, maps, O, LSE, st);
         default: return cudaErrorNotSupported;
     }
 }

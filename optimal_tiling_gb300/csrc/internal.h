@@ -72,10 +72,13 @@ struct BwdMaps {
 // that wave are split into two query halves each (dense problems), so that the wave takes
 // half a tile's time; the halves add fp32 partial dK and dV into scratch (kvacc, zeroed by
 // the launch) and a small kernel converts them.
-// Scratch every backward needs: D (B*H*N fp32) and, for bf16, the fp32 dQ accumulator,
-// each rounded up to 256 bytes; the last-wave split's scratch follows it.
+// Scratch every backward needs: D (B*H*N fp32) and, for bf16, LSE log2(e) and the fp32 dQ
+// accumulator, each rounded up to 256 bytes; the last-wave split's scratch follows it.  The
+// bf16 row terms and accumulator hold bwd_rows_per_head(N) rows per head: N rounded up to the
+// 64-row query block (the rows past N are padding that the kernels write and read).
 size_t bwd_base_bytes(int B, int H, int N, int d, bool bf16);
-int bwd_split_tiles(int B, int H, int N);        // tiles to split, 0 for none
+int bwd_rows_per_head(int N);
+int bwd_split_tiles(int B, int H, int N);        // tiles to split, 0 for none (and when 128 does not divide N)
 size_t bwd_split_bytes(int split_tiles, int d);  // fp32 dK and dV of the split tiles
 cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O,
                             const void *dO, const float *LSE, void *dQ, void *dK, void *dV,

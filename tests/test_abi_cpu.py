@@ -60,7 +60,6 @@ def test_forward_argument_checks(lib):
     assert _fwd(lib, q=MIS) == attn.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, dt=7) == attn.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
-    assert _fwd(lib, N=200) == attn.ATTN_ERR_UNSUPPORTED          # bf16 needs N % 128 == 0
     assert _fwd(lib, d=96) == attn.ATTN_ERR_UNSUPPORTED           # bf16 d in {64,128,256}
     assert _fwd(lib, d=300, dt=attn.ATTN_DTYPE_F32) == attn.ATTN_ERR_UNSUPPORTED
     # more (b, h) pairs than a grid dimension holds: refused before any CUDA call
@@ -73,7 +72,10 @@ def test_backward_argument_checks(lib):
         return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, N, d, 0.1, dt,
                             None, ws, wsz, None)
     assert bwd(d=256) == attn.ATTN_ERR_UNSUPPORTED
-    assert bwd(N=100) == attn.ATTN_ERR_UNSUPPORTED
+    # bf16: the row terms and dQ accumulator have N rounded up to 64 rows per head, which
+    # must stay within 2^31 rows too (3 x 715827882 rows fit, 3 x 715827904 do not)
+    assert lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 715827882, 64, 0.1,
+                        attn.ATTN_DTYPE_BF16, None, FAKE, 1 << 62, None) == attn.ATTN_ERR_UNSUPPORTED
     assert bwd(ws=None) == attn.ATTN_ERR_WORKSPACE
     need = lib.attn_bwd_workspace_size(1, 2, 256, 128, attn.ATTN_DTYPE_BF16)
     assert need >= 2 * 256 * 4 + 2 * 256 * 128 * 4
@@ -108,6 +110,24 @@ def test_materialized_argument_checks(lib):
     r = lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 256, 64, 0.1, attn.ATTN_DTYPE_F32,
                                   None, FAKE, need, None)
     assert r == attn.ATTN_ERR_UNSUPPORTED
+    # the materialising schedules take whole 128-row tiles only
+    r = lib.attn_fwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 200, 64, 0.1, attn.ATTN_DTYPE_BF16,
+                                  None, FAKE, 1 << 40, None)
+    assert r == attn.ATTN_ERR_UNSUPPORTED
+    r = lib.attn_bwd_materialized(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 200, 64, 0.1,
+                                  attn.ATTN_DTYPE_BF16, None, FAKE, 1 << 40, None)
+    assert r == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_workspace_with_partial_tiles(lib):
+    """When 128 does not divide N: D and LSE log2(e), then the fp32 dQ accumulator, with N
+    rounded up to 64 rows per head, and no last-wave split (N = 128 (t + 1/2) for t tiles
+    around the SM count would be split if whole)."""
+    up = lambda x: -(-x // 256) * 256
+    for B, H, N, d in ((1, 3, 200, 128), (2, 5, 1, 64), (1, 1, 4097, 128), (1, 1, 128 * 153 + 64, 128)):
+        rows = B * H * (-(-N // 64) * 64)
+        assert lib.attn_bwd_workspace_size(B, H, N, d, attn.ATTN_DTYPE_BF16) == up(2 * rows * 4) + up(rows * d * 4)
+        assert lib.attn_bwd_workspace_size(B, H, N, d, attn.ATTN_DTYPE_F32) == up(B * H * N * 4)
 
 
 def test_selftest_rejects_bad_limits(lib):
@@ -148,7 +168,7 @@ def test_masked_entry_point_checks(lib):
     assert bwd(stride=-64) == attn.ATTN_ERR_INVALID_ARG
     assert bwd(d=96) == attn.ATTN_ERR_UNSUPPORTED
     bm = attn.BlockMask(FAKE, 64, 0)
-    assert lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 200, 64, 1.0, attn.ATTN_DTYPE_BF16,
+    assert lib.attn_fwd_masked(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 200, 96, 1.0, attn.ATTN_DTYPE_BF16,
                                ctypes.byref(bm), None) == attn.ATTN_ERR_UNSUPPORTED
 
 
@@ -175,7 +195,7 @@ def test_static_workspace_checks_arguments_before_its_size(lib):
     assert call(dt=7) == attn.ATTN_ERR_INVALID_ARG
     assert call(scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
     assert call(d=96) == attn.ATTN_ERR_UNSUPPORTED
-    assert call(N=4000) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(N=4000) == attn.ATTN_ERR_WORKSPACE   # valid (a partial last tile), too large
     assert call() == attn.ATTN_ERR_WORKSPACE
 
 
