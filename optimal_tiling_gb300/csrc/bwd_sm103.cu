@@ -138,9 +138,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Product of two packed fp32 pairs (one instruction, round to nearest).
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ------------------------------------------------------------------------- 1
 // D_i = sum_t dO_it O_it and L2_i = LSE_i log2(e) (the row's log-sum-exp in the base-2 units of
-// the exponentials below); the dQ accumulator row is zeroed.  One warp per row.
+// the exponentials below), both stored negated (-D, -L2: the main kernel adds them in packed
+// pairs); the dQ accumulator row is zeroed.  One warp per row.
 // The split tiles' partial dK, dV (kv4: kv_n4 float4) are zeroed grid-stride.
 // D, L2 and the accumulator hold npad rows per head (N rounded up to the 64-row query block;
 // npad = N when 64 divides N, PAD = false): the rows from N on get D = 0 and L2 = +inf, so that
@@ -179,8 +187,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     }
     if (lane == 0) {
-        Dv[prow] = acc;
-        L2[prow] = pad ? INFINITY : LSE[row] * kLog2e;
+        Dv[prow] = -acc;
+        L2[prow] = pad ? -INFINITY : -(LSE[row] * kLog2e);
     }
     float4 *z = reinterpret_cast<float4 *>(dQacc + prow * D);
     for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -474,8 +482,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const float *l2 = ld_f + s * 2 * BQ;  // LSE log2(e) of the 64 queries, then D
-            const float *dvv = l2 + BQ;
+            const float *nl2 = ld_f + s * 2 * BQ;  // -LSE log2(e) of the 64 queries, then -D
+            const float *ndv = nl2 + BQ;
             uint32_t pk[16], dk[16];
             uint32_t sr[32], pr[32];
             if (row_kept) {
@@ -496,13 +504,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                 for (int t = 0; t < 16; ++t) pk[t] = dk[t] = 0u;
             } else {
+                // two queries per step on the packed fp32 path: x = s log2(e) S - L2, p = 2^x,
+                // dS = p (dP - D); the same roundings as one query at a time
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int q = h * 32 + 2 * t;
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * t]), sl2, -l2[q]));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * t + 1]), sl2, -l2[q + 1]));
-                    const float d0 = p0 * (__uint_as_float(pr[2 * t]) - dvv[q]);
-                    const float d1 = p1 * (__uint_as_float(pr[2 * t + 1]) - dvv[q + 1]);
+                    // the row terms of four queries per 16-byte load, two of them per step
+                    float4 nl, nd;
+                    if ((t & 1) == 0) {
+                        nl = *reinterpret_cast<const float4 *>(nl2 + q);
+                        nd = *reinterpret_cast<const float4 *>(ndv + q);
+                    }
+                    const uint64_t l2p = (t & 1) ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y);
+                    const uint64_t dvp = (t & 1) ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y);
+                    const uint64_t x2 =
+                        f2_fma(f2_pack(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1])), sl2x2, l2p);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    const uint64_t g2 =
+                        f2_add(f2_pack(__uint_as_float(pr[2 * t]), __uint_as_float(pr[2 * t + 1])), dvp);
+                    float d0, d1;
+                    f2_unpack(f2_mul(f2_pack(p0, p1), g2), d0, d1);
                     pk[t] = pack_bf16(p0, p1);
                     dk[t] = pack_bf16(d0, d1);
                 }
