@@ -268,13 +268,21 @@ __global__ void __launch_bounds__(320, D == 64 ? 2 : 1) mat_scores_kernel(const 
                     tmem_wait_ld();
                     reg_fence(r);
                     uint32_t pk[16];
+                    // two scores per step on the packed fp32 path; the row sum adds the values
+                    // actually stored (bf16 widened by a shift), in an even and an odd chain
+                    const uint64_t sl2x2 = f2_pack(sl2, sl2), nc2 = f2_pack(-c2, -c2);
+                    uint64_t rs2 = f2_pack(0.f, 0.f);
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
-                        pk[t] = pack_bf16(ex2(fmaf(__uint_as_float(r[2 * t]), sl2, -c2)),
-                                          ex2(fmaf(__uint_as_float(r[2 * t + 1]), sl2, -c2)));
-                        const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[t]));
-                        rs += back.x + back.y;  // the row sum of the values actually stored
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])), sl2x2, nc2),
+                                  x0, x1);
+                        pk[t] = pack_bf16(ex2(x0), ex2(x1));
+                        rs2 = f2_add(rs2, f2_pack(__uint_as_float(pk[t] << 16), __uint_as_float(pk[t] & 0xffff0000u)));
                     }
+                    float rs0, rs1;
+                    f2_unpack(rs2, rs0, rs1);
+                    rs += rs0 + rs1;
                     const int slab = c0 / 64;
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
