@@ -557,7 +557,7 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             mbar_init(bars.kfull(s), 1);
             mbar_init(bars.kempty(s), 1);
             mbar_init(bars.vfull(s), 1);
-            mbar_init(bars.vempty(s), 1);
+            mbar_init(bars.vempty(s), 1);  // unused: a V stage is free when the next K stage is
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bars.sfull(x), 1);
@@ -594,7 +594,12 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 mbar_arrive_expect_tx(bars.kfull(s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sK + s * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(s));
-                if (j >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                // V(j - S) was read by PV_A, PV_B(j - S), which complete before S_B(j - S + 1), whose
+                // commit releases K(j - S + 1) (kempty completes once per use of a K stage): that
+                // release frees V's stage too, one commit per block fewer on the issuing thread
+                if (j >= S && !mbar_wait(bars.kempty((j - S + 1) % S), (uint32_t)((j - S + 1) / S) & 1u, abort_flag,
+                                         p.dev_status))
+                    break;
                 mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
@@ -648,7 +653,6 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 if (!(ok = mbar_wait(bars.pfull(1), ph, abort_flag, p.dev_status))) break;
                 tc_fence_after();
                 mma_pv(1, j);
-                mma_commit(bars.vempty(s));
                 if (more) {
                     mma_s(1, j + 1);
                     mma_commit(bars.kempty((j + 1) % S));
