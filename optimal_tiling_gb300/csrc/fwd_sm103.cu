@@ -161,7 +161,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bars.sfull(b), 1);
             mbar_init(bars.pfull(b), 4 * 32);
         }
-        mbar_init(bars.odone(), 1);
+        mbar_init(bars.odone(), 1);  // unused: vempty of the last V stage marks PV done
         mbar_init(bars.drain(), 1);
         fence_barrier_init();
         // the Q tile is needed whatever the mask says: start its load before the mask is read
@@ -255,8 +255,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int ks = 0; ks < BN / 16; ++ks)
                     mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO,
                            (it > 0 || ks > 0) ? 1u : 0u);
+                // vempty(s) also tells the softmax that PV_it is complete (O may be rescaled, or read
+                // after the last block): one commit per block fewer than a barrier of its own
                 mma_commit(bars.vempty(s));
-                mma_commit(bars.odone());
             }
             if (!ok) {
                 // let every MMA already issued finish before tensor memory is released
@@ -376,7 +377,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             l = l * alpha + rs;
             tmem_wait_st();
             if (it > 0) {
-                ok = mbar_wait(bars.odone(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status);
+                // PV_{it-1} complete: the release of V stage (it-1) % S, use (it-1) / S
+                ok = mbar_wait(bars.vempty((it - 1) % S), (uint32_t)((it - 1) / S) & 1u, abort_flag, p.dev_status);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -399,7 +401,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n > 0) {
-            ok = mbar_wait(bars.odone(), (uint32_t)(n - 1) & 1u, abort_flag, p.dev_status);
+            ok = mbar_wait(bars.vempty((n - 1) % S), (uint32_t)((n - 1) / S) & 1u, abort_flag, p.dev_status);
             ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
         }
@@ -430,7 +432,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (tid < valid) LSE[grow] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
             }
         } else if (n > 0) {
-            // O leaves through the Q tile (the last MMA that read it completed before odone):
+            // O leaves through the Q tile (the last MMA that read it completed before PV_{n-1}):
             // rows in the 128-byte-swizzled layout of the 64-column TMA box, then one thread
             // stores the tile.  The four warps meet at the named barrier whatever `ok` says.
             uint8_t *stage = sm + C::kQOff;
