@@ -838,21 +838,28 @@ fwd_bf16_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 // head 2g and tile B the same query tile of head 2g + 1, so both visit the same key blocks and
 // alternate on the tensor core exactly as in the two-tile kernel above (MMA order per visited
 // block i: PV_A(i), S_A(i+1), PV_B(i), S_B(i+1); one issuing thread).  Their K and V differ, so
-// the K and V tiles of both heads stream through one ring of tile-sized pieces, loaded and
-// consumed in that order: K_A(0), K_B(0), then V_A(i), K_A(i+1), V_B(i), K_B(i+1) for every
-// visited block.  Used for 128 x 128 block masks shared by all heads (B * H even, d = 64, 128),
-// where pairing two tiles of one head would give them different visit lists.
+// the K and V tiles of both heads stream in, loaded and consumed in that order: K_A(0), K_B(0),
+// then V_A(i), K_A(i+1), V_B(i), K_B(i+1) for every visited block, K tiles through a ring of
+// their own and V tiles through another.  K piece 2j + x is K of head 2g + x at the j-th visited
+// block, V piece 2i + x likewise.  Only the S products commit a release: V piece v is free once
+// K piece v + 2 is (PV_x(i) precedes S_x(i+1) in the issuing thread's order), so the issuing
+// thread commits four times per visited block instead of six.  Used for 128 x 128 block masks
+// shared by all heads (B * H even, d = 64, 128), where pairing two tiles of one head would give
+// them different visit lists.
 template <int D>
 struct PP2Cfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = BM * D * 2;                  // a Q, K or V tile
     static constexpr int kChunkBytes = BM * 128;
-    static constexpr int kPieces = D == 64 ? 10 : 5;               // ring of K / V tiles of either head
+    static constexpr int kKSlots = D == 64 ? 6 : 3;               // K ring (tiles of either head)
+    static constexpr int kVSlots = D == 64 ? 4 : 2;               // V ring
+    static_assert(kKSlots >= kVSlots && kVSlots >= 2, "V releases ride on K releases");
     static constexpr int kQOff = 0;                                // Q_A, Q_B
-    static constexpr int kRingOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kRingOff + kPieces * kTileBytes;
-    // q, full[P], empty[P], sfull[2], pfull[2], odone[2], drain
-    static constexpr int kNumBars = 1 + 2 * kPieces + 2 + 2 + 2 + 1;
+    static constexpr int kKOff = 2 * kTileBytes;
+    static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVSlots * kTileBytes;
+    // q, kfull[KS], kempty[KS], vfull[VS], sfull[2], pfull[2], odone[2], drain
+    static constexpr int kNumBars = 1 + 2 * kKSlots + kVSlots + 2 + 2 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // visited key blocks as a bit set: masks with up to 32 * kMaxMaskWords blocks per row
     static constexpr int kMaxMaskWords = 256;
@@ -864,16 +871,17 @@ struct PP2Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
+template <int KS, int VS>
 struct PP2Bars {
     uint32_t base;
-    int pieces;
     __device__ uint32_t q() const { return base; }
-    __device__ uint32_t full(int s) const { return base + 8u * (1 + s); }
-    __device__ uint32_t empty(int s) const { return base + 8u * (1 + pieces + s); }
-    __device__ uint32_t sfull(int x) const { return base + 8u * (1 + 2 * pieces + x); }
-    __device__ uint32_t pfull(int x) const { return base + 8u * (3 + 2 * pieces + x); }
-    __device__ uint32_t odone(int x) const { return base + 8u * (5 + 2 * pieces + x); }
-    __device__ uint32_t drain() const { return base + 8u * (7 + 2 * pieces); }
+    __device__ uint32_t kfull(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t kempty(int s) const { return base + 8u * (1 + KS + s); }
+    __device__ uint32_t vfull(int s) const { return base + 8u * (1 + 2 * KS + s); }
+    __device__ uint32_t sfull(int x) const { return base + 8u * (1 + 2 * KS + VS + x); }
+    __device__ uint32_t pfull(int x) const { return base + 8u * (3 + 2 * KS + VS + x); }
+    __device__ uint32_t odone(int x) const { return base + 8u * (5 + 2 * KS + VS + x); }
+    __device__ uint32_t drain() const { return base + 8u * (7 + 2 * KS + VS); }
 };
 
 template <int D>
@@ -882,10 +890,10 @@ fwd_bf16_pp2h_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                      const Problem p, __nv_bfloat16 *__restrict__ O, float *__restrict__ LSE) {
     using C = PP2Cfg<D>;
-    constexpr int P = C::kPieces;
+    constexpr int KS = C::kKSlots, VS = C::kVSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const PP2Bars bars{smem_addr(sm + C::kBarOff), P};
+    const PP2Bars<KS, VS> bars{smem_addr(sm + C::kBarOff)};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
 
@@ -898,15 +906,16 @@ fwd_bf16_pp2h_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     const int nwords = (nb + 31) >> 5;
     const bool use_bits = nwords <= C::kMaxMaskWords;
     auto kept = [&](int j) { return visited(hm, 128, mnb, tile, j); };
-    const uint32_t sQ = smem_addr(sm + C::kQOff), sR = smem_addr(sm + C::kRingOff);
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
 
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(bars.q(), 1);
-        for (int s = 0; s < P; ++s) {
-            mbar_init(bars.full(s), 1);
-            mbar_init(bars.empty(s), 1);
+        for (int s = 0; s < KS; ++s) {
+            mbar_init(bars.kfull(s), 1);
+            mbar_init(bars.kempty(s), 1);
         }
+        for (int s = 0; s < VS; ++s) mbar_init(bars.vfull(s), 1);
         for (int x = 0; x < 2; ++x) {
             mbar_init(bars.sfull(x), 1);
             mbar_init(bars.pfull(x), 128);
@@ -951,19 +960,34 @@ fwd_bf16_pp2h_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
         if (lane == 0 && n > 0) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            int q = 0;
-            // piece q (the K or V tile of head 2 pair + x at key block blk) into slot q % P, once
-            // the MMAs of piece q - P have released it
+            int kq = 0, vq = 0;  // next K piece, next V piece
+            // K piece kq (K of head 2 pair + x at key block blk) into K slot kq % KS once the S
+            // product of K piece kq - KS has completed; V piece vq into V slot vq % VS once V piece
+            // vq - VS has been read, which the release of K piece vq - VS + 2 implies (kempty
+            // completes once per use of a K slot)
             auto load = [&](int x, bool is_v, int blk) -> bool {
-                const int slot = q % P;
-                if (q >= P && !mbar_wait(bars.empty(slot), ((uint32_t)(q / P) & 1u) ^ 1u, abort_flag, p.dev_status))
-                    return false;
-                mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
                 const int krow = (2 * pair + x) * p.N + blk * BN;
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(sR + slot * C::kTileBytes + c * C::kChunkBytes, is_v ? &tmV : &tmK, c * 64, krow,
-                                bars.full(slot));
-                ++q;
+                if (!is_v) {
+                    const int slot = kq % KS;
+                    if (kq >= KS &&
+                        !mbar_wait(bars.kempty(slot), ((uint32_t)(kq / KS) & 1u) ^ 1u, abort_flag, p.dev_status))
+                        return false;
+                    mbar_arrive_expect_tx(bars.kfull(slot), C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_2d(sK + slot * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(slot));
+                    ++kq;
+                } else {
+                    const int slot = vq % VS;
+                    if (vq >= VS) {
+                        const int r = vq - VS + 2;
+                        if (!mbar_wait(bars.kempty(r % KS), (uint32_t)(r / KS) & 1u, abort_flag, p.dev_status))
+                            return false;
+                    }
+                    mbar_arrive_expect_tx(bars.vfull(slot), C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_2d(sV + slot * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(slot));
+                    ++vq;
+                }
                 return true;
             };
             int jk = next_block(-1), jv = jk;
@@ -982,60 +1006,60 @@ fwd_bf16_pp2h_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             // a negative scale: S = (-Q) K^T, scaled by |s| in the softmax
             const uint32_t idS = p.scale < 0.f ? kIdSNeg : kIdS;
             constexpr uint32_t idO = idesc_bf16_f32(BM, D, false, true);
-            auto wait_piece = [&](int qq) {
-                return mbar_wait(bars.full(qq % P), (uint32_t)(qq / P) & 1u, abort_flag, p.dev_status);
+            auto wait_k = [&](int kk) {
+                return mbar_wait(bars.kfull(kk % KS), (uint32_t)(kk / KS) & 1u, abort_flag, p.dev_status);
             };
-            auto piece = [&](int qq) { return sR + (qq % P) * C::kTileBytes; };
-            auto mma_s = [&](int x, int qq) {
-                const uint32_t kb = piece(qq), qb = sQ + x * C::kTileBytes;
+            auto wait_v = [&](int vv) {
+                return mbar_wait(bars.vfull(vv % VS), (uint32_t)(vv / VS) & 1u, abort_flag, p.dev_status);
+            };
+            // S_x from K piece kk; its commit releases K piece kk (and V piece kk - 2, read before it)
+            auto mma_s = [&](int x, int kk) {
+                const uint32_t kb = sK + (kk % KS) * C::kTileBytes, qb = sQ + x * C::kTileBytes;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
                     mma_ss(tmem + C::scol(x), smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
                            idS, ks > 0);
                 }
-                mma_commit(bars.empty(qq % P));
+                mma_commit(bars.kempty(kk % KS));
                 mma_commit(bars.sfull(x));
             };
-            auto mma_pv = [&](int x, int qq, bool first) {
-                const uint32_t vb = piece(qq);
+            // PV_x from V piece vv: no commit of its own (the next S_x's commit covers it)
+            auto mma_pv = [&](int x, int vv, bool first) {
+                const uint32_t vb = sV + (vv % VS) * C::kTileBytes;
 #pragma unroll
                 for (int ks = 0; ks < BN / 16; ++ks)
                     mma_ts(tmem + C::kOCol0 + x * D, tmem + C::scol(x) + ks * 8,
                            smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO, (!first || ks > 0) ? 1u : 0u);
-                mma_commit(bars.empty(qq % P));
             };
-            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status) && wait_piece(0);
+            bool ok = mbar_wait(bars.q(), 0, abort_flag, p.dev_status) && wait_k(0);
             if (ok) {
                 tc_fence_after();
                 mma_s(0, 0);
-                ok = wait_piece(1);
+                ok = wait_k(1);
             }
             if (ok) {
                 tc_fence_after();
                 mma_s(1, 1);
             }
-            int q = 2;
             for (int i = 0; i < n && ok; ++i) {
                 const bool more = i + 1 < n;
                 const uint32_t ph = (uint32_t)i & 1u;
-                const int qa_v = q, qa_k = q + 1, qb_v = more ? q + 2 : q + 1, qb_k = q + 3;
-                q += more ? 4 : 2;
                 // V_A(i) and K_A(i+1) were loaded long ago: check them while tile A's softmax still
                 // runs, so that only P_A(i) is waited for on the path from softmax to PV
-                if (!(ok = wait_piece(qa_v))) break;
-                if (more && !(ok = wait_piece(qa_k))) break;
+                if (!(ok = wait_v(2 * i))) break;
+                if (more && !(ok = wait_k(2 * i + 2))) break;
                 if (!(ok = mbar_wait(bars.pfull(0), ph, abort_flag, p.dev_status))) break;
                 tc_fence_after();
-                mma_pv(0, qa_v, i == 0);
-                if (more) mma_s(0, qa_k);
+                mma_pv(0, 2 * i, i == 0);
+                if (more) mma_s(0, 2 * i + 2);
                 else mma_commit(bars.odone(0));
-                if (!(ok = wait_piece(qb_v))) break;
-                if (more && !(ok = wait_piece(qb_k))) break;
+                if (!(ok = wait_v(2 * i + 1))) break;
+                if (more && !(ok = wait_k(2 * i + 3))) break;
                 if (!(ok = mbar_wait(bars.pfull(1), ph, abort_flag, p.dev_status))) break;
                 tc_fence_after();
-                mma_pv(1, qb_v, i == 0);
-                if (more) mma_s(1, qb_k);
+                mma_pv(1, 2 * i + 1, i == 0);
+                if (more) mma_s(1, 2 * i + 3);
                 else mma_commit(bars.odone(1));
             }
             if (!ok) {
