@@ -88,7 +88,7 @@ cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O
 int device_sm_count();
 
 // The calling thread's current CUDA context (cuCtxGetCurrent), or nullptr when none is
-// current or the driver entry point is unavailable.  Device addresses of the library's
+// current or the CUDA driver API entry point is unavailable.  Device addresses of the library's
 // __device__ variables are cached per context with it.
 void *current_context();
 
