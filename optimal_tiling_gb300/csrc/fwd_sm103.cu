@@ -124,7 +124,9 @@ __device__ __forceinline__ bool visited(const uint8_t *hm, int mb, int mnb, int 
 constexpr uint32_t kIdS = idesc_bf16_f32(BM, BN, false, false);
 constexpr uint32_t kIdSNeg = kIdS | kIdescNegateA;
 
-template <int D, bool TAIL>
+// FINE: the mask has 64-row blocks (a visited 128-key block can be removed for a 64-key half
+// of a warp's rows, and the softmax then skips that half's scores altogether).
+template <int D, bool TAIL, bool FINE>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, const Problem p,
@@ -273,7 +275,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bool ok = true;
         // 64-row mask blocks: this warp's 32 rows lie in one mask row, so each
         // 64-key half of a visited block is kept or removed for the whole warp.
-        const bool fine = hm != nullptr && mb == 64;
+        constexpr bool fine = FINE;
+        // a removed half's scores are not loaded or reduced (FINE and TAIL only)
+        constexpr bool kSkipHalves = FINE || TAIL;
         // TAIL: rows 64-127 of the last tile may all lie past N, below the mask's last row
         const bool wrow = !TAIL || 2 * tile + warp / 2 < mnb;
         const uint8_t *wmask = fine && wrow ? hm + (size_t)(2 * tile + warp / 2) * mnb : nullptr;
@@ -306,10 +310,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tc_fence_after();
             const uint32_t scol = lane_base + (b ? kSCol1 : kSCol0);
             uint32_t r[4][32];
-            tmem_ld32(scol + 0, r[0]);
-            tmem_ld32(scol + 32, r[1]);
-            tmem_ld32(scol + 64, r[2]);
-            tmem_ld32(scol + 96, r[3]);
+            if (!kSkipHalves || half_kept[0]) {
+                tmem_ld32(scol + 0, r[0]);
+                tmem_ld32(scol + 32, r[1]);
+            }
+            if (!kSkipHalves || half_kept[1]) {
+                tmem_ld32(scol + 64, r[2]);
+                tmem_ld32(scol + 96, r[3]);
+            }
             tmem_wait_ld();
             reg_fence(r[0]);
             reg_fence(r[1]);
@@ -328,6 +336,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             float mxq[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                if (kSkipHalves && !half_kept[q >> 1]) {
+                    mxq[q] = -INFINITY;
+                    continue;
+                }
                 mxq[q] = fmaxf(__uint_as_float(r[q][0]), __uint_as_float(r[q][1]));
 #pragma unroll
                 for (int t = 1; t < 16; ++t)
@@ -1689,9 +1701,9 @@ cudaError_t launch_pp(const Problem &p, const FwdMaps &m, void *O, float *LSE, c
     return cudaGetLastError();
 }
 
-template <int D, bool TAIL>
+template <int D, bool TAIL, bool FINE>
 cudaError_t launch_d(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st) {
-    auto kern = fwd_bf16_kernel<D, TAIL>;
+    auto kern = fwd_bf16_kernel<D, TAIL, FINE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((p.N + BM - 1) / BM, p.B * p.H);
@@ -1715,6 +1727,14 @@ cudaError_t launch_pp2h(const Problem &p, const FwdMaps &m, void *O, float *LSE,
                                                                static_cast<__nv_bfloat16 *>(O), LSE);
     }
     return cudaGetLastError();
+}
+
+// the single-tile kernel's instantiation: partial last tile, 64-row mask blocks
+template <int D>
+cudaError_t launch_single(const Problem &p, const FwdMaps &m, void *O, float *LSE, cudaStream_t st, bool tail) {
+    const bool fine = p.mask != nullptr && p.mask_block == 64;
+    if (tail) return fine ? launch_d<D, true, true>(p, m, O, LSE, st) : launch_d<D, true, false>(p, m, O, LSE, st);
+    return fine ? launch_d<D, false, true>(p, m, O, LSE, st) : launch_d<D, false, false>(p, m, O, LSE, st);
 }
 
 template <bool TAIL>
@@ -1746,13 +1766,11 @@ cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, floa
         case 64:
             return pp     ? launch_pp<64>(p, maps, O, LSE, st)
                    : pp2h ? launch_pp2h<64>(p, maps, O, LSE, st)
-                   : tail ? launch_d<64, true>(p, maps, O, LSE, st)
-                          : launch_d<64, false>(p, maps, O, LSE, st);
+                          : launch_single<64>(p, maps, O, LSE, st, tail);
         case 128:
             return pp     ? launch_pp<128>(p, maps, O, LSE, st)
                    : pp2h ? launch_pp2h<128>(p, maps, O, LSE, st)
-                   : tail ? launch_d<128, true>(p, maps, O, LSE, st)
-                          : launch_d<128, false>(p, maps, O, LSE, st);
+                          : launch_single<128>(p, maps, O, LSE, st, tail);
         case 256: return tail ? launch_ring<true>(p, maps, O, LSE, st) : launch_ring<false>(p, maps, O, LSE, st);
         default: return cudaErrorNotSupported;
     }
