@@ -78,11 +78,15 @@ struct FwdCfg {
     static constexpr int kBarOff = kVOff + kStages * kTileBytes;
     // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain
     static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
+    // misc: tensor-memory address (+0), abort flag (+8), per K/V stage the 64-key halves of its
+    // block that some row of the tile keeps (+16, 64-row masks)
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kHalvesOff = kMiscOff + 16;
     // visited key blocks as a bit set: masks with up to 32 * kMaxMaskWords blocks per row
     static constexpr int kMaxMaskWords = 256;
     static constexpr int kBitsOff = kMiscOff + 64;
     static constexpr int kSmemBytes = kBitsOff + 4 * kMaxMaskWords + 1024;  // + slack to align the base
+    static_assert(kHalvesOff + kStages <= kBitsOff, "misc area");
     static_assert(kChunkBytes == 16384, "slab layout");
     static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -149,6 +153,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
     const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
     const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+    // FINE: per K/V stage, the key halves of its block that some row of the tile keeps (bit 0:
+    // keys 0-63), written by the producer before the V load's arrival and read by the issuer after
+    // its wait on V, so that PV skips the k-steps of a half no row keeps (their P is zero)
+    uint8_t *khalves = sm + C::kHalvesOff;
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -213,6 +221,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sK + s * C::kTileBytes + c * C::kChunkBytes, &tmK, c * 64, krow, bars.kfull(s));
                 if (it >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                if constexpr (FINE) {
+                    const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + 2 * j, *r1 = r0 + mnb;
+                    const bool t1 = !TAIL || 2 * tile + 1 < mnb, j1 = !TAIL || 2 * j + 1 < mnb;
+                    const bool h0 = (r0[0] | (t1 ? r1[0] : 0)) != 0;
+                    const bool h1 = ((j1 ? r0[1] : 0) | (t1 && j1 ? r1[1] : 0)) != 0;
+                    khalves[s] = (uint8_t)((h0 ? 1u : 0u) | (h1 ? 2u : 0u));
+                }
                 mbar_arrive_expect_tx(bars.vfull(s), C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sV + s * C::kTileBytes + c * C::kChunkBytes, &tmV, c * 64, krow, bars.vfull(s));
@@ -253,10 +268,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 tc_fence_after();
                 const uint32_t pcol = tmem + ((it & 1) ? kSCol1 : kSCol0);
                 const uint32_t vb = sV + s * C::kTileBytes;
+                const uint32_t kh = FINE ? khalves[s] : 3u;
+                if (kh == 3u) {
 #pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks)
-                    mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024), idO,
-                           (it > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < BN / 16; ++ks)
+                        mma_ts(tmem + kOCol, pcol + ks * 8, smem_desc_sw128(vb + ks * 2048, C::kChunkBytes, 1024),
+                               idO, (it > 0 || ks > 0) ? 1u : 0u);
+                } else {  // one key half kept by some row: its four k-steps only
+                    const int k0 = kh == 1u ? 0 : 4;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        mma_ts(tmem + kOCol, pcol + (k0 + k4) * 8,
+                               smem_desc_sw128(vb + (k0 + k4) * 2048, C::kChunkBytes, 1024), idO,
+                               (it > 0 || k4 > 0) ? 1u : 0u);
+                }
                 // vempty(s) also tells the softmax that PV_it is complete (O may be rescaled, or read
                 // after the last block): one commit per block fewer than a barrier of its own
                 mma_commit(bars.vempty(s));
