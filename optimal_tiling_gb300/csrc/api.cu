@@ -292,8 +292,9 @@ attn_status fwd_impl(const void *Q, const void *K, const void *V, void *O, float
     }
     const uint64_t rows = (uint64_t)B * H * N;
     attn::FwdMaps maps;
-    if (!make_map_bf16(&maps.q, Q, d, rows, 128) || !make_map_bf16(&maps.k, K, d, rows, 128) ||
-        !make_map_bf16(&maps.v, V, d, rows, d == 256 ? 64 : 128) || !make_map_bf16(&maps.o, O, d, rows, 128))
+    const bool half = attn::fwd_kv_half_boxes(p);  // K and V loaded in 64-key mask columns
+    if (!make_map_bf16(&maps.q, Q, d, rows, 128) || !make_map_bf16(&maps.k, K, d, rows, half ? 64 : 128) ||
+        !make_map_bf16(&maps.v, V, d, rows, (half || d == 256) ? 64 : 128) || !make_map_bf16(&maps.o, O, d, rows, 128))
         return ATTN_ERR_CUDA;
     return launch_status(attn::launch_fwd_bf16(p, maps, O, LSE, st));
 }

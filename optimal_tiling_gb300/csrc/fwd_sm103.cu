@@ -149,7 +149,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint8_t *hm = p.head_mask(head);
     const int mb = p.mask_block, mnb = p.mask_nb();
     uint32_t *vwords = reinterpret_cast<uint32_t *>(sm + C::kBitsOff);
-    const int nwords = (nb + 31) >> 5;
+    // FINE without TAIL: the visit set is over 64-key mask columns (a column is visited when
+    // either 64-row half of the tile keeps it), and the visited columns are taken two at a time
+    // into one 128-key block: K and V rows of the first in rows 0-63 of the ring stage, of the
+    // second in rows 64-127 (K and V maps with 64-row boxes).  A lone last column leaves the upper
+    // rows unused: its upper key half counts as removed for every row.
+    constexpr bool kPack = FINE && !TAIL;
+    const int nunits = kPack ? 2 * nb : nb;  // bit-set units: mask columns or key blocks
+    const int nwords = (nunits + 31) >> 5;
     const bool use_bits = hm != nullptr && nwords <= C::kMaxMaskWords;
     const int row0 = head * p.N + tile * BM;  // first row of this tile in the [B*H*N, D] view
     const uint32_t sQ = smem_addr(sm + C::kQOff), sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
@@ -178,7 +185,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mbar_arrive_expect_tx(bars.q(), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) tma_load_2d(sQ + c * C::kChunkBytes, &tmQ, c * 64, row0, bars.q());
     }
-    if (use_bits) build_visit_bits(vwords, nb, [&](int j) { return visited<TAIL>(hm, mb, mnb, tile, j); });
+    // kPack: mask column c of the tile's two mask rows
+    auto col_kept = [&](int c) -> bool {
+        const uint8_t *r0 = hm + (size_t)(2 * tile) * mnb + c;
+        return (r0[0] | r0[mnb]) != 0;
+    };
+    auto unit_visited = [&](int u) -> bool { return kPack ? col_kept(u) : visited<TAIL>(hm, mb, mnb, tile, u); };
+    if (use_bits) build_visit_bits(vwords, nunits, unit_visited);
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -188,21 +201,28 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const VisitBits vb{vwords, nwords};
-    int n = nb;  // key blocks this query tile visits
+    int nu = nunits;  // units (key blocks, or mask columns under kPack) this query tile visits
     if (use_bits) {
-        n = vb.count();
+        nu = vb.count();
     } else if (hm != nullptr) {  // rows longer than the bit set: read the mask directly
-        n = 0;
-        for (int j = 0; j < nb; ++j) n += visited<TAIL>(hm, mb, mnb, tile, j) ? 1 : 0;
+        nu = 0;
+        for (int u = 0; u < nunits; ++u) nu += unit_visited(u) ? 1 : 0;
     }
-    // the visited key block after j (callers ask only while one remains)
-    auto next_block = [&](int j) -> int {
-        if (hm == nullptr) return j + 1;
-        if (use_bits) return vb.next(j);
+    const int n = kPack ? (nu + 1) / 2 : nu;  // key blocks of the loop
+    // the visited unit after u (callers ask only while one remains)
+    auto next_block = [&](int u) -> int {
+        if (hm == nullptr) return u + 1;
+        if (use_bits) return vb.next(u);
         do {
-            ++j;
-        } while (!visited<TAIL>(hm, mb, mnb, tile, j));
-        return j;
+            ++u;
+        } while (!unit_visited(u));
+        return u;
+    };
+    // kPack: the two mask columns of block it, c[1] = -1 for a lone last column
+    auto block_cols = [&](int it, int &cur, int c[2]) {
+        c[0] = cur = next_block(cur);
+        c[1] = -1;
+        if (2 * it + 1 < nu) c[1] = cur = next_block(cur);
     };
 
     if (warp == kTmaWarp) {
@@ -212,9 +232,32 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             tma_prefetch_desc(&tmV);
             int j = -1;
             for (int it = 0; it < n; ++it) {
-                j = next_block(j);
                 const int s = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
+                if constexpr (kPack) {
+                    int cols[2];
+                    block_cols(it, j, cols);
+                    const int r0 = head * p.N + cols[0] * 64, r1 = head * p.N + cols[1] * 64;
+                    const uint32_t bytes = (cols[1] >= 0 ? 2u : 1u) * (uint32_t)(C::kTileBytes / 2);
+                    if (it >= S && !mbar_wait(bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                    mbar_arrive_expect_tx(bars.kfull(s), bytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        const uint32_t dst = sK + s * C::kTileBytes + c * C::kChunkBytes;
+                        tma_load_2d(dst, &tmK, c * 64, r0, bars.kfull(s));
+                        if (cols[1] >= 0) tma_load_2d(dst + C::kChunkBytes / 2, &tmK, c * 64, r1, bars.kfull(s));
+                    }
+                    if (it >= S && !mbar_wait(bars.vempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
+                    // every visited column is kept by some row of the tile
+                    khalves[s] = cols[1] >= 0 ? 3u : 1u;
+                    mbar_arrive_expect_tx(bars.vfull(s), bytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        const uint32_t dst = sV + s * C::kTileBytes + c * C::kChunkBytes;
+                        tma_load_2d(dst, &tmV, c * 64, r0, bars.vfull(s));
+                        if (cols[1] >= 0) tma_load_2d(dst + C::kChunkBytes / 2, &tmV, c * 64, r1, bars.vfull(s));
+                    }
+                    continue;
+                }
+                j = next_block(j);
                 const int krow = head * p.N + j * BN;
                 if (it >= S && !mbar_wait(bars.kempty(s), ph ^ 1u, abort_flag, p.dev_status)) break;
                 mbar_arrive_expect_tx(bars.kfull(s), C::kTileBytes);
@@ -310,7 +353,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         for (int it = 0; it < n; ++it) {
             const int b = it & 1;
             bool half_kept[2] = {true, true};
-            if (fine) {
+            if constexpr (kPack) {
+                int cols[2];
+                block_cols(it, j, cols);
+                half_kept[0] = wmask[cols[0]] != 0;
+                half_kept[1] = cols[1] >= 0 && wmask[cols[1]] != 0;
+            } else if (fine) {
                 j = next_block(j);
                 if (wmask != nullptr) {
                     half_kept[0] = wmask[2 * j] != 0;
@@ -1777,6 +1825,11 @@ cudaError_t launch_ring(const Problem &p, const FwdMaps &m, void *O, float *LSE,
 }
 
 }  // namespace
+
+bool fwd_kv_half_boxes(const Problem &p) {
+    // the single-tile kernel's FINE instantiation without TAIL (launch_single)
+    return p.mask != nullptr && p.mask_block == 64 && p.N % BM == 0 && (p.d == 64 || p.d == 128);
+}
 
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE, cudaStream_t st) {
     if (p.B * p.H > 65535) return cudaErrorNotSupported;

@@ -60,6 +60,9 @@ cudaError_t launch_bwd_f32(const Problem &p, const float *Q, const float *K, con
 struct FwdMaps {
     CUtensorMap q, k, v, o;  // 128-row boxes; at d = 256 V has 64-row boxes (loaded in 64-key halves)
 };
+// True when the forward kernel for p loads K and V in 64-row boxes (64-row masks, 128 | N,
+// d in {64, 128}: the visited 64-key mask columns are packed two to a key block).
+bool fwd_kv_half_boxes(const Problem &p);
 cudaError_t launch_fwd_bf16(const Problem &p, const FwdMaps &maps, void *O, float *LSE,
                             cudaStream_t st);
 

@@ -213,3 +213,51 @@ def test_long_mask_rows(oracle_mod, N, H, with_bwd):
                 gQ, gK, gV, _, _ = oracle_mod.bwd_naive(sub["q"], sub["k"], sub["v"], sub["do"], scale)
                 for g, r in zip(grads, (gQ, gK, gV)):
                     assert rel_l2(g[0, h][sl], r[0, 0]) <= TOL_BF16_GRAD_RL2
+
+
+def _kept_keys(mask_row, N):
+    """Key indices of the kept 64-blocks of one mask row."""
+    cols = np.nonzero(np.asarray(mask_row))[0]
+    return np.concatenate([np.arange(64 * c, min(64 * c + 64, N)) for c in cols]) if cols.size else np.zeros(0, int)
+
+
+def test_fine_mask_full_size_sampled(oracle_mod):
+    """The 64-row-block workload at full size in the bench's launch configuration (B=1 H=16
+    N=16384 d=128, one band-plus-random mask per head): sampled 64-row blocks against the
+    oracle's forward of those rows over the keys their mask row keeps (a removed score has
+    no weight, so the row's softmax is the one over the kept keys alone)."""
+    B, H, N, d = 1, 16, 16384, 128
+    scale = 1.0 / math.sqrt(d)
+    x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=0, with_do=False)
+    mask = inputs.band_random_mask_fine(N, B * H, seed=0)
+    o, lse = _fwd(x, scale, mask, 64, guarded=False)
+    O, L = o.float().cpu().numpy()[0], lse.cpu().numpy()[0]
+    nb = N // 64
+    for h, blk in ((0, 0), (3, 1), (7, 100), (11, 201), (15, nb - 1), (5, nb // 2)):
+        keys = _kept_keys(mask[h, blk], N)
+        rows = slice(64 * blk, 64 * blk + 64)
+        q = x["q"][0, h, rows][None, None]
+        kk = torch.from_numpy(keys)
+        k, v = x["k"][0, h, kk][None, None], x["v"][0, h, kk][None, None]
+        Or, Lr = oracle_mod.fwd_rect(q, k, v, scale)
+        assert max_abs(O[h, rows], Or[0, 0]) <= TOL_BF16_O_ABS
+        assert lse_rel(L[h, rows], Lr[0, 0]) <= TOL_BF16_LSE_REL
+
+
+@pytest.mark.parametrize("N", [524288, 532480])
+def test_long_fine_mask_rows(oracle_mod, N):
+    """64-row blocks on long rows, the diagonal kept: the forward keeps the visited 64-key
+    columns as a bit set up to 8192 columns (N = 524288) and reads the mask directly beyond.
+    Each 64-row block is an independent problem; sampled blocks against the oracle."""
+    d, scale = 128, 1.0 / math.sqrt(128)
+    x = inputs.make_inputs(1, 1, N, d, torch.bfloat16, seed=N % 997, with_do=False)
+    nb = N // 64
+    mask = torch.eye(nb, dtype=torch.uint8)
+    o, lse = _fwd(x, scale, mask, 64, guarded=False)
+    O, L = o.float().cpu().numpy()[0, 0], lse.cpu().numpy()[0, 0]
+    for blk in (0, 1, nb // 2 + 1, nb - 2, nb - 1):
+        sl = slice(blk * 64, (blk + 1) * 64)
+        sub = {k: v[:, :, sl] for k, v in x.items()}
+        Or, Lr = oracle_mod.fwd_naive(sub["q"], sub["k"], sub["v"], scale)
+        assert max_abs(O[sl], Or[0, 0]) <= TOL_BF16_O_ABS
+        assert lse_rel(L[sl], Lr[0, 0]) <= TOL_BF16_LSE_REL
