@@ -103,8 +103,9 @@ struct BwdCfg {
     static constexpr uint32_t kDqALbo = D == 64 ? (uint32_t)(kZeroOff - kKOff) : (uint32_t)kKVSlab;
     static constexpr int kDqM = 128;                     // M of the dQ^T product
     static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
-    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull, dqfree, dpfree, kvdone, drain[3]
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3;
+    // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull, dqfree, dpfree, kvdone, drain[3],
+    // stagefree (the persistent kernel)
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // visited query blocks as a bit set: up to 32 * kMaxMaskWords 64-row blocks (N <= 131072)
     static constexpr int kMaxMaskWords = 64;
@@ -132,6 +133,7 @@ struct BwdBars {
     __device__ uint32_t dpfree() const { return base + 8u * (9 + 2 * kStages); }
     __device__ uint32_t kvdone() const { return base + 8u * (10 + 2 * kStages); }
     __device__ uint32_t drain(int role) const { return base + 8u * (11 + 2 * kStages + role); }
+    __device__ uint32_t stagefree() const { return base + 8u * (14 + 2 * kStages); }
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -740,6 +742,410 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if constexpr (HALVES) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// ------------------------------------------------------------------------- 2b
+// Every bulk group this thread committed has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Persistent form of bwd_main for dense problems (no mask, 128 | N): a grid of at most one CTA per
+// SM, CTA c taking key tiles c, c + P, c + 2P, ... (P = gridDim.x) below split_from.  Every tile
+// has the same n query blocks, so each role's block counter g = T n + it (T = the CTA's tile
+// number) runs on across tiles, and the ring, S, dP, dS and dQ^T barriers keep one phase sequence.
+// Between tiles:
+//   - kvdone counts three commits, one per issuing thread after a tile's last products: then K, V
+//     and dS are no longer read and dK, dV are final.  The producer then loads the next K/V tile,
+//     which overlaps the epilogue; the Q/dO ring runs on without a break.
+//   - The epilogue reads dK and dV into registers before its warps signal pfull for the next tile's
+//     first block, and the next dV and dK products wait for that pfull, so they cannot overwrite
+//     the accumulators early.
+//   - dK is staged in the two dS tiles, dV in the dQ staging tile once the drain's reductions of the
+//     tile have read it (stagefree); all eight P/dS warps meet after the stores have read both, so
+//     that no dS or dQ of the next tile is written there before.
+// One CTA per SM also removes the per-CTA start (barrier set-up, tensor-memory allocation, the
+// first loads) from all tiles but the first.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                   const Problem p, const float *__restrict__ L2, const float *__restrict__ Dv,
+                   float *__restrict__ dQacc, const int split_from) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const BwdBars bars{smem_addr(sm + C::kBarOff)};
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::kMiscOff + 8);
+    // the grid of split tiles reads nothing this grid writes (both only add into accumulators)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = p.N / BQ;        // query blocks of every tile
+    const int tph = p.N / BKV;     // key tiles per head
+    const int cta = (int)blockIdx.x, P = (int)gridDim.x;
+    const int ntile = cta < split_from ? (split_from - 1 - cta) / P + 1 : 0;
+    auto tile_head = [&](int T) -> int { return (cta + T * P) / tph; };
+    auto tile_kv0 = [&](int T) -> int {  // first K/V row of the CTA's tile T in the [B*H*N, D] view
+        const int tile = cta + T * P;
+        return (tile / tph) * p.N + (tile % tph) * BKV;
+    };
+    const uint32_t sK = smem_addr(sm + C::kKOff), sV = smem_addr(sm + C::kVOff);
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bars.kv(), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bars.qfull(s), 1);
+            mbar_init(bars.qempty(s), 2);   // dV (warp 13) and dK (warp 14) are the last readers
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars.sfull(b), 2);    // S^T (warp 13) and dP^T (warp 14)
+            mbar_init(bars.pfull(b), 8);    // one lane of each P/dS warp
+            mbar_init(bars.dsfree(b), 2);   // dK (warp 14) and dQ^T (warp 15) read dS
+        }
+        mbar_init(bars.dqfull(), 1);
+        mbar_init(bars.dqfree(), 4);        // the drain warps have read dQ^T (one lane each)
+        mbar_init(bars.dpfree(), 8);        // the P/dS warps have read dP^T (one lane each)
+        mbar_init(bars.kvdone(), 3);        // a tile's products complete: one commit per issuer
+        mbar_init(bars.stagefree(), 1);     // the drain's reductions of a tile have read its staging
+        for (int r = 0; r < 3; ++r) mbar_init(bars.drain(r), 1);
+        fence_barrier_init();
+        if (ntile > 0) {
+            mbar_arrive_expect_tx(bars.kv(), 2 * C::kKVTile);
+            const int kv0 = tile_kv0(0);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_2d(sK + c * C::kKVSlab, &tmK, c * 64, kv0, bars.kv());
+                tma_load_2d(sV + c * C::kKVSlab, &tmV, c * 64, kv0, bars.kv());
+            }
+        }
+    }
+    if constexpr (C::kZeroBytes > 0) {
+        // the zero rows of the padded K^T operand (read by the tensor core: async proxy)
+        uint4 *z = reinterpret_cast<uint4 *>(sm + C::kZeroOff);
+        for (int i = tid; i < C::kZeroBytes / 16; i += kThreads) z[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sQ = smem_addr(sm + C::kQOff), sdO = smem_addr(sm + C::kdOOff);
+    const uint32_t sDs = smem_addr(sm + C::kDsOff), sDq = smem_addr(sm + C::kDqOff);
+    const uint32_t sLd = smem_addr(sm + C::kLdOff);
+    const float *ld_f = reinterpret_cast<const float *>(sm + C::kLdOff);
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && ntile > 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmdO);
+            bool ok = true;
+            for (int T = 0; T < ntile && ok; ++T) {
+                const int head = tile_head(T);
+                if (T > 0) {
+                    // every product of the previous tile is complete: K and V may be reloaded
+                    if (!(ok = role_wait<D>(bars.kvdone(), (uint32_t)(T - 1) & 1u, abort_flag, p.dev_status)))
+                        break;
+                    const int kv0 = tile_kv0(T);
+                    mbar_arrive_expect_tx(bars.kv(), 2 * C::kKVTile);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_2d(sK + c * C::kKVSlab, &tmK, c * 64, kv0, bars.kv());
+                        tma_load_2d(sV + c * C::kKVSlab, &tmV, c * 64, kv0, bars.kv());
+                    }
+                }
+                for (int it = 0; it < n; ++it) {
+                    const int g = T * n + it, s = g % kStages;
+                    if (g >= kStages &&
+                        !(ok = role_wait<D>(bars.qempty(s), ((uint32_t)(g / kStages) & 1u) ^ 1u, abort_flag,
+                                            p.dev_status)))
+                        break;
+                    const int q0 = head * p.N + it * BQ;
+                    mbar_arrive_expect_tx(bars.qfull(s), 2 * C::kQTile + 2 * BQ * 4);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_2d(sQ + s * C::kQTile + c * C::kQSlab, &tmQ, c * 64, q0, bars.qfull(s));
+                        tma_load_2d(sdO + s * C::kQTile + c * C::kQSlab, &tmdO, c * 64, q0, bars.qfull(s));
+                    }
+                    bulk_load(sLd + s * 2 * BQ * 4, L2 + q0, BQ * 4, bars.qfull(s));
+                    bulk_load(sLd + s * 2 * BQ * 4 + BQ * 4, Dv + q0, BQ * 4, bars.qfull(s));
+                }
+            }
+        }
+    } else if (warp >= kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        const int role = warp - kMmaWarp;  // 0: S^T then dV, 1: dP^T then dK, 2: dQ^T
+        if (lane == 0 && ntile > 0) {
+            constexpr uint32_t idSP = idesc_bf16_f32(BKV, BQ, false, false);  // S^T, dP^T
+            constexpr uint32_t idKV = idesc_bf16_f32(BKV, D, false, true);    // dV, dK
+            constexpr uint32_t idQ = idesc_bf16_f32(C::kDqM, BQ, true, true); // dQ^T (M padded to 128)
+            bool ok = true;
+            // S^T_g (role 0) or dP^T_g (role 1) into buffer g & 1
+            auto issue_first = [&](int g) -> bool {
+                const int s = g % kStages, b = g & 1;
+                if (!role_wait<D>(bars.qfull(s), (uint32_t)(g / kStages) & 1u, abort_flag, p.dev_status))
+                    return false;
+                // one dP buffer: the P/dS warps must have read dP^T of block g-1
+                if (role == 1 && g >= 1 &&
+                    !role_wait<D>(bars.dpfree(), (uint32_t)(g - 1) & 1u, abort_flag, p.dev_status))
+                    return false;
+                tc_fence_after();
+                const uint32_t xb = (role == 0 ? sQ : sdO) + s * C::kQTile;
+                const uint32_t kb = role == 0 ? sK : sV;
+                const uint32_t dcol = tmem + (role == 0 ? C::kColS + b * BQ : C::kColDP);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t ko = (ks >> 2) * C::kKVSlab + (ks & 3) * 32;
+                    const uint32_t qo = (ks >> 2) * C::kQSlab + (ks & 3) * 32;
+                    mma_ss(dcol, smem_desc_sw128(kb + ko, 16, 1024), smem_desc_sw128(xb + qo, 16, 1024), idSP,
+                           ks > 0);
+                }
+                mma_commit(bars.sfull(b));
+                return true;
+            };
+            for (int T = 0; T < ntile && ok; ++T) {
+                // K and V of tile T are in shared memory
+                if (!(ok = role_wait<D>(bars.kv(), (uint32_t)T & 1u, abort_flag, p.dev_status))) break;
+                const int g0 = T * n;
+                if (role < 2) {
+                    if (!(ok = issue_first(g0))) break;
+                    for (int it = 0; it < n && ok; ++it) {
+                        const int g = g0 + it, s = g % kStages, b = g & 1;
+                        if (it + 1 < n && !(ok = issue_first(g + 1))) break;
+                        if (!(ok = role_wait<D>(bars.pfull(b), (uint32_t)(g >> 1) & 1u, abort_flag, p.dev_status)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t qb = sQ + s * C::kQTile, gb = sdO + s * C::kQTile, dsb = sDs + b * C::kDsTile;
+                        if (role == 0) {
+                            // dV += P^T dO_i : A = P^T (bf16 pairs in the S columns), B = dO_i
+#pragma unroll
+                            for (int ks = 0; ks < BQ / 16; ++ks)
+                                mma_ts(tmem + C::kColDV, tmem + C::kColS + b * BQ + (ks >> 1) * 32 + (ks & 1) * 8,
+                                       smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV,
+                                       (it > 0 || ks > 0) ? 1u : 0u);
+                        } else {
+                            // dK += dS^T Q_i : A = dS^T (K-major, 64 q per row), B = Q_i
+#pragma unroll
+                            for (int ks = 0; ks < BQ / 16; ++ks)
+                                mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
+                                       smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV,
+                                       (it > 0 || ks > 0) ? 1u : 0u);
+                            mma_commit(bars.dsfree(b));
+                        }
+                        mma_commit(bars.qempty(s));
+                    }
+                } else {
+                    for (int it = 0; it < n && ok; ++it) {
+                        const int g = g0 + it, b = g & 1;
+                        if (!(ok = role_wait<D>(bars.pfull(b), (uint32_t)(g >> 1) & 1u, abort_flag, p.dev_status)))
+                            break;
+                        // one dQ^T buffer: the drain warps must have read dQ^T of block g-1
+                        if (g >= 1 &&
+                            !(ok = role_wait<D>(bars.dqfree(), (uint32_t)(g - 1) & 1u, abort_flag, p.dev_status)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t dsb = sDs + b * C::kDsTile;
+                        // dQ_i^T = K^T dS_i^T : A = K^T (d contiguous), B = dS (q contiguous)
+#pragma unroll
+                        for (int ks = 0; ks < BKV / 16; ++ks)
+                            mma_ss(tmem + C::kColQ, smem_desc_sw128(sK + ks * 2048, C::kDqALbo, 1024),
+                                   smem_desc_sw128(dsb + ks * 2048, C::kDsTile, 1024), idQ, ks > 0);
+                        mma_commit(bars.dsfree(b));
+                        mma_commit(bars.dqfull());
+                    }
+                }
+                // this thread's products of tile T (those reading K, V and dS included)
+                if (ok) mma_commit(bars.kvdone());
+            }
+            if (!ok) {
+                // let every MMA this thread issued finish before tensor memory is released
+                mma_commit(bars.drain(role));
+                mbar_wait(bars.drain(role), 0, abort_flag, p.dev_status);
+            }
+        }
+    } else if (warp < kDqWarp0) {
+        // ------------------------------------------------------------ P / dS warps 0-7
+        // As in bwd_main: thread = key, warps 0-3 queries 0-31 of a block, warps 4-7 queries 32-63.
+        const int h = warp >> 2;
+        const int key = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const float sl2 = p.scale * kLog2e;
+        const uint32_t my_ds_row = (uint32_t)key * 128u;
+        uint8_t *ds_gen = sm + C::kDsOff;
+        bool ok = true;
+        for (int T = 0; T < ntile; ++T) {
+            for (int it = 0; it < n && ok; ++it) {
+                const int g = T * n + it, s = g % kStages, b = g & 1;
+                ok = mbar_wait(bars.sfull(b), (uint32_t)(g >> 1) & 1u, abort_flag, p.dev_status);
+                if (ok && g >= 2)
+                    ok = mbar_wait(bars.dsfree(b), (uint32_t)((g - 2) >> 1) & 1u, abort_flag, p.dev_status);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const float *nl2 = ld_f + s * 2 * BQ;  // -LSE log2(e) of the 64 queries, then -D
+                const float *ndv = nl2 + BQ;
+                uint32_t pk[16], dk[16];
+                uint32_t sr[32], pr[32];
+                tmem_ld32(lane_base + C::kColS + b * BQ + h * 32, sr);
+                tmem_ld32(lane_base + C::kColDP + h * 32, pr);
+                tmem_wait_ld();
+                reg_fence(sr);
+                reg_fence(pr);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.dpfree());
+                const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const int q = h * 32 + 2 * t;
+                    float4 nl, nd;
+                    if ((t & 1) == 0) {
+                        nl = *reinterpret_cast<const float4 *>(nl2 + q);
+                        nd = *reinterpret_cast<const float4 *>(ndv + q);
+                    }
+                    const uint64_t l2p = (t & 1) ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y);
+                    const uint64_t dvp = (t & 1) ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y);
+                    const uint64_t x2 =
+                        f2_fma(f2_pack(__uint_as_float(sr[2 * t]), __uint_as_float(sr[2 * t + 1])), sl2x2, l2p);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    const uint64_t g2 =
+                        f2_add(f2_pack(__uint_as_float(pr[2 * t]), __uint_as_float(pr[2 * t + 1])), dvp);
+                    float d0, d1;
+                    f2_unpack(f2_mul(f2_pack(p0, p1), g2), d0, d1);
+                    pk[t] = pack_bf16(p0, p1);
+                    dk[t] = pack_bf16(d0, d1);
+                }
+                tmem_st16(lane_base + C::kColS + b * BQ + h * 32, pk);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = h * 4 + c;
+                    const uint32_t off = my_ds_row + (uint32_t)((chunk ^ (key & 7)) * 16);
+                    *reinterpret_cast<uint4 *>(ds_gen + b * C::kDsTile + off) =
+                        make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.pfull(b));
+            }
+            // -------------------------------------------------------- dK (warps 0-3), dV (warps 4-7) of tile T
+            // The warps meet at the named barriers whatever `ok` says (after a timed-out wait the
+            // work is skipped, the barriers kept), so that no warp waits for one that gave up.
+            if (ok) {
+                ok = mbar_wait(bars.kvdone(), (uint32_t)T & 1u, abort_flag, p.dev_status);
+                if (ok && h == 1) ok = mbar_wait(bars.stagefree(), (uint32_t)T & 1u, abort_flag, p.dev_status);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+            }
+            uint8_t *stage = sm + (h == 0 ? C::kDsOff : C::kDqOff);
+            const uint32_t acc = lane_base + (h == 0 ? C::kColDK : C::kColDV);
+            const float mul = h == 0 ? p.scale : 1.f;
+            if (ok) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(acc + c0, a);
+                    tmem_wait_ld();
+                    reg_fence(a);
+                    uint32_t pa[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        pa[t] = pack_bf16(__uint_as_float(a[2 * t]) * mul, __uint_as_float(a[2 * t + 1]) * mul);
+                    uint8_t *slab = stage + (c0 >> 6) * C::kKVSlab + key * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int u = ((c0 & 63) >> 3) + q;  // 16-byte unit within the 128-byte row
+                        *reinterpret_cast<uint4 *>(slab + ((u ^ (key & 7)) << 4)) =
+                            make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+            }
+            // the accumulators are read: the next tile's first dV and dK (after its first pfull)
+            // may overwrite them
+            tc_fence_before();
+            named_bar_sync(2 + h, 128);
+            if ((tid & 127) == 0 && ok) {
+                const CUtensorMap *tm = h == 0 ? &tmdK : &tmdV;
+                const uint32_t src = smem_addr(stage);
+                const int kv0 = tile_kv0(T);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) tma_store_2d(tm, c * 64, kv0, src + c * C::kKVSlab);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+            // both staging tiles have been read: dS and dQ of the next tile may be written there
+            named_bar_sync(4, 256);
+        }
+        if ((tid & 127) == 0) bulk_wait_all();
+    } else if (warp < kTmaWarp) {
+        // ------------------------------------------------------------ dQ drain warps 8-11
+        // As in bwd_main; every drain thread runs the same sequence of named barriers whatever
+        // happens (after a failed wait the work is skipped, the barriers kept).
+        const int t = tid - kDqWarp0 * 32;  // 0..127 = d index (tensor memory lane); rows >= D are padding
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        float *dq_gen = reinterpret_cast<float *>(sm + C::kDqOff);
+        bool alive = true;
+        for (int T = 0; T < ntile; ++T) {
+            const int head = tile_head(T);
+            for (int it = 0; it < n; ++it) {
+                const int g = T * n + it;
+                bool ok = alive && mbar_wait(bars.dqfull(), (uint32_t)g & 1u, abort_flag, p.dev_status);
+                ok = __all_sync(0xffffffffu, ok);
+                uint32_t r0[32], r1[32];
+                if (ok) {
+                    tc_fence_after();
+                    tmem_ld32(lane_base + C::kColQ, r0);
+                    tmem_ld32(lane_base + C::kColQ + 32, r1);
+                    tmem_wait_ld();
+                    reg_fence(r0);
+                    reg_fence(r1);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars.dqfree());
+                }
+                const size_t q0 = (size_t)head * p.N + (size_t)it * BQ;  // the block's accumulator rows
+                auto stage = [&](const uint32_t(&r)[32], int hq) {
+                    if (t == 0) bulk_wait_read_but_one();
+                    named_bar_sync(1, 128);
+                    if (ok && t < D) {
+                        float *dst = dq_gen + hq * 32 * D;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) dst[q * D + t] = __uint_as_float(r[q]);
+                        fence_proxy_async_smem();
+                    }
+                    named_bar_sync(1, 128);
+                    if (t == 0 && ok) {
+                        bulk_reduce_add_f32(dQacc + (q0 + 32 * hq) * D, sDq + hq * (C::kDqTile / 2),
+                                            C::kDqTile / 2);
+                        bulk_commit();
+                    }
+                };
+                stage(r0, 0);
+                stage(r1, 1);
+                alive = alive && ok;
+            }
+            // the tile's reductions have read the staging tile: the epilogue may stage dV there
+            if (t == 0) {
+                bulk_wait_read_all();
+                if (alive) mbar_arrive(bars.stagefree());
+            }
+        }
+        if (t == 0) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 // ------------------------------------------------------------------------- 3
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__restrict__ acc,
                                                               __nv_bfloat16 *__restrict__ dQ, float scale,
@@ -835,18 +1241,28 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
         }
         return cudaGetLastError();
     }
+    // dense problems: the persistent kernel (every tile has the same query blocks)
+    const bool persist = p.mask == nullptr;
     auto kern = bwd_main_kernel<D, false, false>;
+    auto kp = bwd_persist_kernel<D>;
     auto kh = bwd_main_kernel<D, true, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
+    e = persist ? cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes)
+                : cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
     if (e == cudaSuccess && split > 0)
         e = cudaFuncSetAttribute(kh, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     {
         // one timing scope over both launches: together they are the five products of every tile
         ProfScope prof_("bwd_main", st);
-        kern<<<dim3(p.N / BKV, p.B * p.H), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
-            m.q, m.k, m.v, m.dO, m.dk, m.dv, p, Dv + rows, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
-            static_cast<__nv_bfloat16 *>(dV), tiles - split, kvacc);
+        if (persist) {
+            const int full = tiles - split;  // tiles of the persistent grid, the rest split in halves
+            kp<<<(unsigned)std::min(full, device_sm_count()), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
+                m.q, m.k, m.v, m.dO, m.dk, m.dv, p, Dv + rows, Dv, dQacc, full);
+        } else {
+            kern<<<dim3(p.N / BKV, p.B * p.H), kThreads, BwdCfg<D>::kSmemBytes, st>>>(
+                m.q, m.k, m.v, m.dO, m.dk, m.dv, p, Dv + rows, Dv, dQacc, static_cast<__nv_bfloat16 *>(dK),
+                static_cast<__nv_bfloat16 *>(dV), tiles - split, kvacc);
+        }
         e = cudaGetLastError();
         if (e == cudaSuccess && split > 0) {
             // programmatic dependent launch: the halves may start while the last full tiles run

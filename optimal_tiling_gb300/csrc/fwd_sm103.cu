@@ -76,8 +76,9 @@ struct FwdCfg {
     static constexpr int kKOff = kQOff + kTileBytes;
     static constexpr int kVOff = kKOff + kStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], odone, drain
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1 + 1;
+    // q, kfull[S], kempty[S], vfull[S], vempty[S], sfull[2], pfull[2], drain (PV's completion is
+    // read from the release of its V stage)
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1;
     // misc: tensor-memory address (+0), abort flag (+8), per K/V stage the 64-key halves of its
     // block that some row of the tile keeps (+16, 64-row masks)
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -102,8 +103,7 @@ struct Bars {
     __device__ uint32_t vempty(int s) const { return base + 8u * (1 + 3 * stages + s); }
     __device__ uint32_t sfull(int b) const { return base + 8u * (1 + 4 * stages + b); }
     __device__ uint32_t pfull(int b) const { return base + 8u * (3 + 4 * stages + b); }
-    __device__ uint32_t odone() const { return base + 8u * (5 + 4 * stages); }
-    __device__ uint32_t drain() const { return base + 8u * (6 + 4 * stages); }
+    __device__ uint32_t drain() const { return base + 8u * (5 + 4 * stages); }
 };
 
 // Key block j (128 keys) is visited by query tile t when any mask entry that
@@ -178,7 +178,6 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             mbar_init(bars.sfull(b), 1);
             mbar_init(bars.pfull(b), 4 * 32);
         }
-        mbar_init(bars.odone(), 1);  // unused: vempty of the last V stage marks PV done
         mbar_init(bars.drain(), 1);
         fence_barrier_init();
         // the Q tile is needed whatever the mask says: start its load before the mask is read
