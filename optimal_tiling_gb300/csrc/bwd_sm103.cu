@@ -184,11 +184,14 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 // ------------------------------------------------------------------------- 1
 // D_i = sum_t dO_it O_it and L2_i = LSE_i log2(e) (the row's log-sum-exp in the base-2 units of
 // the exponentials below), both stored negated (-D, -L2: the main kernel adds them in packed
-// pairs); the dQ accumulator row is zeroed.  One warp per row.
+// pairs); the dQ accumulator row is zeroed.  d / 8 threads per row, each with 16-byte loads of O
+// and dO and two 16-byte zero stores (a warp takes 2 rows at d = 128, 4 at d = 64; 8 warps a block).
 // The split tiles' partial dK, dV (kv4: kv_n4 float4) are zeroed grid-stride.
 // D, L2 and the accumulator hold npad rows per head (N rounded up to the 64-row query block;
 // npad = N when 64 divides N, PAD = false): the rows from N on get D = 0 and L2 = +inf, so that
 // their probabilities, and with them their dS, are exactly zero in the main kernel.
+template <int D>
+constexpr int kPreRowsPerBlock = 8 * (32 / (D / 8));
 template <int D, bool PAD>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ O,
                                                       const __nv_bfloat16 *__restrict__ dO,
@@ -196,38 +199,42 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
                                                       size_t rows, float4 *__restrict__ kv4, size_t kv_n4,
                                                       const float *__restrict__ LSE, float *__restrict__ L2, int N,
                                                       int npad) {
+    constexpr int TPR = D / 8;  // threads per row
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < kv_n4; i += (size_t)gridDim.x * blockDim.x)
         kv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const size_t prow = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // row of the padded layout
-    const int lane = threadIdx.x & 31;
-    if (prow >= rows) return;
+    const int sub = threadIdx.x % TPR;
+    const size_t prow = (size_t)blockIdx.x * kPreRowsPerBlock<D> + threadIdx.x / TPR;  // row of the padded layout
+    const bool in = prow < rows;
     size_t row = prow;  // row of O, dO and LSE
-    bool pad = false;
+    bool pad = !in;
     if constexpr (PAD) {
         const size_t hh = prow / (size_t)npad, q = prow - hh * (size_t)npad;
-        pad = q >= (size_t)N;
+        pad = pad || q >= (size_t)N;
         row = hh * (size_t)N + q;
     }
     float acc = 0.f;
     if (!pad) {
-        constexpr int E = D / 32;  // elements per lane (2 or 4)
-        const __nv_bfloat16 *o = O + row * D + lane * E;
-        const __nv_bfloat16 *g = dO + row * D + lane * E;
+        const uint4 a = *reinterpret_cast<const uint4 *>(O + row * D + sub * 8);
+        const uint4 b = *reinterpret_cast<const uint4 *>(dO + row * D + sub * 8);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int e = 0; e < E; e += 2) {
-            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(o + e));
-            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(g + e));
-            acc = fmaf(a.x, b.x, acc);
-            acc = fmaf(a.y, b.y, acc);
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&aw[e]));
+            const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bw[e]));
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
         }
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     }
-    if (lane == 0) {
+    // the TPR lanes of a row are aligned groups of a warp: xor offsets below TPR stay inside one
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (!in) return;
+    if (sub == 0) {
         Dv[prow] = -acc;
         L2[prow] = pad ? -INFINITY : -(LSE[row] * kLog2e);
     }
-    float4 *z = reinterpret_cast<float4 *>(dQacc + prow * D);
-    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 *z = reinterpret_cast<float4 *>(dQacc + prow * D) + sub * 2;
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------------- 2
@@ -1150,15 +1157,30 @@ bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *__restrict__ acc,
                                                               __nv_bfloat16 *__restrict__ dQ, float scale,
                                                               size_t n8) {
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
-        const float4 a = reinterpret_cast<const float4 *>(acc)[2 * i];
-        const float4 b = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
-        uint4 o;
-        o.x = pack_bf16(a.x * scale, a.y * scale);
-        o.y = pack_bf16(a.z * scale, a.w * scale);
-        o.z = pack_bf16(b.x * scale, b.y * scale);
-        o.w = pack_bf16(b.z * scale, b.w * scale);
-        reinterpret_cast<uint4 *>(dQ)[i] = o;
+    // four 8-element units per thread and pass, their loads issued before any store
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n8; i0 += 4 * stride) {
+        float4 a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t i = i0 + u * stride;
+            if (i < n8) {
+                a[u] = reinterpret_cast<const float4 *>(acc)[2 * i];
+                b[u] = reinterpret_cast<const float4 *>(acc)[2 * i + 1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const size_t i = i0 + u * stride;
+            if (i < n8) {
+                uint4 o;
+                o.x = pack_bf16(a[u].x * scale, a[u].y * scale);
+                o.y = pack_bf16(a[u].z * scale, a[u].w * scale);
+                o.z = pack_bf16(b[u].x * scale, b[u].y * scale);
+                o.w = pack_bf16(b[u].z * scale, b[u].w * scale);
+                reinterpret_cast<uint4 *>(dQ)[i] = o;
+            }
+        }
     }
 }
 
@@ -1214,7 +1236,7 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
     {
         ProfScope prof_("bwd_pre", st);
         auto pre = npad != p.N ? bwd_pre_kernel<D, true> : bwd_pre_kernel<D, false>;
-        pre<<<(unsigned)((prows + 7) / 8), 256, 0, st>>>(
+        pre<<<(unsigned)((prows + kPreRowsPerBlock<D> - 1) / kPreRowsPerBlock<D>), 256, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dv, dQacc, prows,
             reinterpret_cast<float4 *>(kvacc), bwd_split_bytes(split, D) / sizeof(float4), LSE, Dv + prows, p.N,
             npad);
@@ -1236,7 +1258,8 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
         const size_t n8 = rows * D / 8;
         {
             ProfScope prof_("bwd_dq_convert", st);
-            bwd_dq_convert_rows_kernel<D><<<(unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16), 256, 0, st>>>(
+            const unsigned grid = (unsigned)std::min<size_t>((n8 + 255) / 256, (size_t)device_sm_count() * 16);
+            bwd_dq_convert_rows_kernel<D><<<grid, 256, 0, st>>>(
                 dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8, p.N, npad);
         }
         return cudaGetLastError();
@@ -1297,7 +1320,8 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
     const size_t n8 = rows * D / 8;
     {
         ProfScope prof_("bwd_dq_convert", st);
-        bwd_dq_convert_kernel<<<(unsigned)std::min<size_t>((n8 + 255) / 256, 152 * 16), 256, 0, st>>>(
+        const unsigned grid = (unsigned)std::min<size_t>((n8 + 255) / 256, (size_t)device_sm_count() * 16);
+        bwd_dq_convert_kernel<<<grid, 256, 0, st>>>(
             dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8);
     }
     return cudaGetLastError();
