@@ -184,3 +184,35 @@ def test_side_stream_without_workspace(oracle_mod):
     assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
     assert rel_l2(got[0].float().cpu().numpy(), ref[0].float().cpu().numpy()) <= 1e-3
     del junk
+
+
+def test_masked_with_empty_key_tiles(oracle_mod):
+    """A block mask over more 128-key tiles than the GPU has SMs, with whole key-tile columns
+    removed: dK and dV of the removed columns are exactly zero (their tiles visit no query
+    block), sampled rows of two heads agree with the oracle, and a second call gives the same
+    dK and dV."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, d = 1, 2, 128
+    N = 128 * (sms // 2 + 40)  # H * N / 128 tiles > SMs
+    nb = N // 128
+    s = 1.0 / math.sqrt(d)
+    x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=77)
+    mask = inputs.random_block_mask(N, seed=12, p=0.2)
+    empty = [3, nb // 2, nb - 1]
+    mask[:, empty] = 0
+    dm = mask.to(DEV)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse = attn.attn_fwd(q, k, v, s, block_mask=dm)
+    dq, dk, dv = (t.float().cpu().numpy() for t in attn.attn_bwd(q, k, v, o, do, lse, s, block_mask=dm))
+    dq2, dk2, dv2 = (t.float().cpu().numpy() for t in attn.attn_bwd(q, k, v, o, do, lse, s, block_mask=dm))
+    assert np.array_equal(dk, dk2) and np.array_equal(dv, dv2)
+    for c in empty:
+        assert np.all(dk[0, :, 128 * c:128 * (c + 1)] == 0) and np.all(dv[0, :, 128 * c:128 * (c + 1)] == 0)
+    m = mask.numpy()
+    for h in range(H):
+        qr = _sample(16, N, h)
+        kr = np.concatenate([_sample(12, N, h + 50), [128 * empty[0] + 5]]).astype(np.int32)
+        gQ, gK, gV = oracle_mod.bwd_rows(x["q"][0, h], x["k"][0, h], x["v"][0, h], x["do"][0, h], s, qr, kr, m)
+        assert rel_l2(dq[0, h][qr], gQ) <= TOL_BF16_GRAD_RL2
+        assert rel_l2(dk[0, h][kr], gK) <= TOL_BF16_GRAD_RL2
+        assert rel_l2(dv[0, h][kr], gV) <= TOL_BF16_GRAD_RL2
