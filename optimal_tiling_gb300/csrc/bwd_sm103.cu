@@ -13,7 +13,9 @@
 //   1. bwd_pre:     D = rowsum(dO o O) and L2 = LSE log2(e) in fp32 (so that P is
 //                   one FMA and one exp2 per score), the fp32 dQ accumulator zeroed
 //                   (and the split tiles' fp32 dK, dV scratch, see 2);
-//   2. bwd_main:    one CTA per 128-row K/V tile of one head, looping over the
+//   2. bwd_main:    per 128-row K/V tile of one head (one CTA per tile under a
+//                   mask or with partial tiles; without a mask bwd_persist, one CTA
+//                   per SM taking a fixed set of tiles in turn), looping over the
 //                   64-row query blocks that the block mask keeps (with 64-row
 //                   mask blocks one half of the tile's keys can be removed for a
 //                   visited query block: those keys get P = dS = 0).  Five tcgen05

@@ -216,3 +216,25 @@ def test_masked_with_empty_key_tiles(oracle_mod):
         assert rel_l2(dq[0, h][qr], gQ) <= TOL_BF16_GRAD_RL2
         assert rel_l2(dk[0, h][kr], gK) <= TOL_BF16_GRAD_RL2
         assert rel_l2(dv[0, h][kr], gV) <= TOL_BF16_GRAD_RL2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_tiles_match_one_cta_per_tile(d):
+    """Dense problems run their 128-key tiles in a persistent grid (one CTA per SM, a fixed set
+    of tiles each); an all-ones block mask takes the one-CTA-per-tile kernel, which computes
+    every tile the same way.  Tile counts equal to the SM count, and above it with an uneven
+    share per CTA and no split of the last wave (remainder above half the SMs): dK and dV
+    bit-identical, dQ equal up to the order of its fp32 reductions."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = 1.0 / math.sqrt(d)
+    for tiles, N in ((sms, 128), (sms + sms // 2 + 1, 128), (2 * sms + sms // 2 + 3, 256)):
+        H = -(-tiles // (N // 128))
+        x = inputs.make_inputs(1, H, N, d, torch.bfloat16, seed=tiles + d)
+        q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+        o, lse = attn.attn_fwd(q, k, v, s)
+        dq1, dk1, dv1 = attn.attn_bwd(q, k, v, o, do, lse, s)
+        ones = torch.ones((N // 128, N // 128), dtype=torch.uint8, device=DEV)
+        dq2, dk2, dv2 = attn.attn_bwd_masked(q, k, v, o, do, lse, s, ones)
+        assert attn.attn_device_status() == attn.ATTN_OK
+        assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2), tiles
+        assert rel_l2(dq1.float().cpu().numpy(), dq2.float().cpu().numpy()) <= 1e-3
