@@ -106,8 +106,14 @@ struct BwdCfg {
     static constexpr int kDqM = 128;                     // M of the dQ^T product
     static constexpr int kBarOff = kLdOff + kStages * 2 * BQ * 4;
     // kv, qfull[S], qempty[S], sfull[2], pfull[2], dsfree[2], dqfull, dqfree, dpfree, kvdone, drain[3],
-    // stagefree (the persistent kernel)
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3 + 1;
+    // stagefree (the persistent kernel), kread[2]
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * 3 + 3 + 1 + 3 + 1 + 2;
+    // The persistent kernel at d = 128: dK's A operand, dS^T, comes from tensor memory (bf16 pairs
+    // in the 16 columns of each query half of an S buffer that P leaves free) instead of the dS tile
+    // in shared memory: the products' operand reads from shared memory pace its loop, and this
+    // removes 16 KB of them per block (dense_16k 4.09 -> 4.02 ms).  At d = 64, and in bwd_main
+    // (masked and partial tiles: 1.6-2.0% slower there), dK reads the shared-memory tile.
+    static constexpr bool kDsInTmem = D == 128;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     // visited query blocks as a bit set: up to 32 * kMaxMaskWords 64-row blocks (N <= 131072)
     static constexpr int kMaxMaskWords = 64;
@@ -136,6 +142,8 @@ struct BwdBars {
     __device__ uint32_t kvdone() const { return base + 8u * (10 + 2 * kStages); }
     __device__ uint32_t drain(int role) const { return base + 8u * (11 + 2 * kStages + role); }
     __device__ uint32_t stagefree() const { return base + 8u * (14 + 2 * kStages); }
+    // dK has read dS^T of S buffer b (tensor memory), so S^T two blocks on may overwrite it
+    __device__ uint32_t kread(int b) const { return base + 8u * (15 + 2 * kStages + b); }
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -812,6 +820,7 @@ bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             mbar_init(bars.dsfree(b), 2);   // dK (warp 14) and dQ^T (warp 15) read dS
         }
         mbar_init(bars.dqfull(), 1);
+        for (int b = 0; b < 2; ++b) mbar_init(bars.kread(b), 1);  // dK (warp 14) read dS^T of S buffer b
         mbar_init(bars.dqfree(), 4);        // the drain warps have read dQ^T (one lane each)
         mbar_init(bars.dpfree(), 8);        // the P/dS warps have read dP^T (one lane each)
         mbar_init(bars.kvdone(), 3);        // a tile's products complete: one commit per issuer
@@ -899,6 +908,10 @@ bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 if (role == 1 && g >= 1 &&
                     !role_wait<D>(bars.dpfree(), (uint32_t)(g - 1) & 1u, abort_flag, p.dev_status))
                     return false;
+                // d = 128: S buffer g & 1 holds dS^T of block g-2 until dK (warp 14) has read it
+                if (C::kDsInTmem && role == 0 && g >= 2 &&
+                    !role_wait<D>(bars.kread(b), (uint32_t)((g - 2) >> 1) & 1u, abort_flag, p.dev_status))
+                    return false;
                 tc_fence_after();
                 const uint32_t xb = (role == 0 ? sQ : sdO) + s * C::kQTile;
                 const uint32_t kb = role == 0 ? sK : sV;
@@ -934,12 +947,23 @@ bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                        smem_desc_sw128(gb + ks * 2048, C::kQSlab, 1024), idKV,
                                        (it > 0 || ks > 0) ? 1u : 0u);
                         } else {
-                            // dK += dS^T Q_i : A = dS^T (K-major, 64 q per row), B = Q_i
+                            // dK += dS^T Q_i : B = Q_i; A = dS^T from tensor memory beside P (d = 128)
+                            // or the dS tile (K-major, 64 q per row)
+                            if constexpr (C::kDsInTmem) {
 #pragma unroll
-                            for (int ks = 0; ks < BQ / 16; ++ks)
-                                mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
-                                       smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV,
-                                       (it > 0 || ks > 0) ? 1u : 0u);
+                                for (int ks = 0; ks < BQ / 16; ++ks)
+                                    mma_ts(tmem + C::kColDK,
+                                           tmem + C::kColS + b * BQ + (ks >> 1) * 32 + (ks & 1) * 8 + 16,
+                                           smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV,
+                                           (it > 0 || ks > 0) ? 1u : 0u);
+                                mma_commit(bars.kread(b));
+                            } else {
+#pragma unroll
+                                for (int ks = 0; ks < BQ / 16; ++ks)
+                                    mma_ss(tmem + C::kColDK, smem_desc_sw128(dsb + ks * 32, 16, 1024),
+                                           smem_desc_sw128(qb + ks * 2048, C::kQSlab, 1024), idKV,
+                                           (it > 0 || ks > 0) ? 1u : 0u);
+                            }
                             mma_commit(bars.dsfree(b));
                         }
                         mma_commit(bars.qempty(s));
@@ -1028,6 +1052,7 @@ bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     dk[t] = pack_bf16(d0, d1);
                 }
                 tmem_st16(lane_base + C::kColS + b * BQ + h * 32, pk);
+                if constexpr (C::kDsInTmem) tmem_st16(lane_base + C::kColS + b * BQ + h * 32 + 16, dk);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int chunk = h * 4 + c;

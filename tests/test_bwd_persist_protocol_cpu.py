@@ -15,7 +15,7 @@ wait that passes early (or a buffer rewritten while a read is pending) shows up 
 version; a parity wait two or more completions behind the phase it wants is reported as stuck.
 Planted mistakes (K/V reloaded before the products are complete, dV staged before the drain's
 reductions have read the tile, the next tile's accumulation not ordered after the epilogue's
-reads) are caught."""
+reads, S of a block issued before dK read the dS^T that the same S columns hold) are caught."""
 import random
 
 import pytest
@@ -32,7 +32,7 @@ class Model:
     def __init__(self, n, ntile, rnd, plant=None):
         self.n, self.ntile, self.rnd, self.plant = n, ntile, rnd, plant
         self.arrivals = {}
-        self.count = {"qempty": 2, "sfull": 2, "pfull": 1, "dsfree": 2, "kvdone": 3}
+        self.count = {"qempty": 2, "sfull": 2, "pfull": 1, "dsfree": 2, "kvdone": 3, "kread": 1}
         self.ver = {}        # buffer -> version last written
         self.pending = []    # asynchronous reads in flight: (owner, buffer, expected version)
         self.tma = []        # loads in flight: (buffer, version, barrier)
@@ -88,9 +88,14 @@ def _programs(m):
             yield ("wait", ("qfull", g % STAGES), g // STAGES)
             if role == 1 and g >= 1:
                 yield ("wait", "dpfree", g - 1)
+            # the S buffer also holds dS^T of block g - 2 (d = 128) until dK has read it
+            if role == 0 and g >= 2 and m.plant != "kread_skipped":
+                yield ("wait", ("kread", g & 1), (g - 2) >> 1)
             buf = ("S", g & 1) if role == 0 else ("dP",)
-            yield ("do", lambda: pipe.append([("r", "kv", T), ("r", qs(g), g), ("w", buf, ("S" if role == 0 else "dP", g)),
-                                              ("a", ("sfull", g & 1))]))
+            ops = [("r", "kv", T), ("r", qs(g), g), ("w", buf, ("S" if role == 0 else "dP", g))]
+            if role == 0:
+                ops.append(("w", ("SdS", g & 1), ("S", g)))
+            yield ("do", lambda: pipe.append(ops + [("a", ("sfull", g & 1))]))
 
         for T in range(ntile):
             yield ("wait", "kv", T)
@@ -103,9 +108,11 @@ def _programs(m):
                         yield from first(g + 1, T)
                     yield ("wait", ("pfull", g & 1), g >> 1)
                     acc = "dV" if role == 0 else "dK"
-                    src = [("r", ("S", g & 1), ("P", g))] if role == 0 else [("r", ("dS", g & 1), ("dS", g))]
+                    # dK reads dS^T from the S buffer's free columns (d = 128)
+                    src = [("r", ("S", g & 1), ("P", g))] if role == 0 else [("r", ("SdS", g & 1), ("dS", g))]
                     ops = src + [("r", qs(g), g), ("acc", acc, T, it)]
                     if role == 1:
+                        ops.append(("a", ("kread", g & 1)))
                         ops.append(("a", ("dsfree", g & 1)))
                     ops.append(("a", ("qempty", g % STAGES)))
                     yield ("do", lambda ops=ops: pipe.append(ops))
@@ -137,6 +144,7 @@ def _programs(m):
                 def publish(g=g, T=T, it=it):
                     m.read(qs(g), g, "P/dS row terms")
                     m.write(("S", g & 1), ("P", g))
+                    m.write(("SdS", g & 1), ("dS", g))
                     m.write(("dS", g & 1), ("dS", g))
                     m.arrive(("pfull", g & 1))
                     if m.plant == "acc_unordered" and it == 0 and T > 0:
@@ -276,7 +284,7 @@ def test_persistent_backward_protocol(n, ntile):
         simulate(n, ntile, seed)
 
 
-@pytest.mark.parametrize("plant", ["kv_early", "stage_early", "acc_unordered"])
+@pytest.mark.parametrize("plant", ["kv_early", "stage_early", "acc_unordered", "kread_skipped"])
 def test_planted_protocol_mistakes_are_caught(plant):
     caught = 0
     for seed in range(200):
