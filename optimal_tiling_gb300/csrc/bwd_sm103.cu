@@ -1143,24 +1143,37 @@ bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     if (lane == 0) mbar_arrive(bars.dqfree());
                 }
                 const size_t q0 = (size_t)head * p.N + (size_t)it * BQ;  // the block's accumulator rows
-                auto stage = [&](const uint32_t(&r)[32], int hq) {
-                    if (t == 0) bulk_wait_read_but_one();
-                    named_bar_sync(1, 128);
+                if constexpr (D == 64) {
+                    // d = 64: straight from registers, each warp adding 32 consecutive floats of one
+                    // accumulator row per instruction (measured faster here than the staging tile;
+                    // at d = 128 it was 7% slower)
                     if (ok && t < D) {
-                        float *dst = dq_gen + hq * 32 * D;
+                        float *dst = dQacc + q0 * D + t;
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) dst[q * D + t] = __uint_as_float(r[q]);
-                        fence_proxy_async_smem();
+                        for (int q = 0; q < 32; ++q) atomicAdd(dst + (size_t)q * D, __uint_as_float(r0[q]));
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) atomicAdd(dst + (size_t)(32 + q) * D, __uint_as_float(r1[q]));
                     }
-                    named_bar_sync(1, 128);
-                    if (t == 0 && ok) {
-                        bulk_reduce_add_f32(dQacc + (q0 + 32 * hq) * D, sDq + hq * (C::kDqTile / 2),
-                                            C::kDqTile / 2);
-                        bulk_commit();
-                    }
-                };
-                stage(r0, 0);
-                stage(r1, 1);
+                } else {
+                    auto stage = [&](const uint32_t(&r)[32], int hq) {
+                        if (t == 0) bulk_wait_read_but_one();
+                        named_bar_sync(1, 128);
+                        if (ok && t < D) {
+                            float *dst = dq_gen + hq * 32 * D;
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) dst[q * D + t] = __uint_as_float(r[q]);
+                            fence_proxy_async_smem();
+                        }
+                        named_bar_sync(1, 128);
+                        if (t == 0 && ok) {
+                            bulk_reduce_add_f32(dQacc + (q0 + 32 * hq) * D, sDq + hq * (C::kDqTile / 2),
+                                                C::kDqTile / 2);
+                            bulk_commit();
+                        }
+                    };
+                    stage(r0, 0);
+                    stage(r1, 1);
+                }
                 alive = alive && ok;
             }
             // the tile's reductions have read the staging tile: the epilogue may stage dV there
