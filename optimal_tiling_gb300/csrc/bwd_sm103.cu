@@ -777,6 +777,9 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 //   - dK is staged in the two dS tiles, dV in the dQ staging tile once the drain's reductions of the
 //     tile have read it (stagefree); all eight P/dS warps meet after the stores have read both, so
 //     that no dS or dQ of the next tile is written there before.
+// Within a block, at d = 128 dK's A operand (dS^T) is read from tensor memory beside P (kDsInTmem),
+// and S^T two blocks on waits for dK's release of those columns (kread); at d = 64 the dQ drain
+// adds straight from registers instead of through the staging tile.
 // One CTA per SM also removes the per-CTA start (barrier set-up, tensor-memory allocation, the
 // first loads) from all tiles but the first.
 template <int D>
