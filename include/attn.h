@@ -42,7 +42,7 @@
  *               that attn_device_status() reports as ATTN_ERR_TIMEOUT.
  *   Shapes      fp32: any N >= 1, 1 <= d <= 256 (SIMT kernels).
  *               bf16: fused forward any N >= 1, d in {64, 128, 256}; fused
- *               backward any N >= 1, d in {64, 128}; materialising forward
+ *               backward any N >= 1, d in {64, 128, 256}; materialising forward
  *               (N a multiple of 128) d in {64, 128, 256}; materialising
  *               backward (N a multiple of 128) d in {64, 128}.  When 128 does
  *               not divide N, the last 128-row tile of each head is partial:

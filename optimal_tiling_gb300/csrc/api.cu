@@ -125,7 +125,7 @@ attn_status check_common(int B, int H, int N, int d, attn_dtype dt) {
 }
 
 bool bf16_fwd_shape_ok(int N, int d) { return N >= 1 && (d == 64 || d == 128 || d == 256); }
-bool bf16_bwd_shape_ok(int N, int d) { return N >= 1 && (d == 64 || d == 128); }
+bool bf16_bwd_shape_ok(int N, int d) { return N >= 1 && (d == 64 || d == 128 || d == 256); }
 bool bf16_matfwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128 || d == 256); }
 bool bf16_matbwd_shape_ok(int N, int d) { return N % 128 == 0 && (d == 64 || d == 128); }
 
@@ -320,7 +320,7 @@ attn_status attn_fwd_masked(const void *Q, const void *K, const void *V, void *O
 size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype dtype) {
     if (check_common(B, H, N, d, dtype) != ATTN_OK) return 0;
     size_t bytes = attn::bwd_base_bytes(B, H, N, d, dtype == ATTN_DTYPE_BF16);
-    if (dtype == ATTN_DTYPE_BF16)  // fp32 partial dK, dV of the last wave's split tiles
+    if (dtype == ATTN_DTYPE_BF16 && d != 256)  // fp32 partial dK, dV of the last wave's split tiles
         bytes += align_up(attn::bwd_split_bytes(attn::bwd_split_tiles(B, H, N), d), 256);
     return bytes;
 }
@@ -379,7 +379,7 @@ attn_status bwd_impl(const void *Q, const void *K, const void *V, const void *O,
     const size_t prows = (size_t)B * H * attn::bwd_rows_per_head(N);
     float *dQacc = reinterpret_cast<float *>(static_cast<char *>(workspace) + align_up(2 * prows * sizeof(float), 256));
     // split the last wave (dense problems) when the workspace also holds the partial dK, dV
-    int split = mask == nullptr ? attn::bwd_split_tiles(B, H, N) : 0;
+    int split = mask == nullptr && d != 256 ? attn::bwd_split_tiles(B, H, N) : 0;  // no split pass at d = 256
     if (split > 0 && workspace_bytes < need + attn::bwd_split_bytes(split, d)) split = 0;
     float *kvacc = split > 0 ? reinterpret_cast<float *>(static_cast<char *>(workspace) + need) : nullptr;
     attn::BwdMaps maps;

@@ -1370,6 +1370,33 @@ cudaError_t launch_d(const Problem &p, const BwdMaps &m, const void *O, const vo
     return cudaGetLastError();
 }
 
+// d = 256: bwd_pre, the two passes of bwd256_sm103.cu, the dQ conversion (no last-wave split).
+cudaError_t launch_d256(const Problem &p, const BwdMaps &m, const void *O, const void *dO, const float *LSE,
+                        void *dQ, void *dK, void *dV, float *Dv, float *dQacc, cudaStream_t st) {
+    constexpr int D = 256;
+    const int npad = bwd_rows_per_head(p.N);
+    const size_t rows = (size_t)p.B * p.H * p.N, prows = (size_t)p.B * p.H * npad;
+    {
+        ProfScope prof_("bwd_pre", st);
+        auto pre = npad != p.N ? bwd_pre_kernel<D, true> : bwd_pre_kernel<D, false>;
+        pre<<<(unsigned)((prows + kPreRowsPerBlock<D> - 1) / kPreRowsPerBlock<D>), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(O), static_cast<const __nv_bfloat16 *>(dO), Dv, dQacc, prows,
+            nullptr, 0, LSE, Dv + prows, p.N, npad);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = launch_bwd256_main(p, m, Dv + prows, Dv, dQacc, dK, dV, st);
+    if (e != cudaSuccess) return e;
+    const size_t n8 = rows * D / 8;
+    const unsigned grid = (unsigned)std::min<size_t>((n8 + 255) / 256, (size_t)device_sm_count() * 16);
+    ProfScope prof_("bwd_dq_convert", st);
+    if (npad != p.N)
+        bwd_dq_convert_rows_kernel<D><<<grid, 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8,
+                                                            p.N, npad);
+    else
+        bwd_dq_convert_kernel<<<grid, 256, 0, st>>>(dQacc, static_cast<__nv_bfloat16 *>(dQ), p.scale, n8);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 int bwd_rows_per_head(int N) { return (N + BQ - 1) / BQ * BQ; }
@@ -1391,6 +1418,7 @@ cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O
     switch (p.d) {
         case 64: return launch_d<64>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, kvacc, split_tiles, st);
         case 128: return launch_d<128>(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, kvacc, split_tiles, st);
+        case 256: return launch_d256(p, maps, O, dO, LSE, dQ, dK, dV, Dv, dQacc, st);
         default: return cudaErrorNotSupported;
     }
 }

@@ -87,6 +87,12 @@ cudaError_t launch_bwd_bf16(const Problem &p, const BwdMaps &maps, const void *O
                             const void *dO, const float *LSE, void *dQ, void *dK, void *dV,
                             float *D, float *dQacc, float *kvacc, int split_tiles, cudaStream_t st);
 
+// d = 256: the two passes of the recompute backward (bwd256_sm103.cu) on the row terms and
+// accumulator that bwd_pre prepared (L2 = -LSE log2(e), Dv = -D, dQacc zeroed; npad rows per
+// head): dK with dQ added into dQacc, then dV.
+cudaError_t launch_bwd256_main(const Problem &p, const BwdMaps &maps, const float *L2, const float *Dv,
+                               float *dQacc, void *dK, void *dV, cudaStream_t st);
+
 // SM count of the current device (152 when it cannot be asked).
 int device_sm_count();
 

@@ -59,7 +59,7 @@ WORKLOADS = {
     "teaching": Workload("teaching", 4, 16, 4096, 64, "bf16", _s(64), passes=("fwd", "bwd")),
     "dsweep_d64": Workload("dsweep_d64", 2, 16, 8192, 64, "bf16", _s(64), passes=("fwd", "mat")),
     "dsweep_d128": Workload("dsweep_d128", 2, 16, 8192, 128, "bf16", _s(128), passes=("fwd", "mat")),
-    "dsweep_d256": Workload("dsweep_d256", 2, 16, 8192, 256, "bf16", _s(256), passes=("fwd", "mat")),
+    "dsweep_d256": Workload("dsweep_d256", 2, 16, 8192, 256, "bf16", _s(256), passes=("fwd", "mat", "bwd")),
     "bwd_d128": Workload("bwd_d128", 4, 16, 4096, 128, "bf16", _s(128), passes=("fwd", "bwd", "matbwd")),
     "sparse_16k": Workload("sparse_16k", 1, 16, 16384, 128, "bf16", _s(128), mask="band_random",
                            passes=("fwd", "bwd")),

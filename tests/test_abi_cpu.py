@@ -71,7 +71,8 @@ def test_backward_argument_checks(lib):
     def bwd(d=128, N=256, ws=FAKE, wsz=1 << 30, dt=attn.ATTN_DTYPE_BF16):
         return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, N, d, 0.1, dt,
                             None, ws, wsz, None)
-    assert bwd(d=256) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(d=96) == attn.ATTN_ERR_UNSUPPORTED
+    assert bwd(d=512) == attn.ATTN_ERR_UNSUPPORTED
     # bf16: the row terms and dQ accumulator have N rounded up to 64 rows per head, which
     # must stay within 2^31 rows too (3 x 715827882 rows fit, 3 x 715827904 do not)
     assert lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 715827882, 64, 0.1,
@@ -98,6 +99,8 @@ def test_bwd_workspace_holds_the_last_wave_split(lib):
         base = up(2 * N * 4) + up(N * 128 * 4)   # D and LSE log2(e), then the fp32 dQ accumulator
         assert lib.attn_bwd_workspace_size(1, 1, N, 128, attn.ATTN_DTYPE_BF16) == base + split * 2 * 128 * 128 * 4
         assert lib.attn_bwd_workspace_size(1, 1, N, 128, attn.ATTN_DTYPE_F32) == up(N * 4)
+        # d = 256 runs two passes per key tile and never splits the last wave
+        assert lib.attn_bwd_workspace_size(1, 1, N, 256, attn.ATTN_DTYPE_BF16) == up(2 * N * 4) + up(N * 256 * 4)
 
 
 def test_materialized_argument_checks(lib):

@@ -43,7 +43,7 @@ def _check_full(x, scale, oracle_mod, mask=None):
     return dq, dk, dv
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N,BH", [(128, (1, 1)), (256, (1, 3)), (384, (3, 1)), (1024, (1, 2))])
 def test_small_shapes(oracle_mod, N, BH, d):
     B, H = BH
@@ -51,7 +51,7 @@ def test_small_shapes(oracle_mod, N, BH, d):
     _check_full(x, 1.0 / math.sqrt(d), oracle_mod)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_block_masks_and_empty_rows(oracle_mod, d):
     N = 768
     x = inputs.make_inputs(1, 2, N, d, torch.bfloat16, seed=21 + d)
@@ -68,7 +68,7 @@ def test_block_masks_and_empty_rows(oracle_mod, d):
     assert np.all(dk[:, :, 0:128] == 0) and np.all(dv[:, :, 256:512] == 0)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_gradient_invariants(d):
     """Rows of P sum to one: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i."""
     N = 1024
@@ -80,10 +80,11 @@ def test_gradient_invariants(d):
     assert np.linalg.norm(dv[0, 0].sum(axis=0) - dO.sum(axis=0)) <= 2e-2 * np.linalg.norm(dO.sum(axis=0))
 
 
-def test_deterministic_inputs_repeat():
+@pytest.mark.parametrize("d", [128, 256])
+def test_deterministic_inputs_repeat(d):
     """Two calls on the same inputs agree to the rounding of fp32 additions
     (the dQ accumulation order between key tiles is not fixed)."""
-    x = inputs.make_inputs(1, 2, 512, 128, torch.bfloat16, seed=23)
+    x = inputs.make_inputs(1, 2, 512, d, torch.bfloat16, seed=23)
     a = _fwd_bwd(x, 0.09, guarded=False)
     b = _fwd_bwd(x, 0.09, guarded=False)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])   # dK, dV: fixed order
@@ -95,14 +96,15 @@ def _sample(n, N, seed):
     return np.unique(np.concatenate([[0, N - 1], r.integers(0, N, n - 2)])).astype(np.int32)
 
 
-@pytest.mark.parametrize("name", ["teaching", "bwd_d128", "sparse_16k", "dense_16k"])
+@pytest.mark.parametrize("name", ["teaching", "bwd_d128", "sparse_16k", "dense_16k", "dsweep_d256"])
 def test_full_size_workloads_sampled(oracle_mod, name):
     """Full-size workloads in the bench's launch configuration; the oracle computes
     sampled gradient rows of the first and the last head: dQ rows (one query row each)
     and dK, dV rows (which need every query row's LSE and D of that head).  On the
     N = 16384 shapes the last head holds tiles of the split last wave (2048 key tiles
     on 152 SMs leave 72 in the last wave), each accumulating 128 query blocks per
-    half; the key rows sampled there include the head's last one."""
+    half; the key rows sampled there include the head's last one.  The d-sweep's
+    d = 256 shape (2 x 16 x 8192) takes the two-pass backward."""
     w = inputs.WORKLOADS[name]
     x, mask = inputs.workload_inputs(w)
     dq, dk, dv = _fwd_bwd(x, w.scale, mask, guarded=False)

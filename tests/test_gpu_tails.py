@@ -81,7 +81,7 @@ def test_forward_tails_masked(oracle_mod, N, d, block, shared):
 
 
 @pytest.mark.parametrize("N", [1, 37, 64, 100, 129, 192, 200, 383])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_backward_tails(oracle_mod, N, d):
     """The backward's row terms and dQ accumulator have N rounded up to 64 rows per head;
     the rows past N are padding with zero weight."""
@@ -95,7 +95,8 @@ def test_backward_tails(oracle_mod, N, d):
         assert rel_l2(got, ref) <= TOL_BF16_GRAD_RL2, name
 
 
-@pytest.mark.parametrize("N,d,block", [(200, 128, 128), (300, 64, 64), (150, 128, 64), (383, 64, 128)])
+@pytest.mark.parametrize("N,d,block", [(200, 128, 128), (300, 64, 64), (150, 128, 64), (383, 64, 128),
+                                         (200, 256, 64), (330, 256, 128)])
 def test_backward_tails_masked(oracle_mod, N, d, block):
     B, H = 1, 2
     x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=7 * N + block)
