@@ -240,3 +240,24 @@ def test_persistent_tiles_match_one_cta_per_tile(d):
         assert attn.attn_device_status() == attn.ATTN_OK
         assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2), tiles
         assert rel_l2(dq1.float().cpu().numpy(), dq2.float().cpu().numpy()) <= 1e-3
+
+
+def test_d256_mask_columns_longer_than_the_bit_set(oracle_mod):
+    """At d = 256 a key tile's visited query blocks are held as a bit set of up to 1024 64-row
+    blocks (N <= 65536); longer mask columns are read entry by entry.  N = 65664 (1026 query
+    blocks) with a tridiagonal 128-block mask: sampled dQ, dK and dV rows of the last blocks,
+    which only the entry-by-entry walk reaches, against the oracle."""
+    N, d = 65664, 256
+    s = 1.0 / math.sqrt(d)
+    nb = N // 128
+    x = inputs.make_inputs(1, 1, N, d, torch.bfloat16, seed=41)
+    i = torch.arange(nb)
+    mask = ((i[:, None] - i[None, :]).abs() <= 1).to(torch.uint8)
+    dq, dk, dv = _fwd_bwd(x, s, mask)
+    qr = np.array([0, 5, N // 2, N - 200, N - 65, N - 1], dtype=np.int32)
+    kr = np.array([3, N // 2 + 7, N - 300, N - 129, N - 2], dtype=np.int32)
+    gQ, gK, gV = oracle_mod.bwd_rows(x["q"][0, 0], x["k"][0, 0], x["v"][0, 0], x["do"][0, 0], s, qr, kr,
+                                     mask.numpy())
+    assert rel_l2(dq[0, 0][qr], gQ) <= TOL_BF16_GRAD_RL2
+    assert rel_l2(dk[0, 0][kr], gK) <= TOL_BF16_GRAD_RL2
+    assert rel_l2(dv[0, 0][kr], gV) <= TOL_BF16_GRAD_RL2
