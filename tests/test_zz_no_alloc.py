@@ -68,6 +68,11 @@ def test_static_workspace_matches_attn_bwd_twice(lib):
     _compare_twice(lib, 1, 4, 1024, 128, (41, 42))
 
 
+def test_static_workspace_at_d256(lib):
+    """d = 256 runs the two-pass backward; its row terms and accumulator fit the array too."""
+    _compare_twice(lib, 1, 2, 1024, 256, (43, 44))
+
+
 def test_static_workspace_with_a_split_last_wave(lib):
     """A dense shape whose last wave of 128-key tiles is split into query halves: the
     fp32 partial dK and dV of the split tiles then also live in the fixed array (after
