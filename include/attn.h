@@ -140,7 +140,8 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d, attn_dtype d
  * workspace: device scratch of at least attn_bwd_workspace_size() bytes
  *      (16-byte aligned, contents on entry ignored); it holds D and, for bf16,
  *      LSE log2(e) and the fp32 dQ accumulator (these three with N rounded up
- *      to a multiple of 64 rows per head).  For bf16 without a mask, when 128
+ *      to a multiple of 64 rows per head).  For bf16 without a mask, d < 256
+ *      (d = 256 runs two passes per key tile and never splits), when 128
  *      divides N, the current device's SM count does not divide the 128-key
  *      tiles and the last wave of tiles would be at most half full, the size
  *      also covers fp32 dK and dV of
