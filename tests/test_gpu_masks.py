@@ -96,7 +96,7 @@ def test_bf16_forward_per_head_masks(oracle_mod, N, d, block):
 
 
 @pytest.mark.parametrize("N,block,d", [(512, 64, 128), (768, 128, 128), (384, 64, 128), (512, 64, 64),
-                                       (768, 128, 64)])
+                                       (768, 128, 64), (384, 64, 256), (512, 128, 256)])
 def test_bf16_backward_per_head_masks(oracle_mod, N, block, d):
     B, H = 1, 2
     x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=3 * N + block + d)
@@ -126,13 +126,14 @@ def _same_grads(g1, g2):
     assert rel_l2(dq1, dq2) <= 1e-3
 
 
-def test_fine_mask_equal_to_coarse_gives_identical_results():
+@pytest.mark.parametrize("d", [128, 256])
+def test_fine_mask_equal_to_coarse_gives_identical_results(d):
     """A 64-block mask that repeats each entry of a 128-block mask 2 x 2 removes the
     same scores: both give bit-identical O, LSE, dK, dV (and dQ up to the order of its
     fp32 reductions).  The 128-block mask is given per head, so that both take the
     kernel with one query tile per CTA (one mask for both heads would pair the heads'
     tiles in one CTA, which rounds differently)."""
-    B, H, N, d = 1, 2, 768, 128
+    B, H, N = 1, 2, 768
     x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=31)
     shared = inputs.random_block_mask(N, seed=9, p=0.4)
     coarse = shared.expand(B, H, -1, -1).contiguous()
@@ -175,9 +176,10 @@ def test_no_mask_through_masked_entry_points():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_all_removed_mask():
+@pytest.mark.parametrize("d", [128, 256])
+def test_all_removed_mask(d):
     """Every block removed: O = 0, LSE = -inf, every gradient zero."""
-    B, H, N, d = 1, 1, 256, 128
+    B, H, N = 1, 1, 256
     x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=61)
     mask = torch.zeros((4, 4), dtype=torch.uint8)
     o, lse = _fwd(x, 0.1, mask, 64)
