@@ -273,7 +273,7 @@ def run_cuda(args):
     gpu_launches = sum(n for (n, t) in prof.values())
 
     # ---------------------------------------------------------------- end to end (host buffers)
-    e2e = _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only=args.fwd_only)
+    e2e = _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, local, fwd_only=args.fwd_only)
 
     result = {
         "metric": METRIC,
@@ -386,7 +386,7 @@ def _io_model(iomodel, N, d, heads, kept, peaks, brief=False):
     }
 
 
-def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only=False):
+def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, gpu_index, fwd_only=False):
     """Same metric through the public API with host buffers.  Every step copies its
     inputs (Q, K, V, dO) host -> device from pinned memory, runs fwd + bwd, and
     copies every result (O, LSE, dQ, dK, dV) device -> host, all inside the timed
@@ -417,14 +417,22 @@ def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only
                 dev_in[b][n].copy_(host_in[b][n], non_blocking=True)
         ev_in[b].record(s_h2d)
 
-    def compute(b):
+    # compute-stream events of the timed runs: the first step's start (after its waits) and the
+    # last step's end, so that the stream's own time per step can be set beside the host's
+    marks = {}
+
+    def compute(b, first=False, last=False):
         stream.wait_event(ev_in[b])
         stream.wait_event(ev_out[b])     # the previous results of this set were copied out
+        if first:
+            marks["c0"].record(stream)
         di, do_ = dev_in[b], dev_out[b]
         attn.attn_fwd(di["q"], di["k"], di["v"], w.scale, block_mask=dmask, out=do_[0], lse=do_[-1], stream=stream)
         if not fwd_only:
             attn.attn_bwd(di["q"], di["k"], di["v"], do_[0], di["do"], do_[-1], w.scale, block_mask=dmask,
                           dq=do_[1], dk=do_[2], dv=do_[3], workspace=wsp, stream=stream)
+        if last:
+            marks["c1"].record(stream)
         ev_done[b].record(stream)
 
     def d2h(b):
@@ -434,18 +442,21 @@ def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only
                 hdst.copy_(dsrc, non_blocking=True)
         ev_out[b].record(s_d2h)
 
-    def run(nsteps):
+    def run(nsteps, timed=False):
         for b in range(2):
             ev_done[b].record(stream)
             ev_out[b].record(s_d2h)
+        if timed:
+            marks["c0"], marks["c1"] = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         h2d(0)
         for i in range(nsteps):
             b = i & 1
             if i + 1 < nsteps:
                 h2d(1 - b)
-            compute(b)
+            compute(b, first=timed and i == 0, last=timed and i == nsteps - 1)
             d2h(b)
         torch.cuda.synchronize(dev)
+        return marks["c0"].elapsed_time(marks["c1"]) / nsteps if timed else None
 
     run(max(2, args.warmup))
     if dist is not None:
@@ -454,11 +465,14 @@ def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only
     # result copy are not overlapped with compute: a short run would charge them to every step)
     steps = max(2, min(args.steps, 60))
     # host-timed, so host and copy-engine jitter show: five timed runs, the median reported
-    runs = []
-    for _ in range(5):
-        t0 = time.perf_counter()
-        run(steps)
-        runs.append((time.perf_counter() - t0) / steps)
+    runs, stream_ms = [], []
+    with ClockSampler(gpu_index) as clk:
+        clk.mark_start()
+        for _ in range(5):
+            t0 = time.perf_counter()
+            stream_ms.append(run(steps, timed=True))
+            runs.append((time.perf_counter() - t0) / steps)
+        clk.mark_end()
     el = _max_over_ranks(dist, sorted(runs)[len(runs) // 2], dev)
     total = _sum_over_ranks(dist, step_flops, dev)
     h2d_bytes = sum(t.numel() * t.element_size() for t in host_in[0].values())
@@ -466,7 +480,11 @@ def _e2e(args, attn, torch, dev, stream, x, dmask, w, step_flops, dist, fwd_only
     return {"value": round(total / el / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(el * 1e3, 3),
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": steps,
             "runs_ms_per_step": [round(r * 1e3, 3) for r in runs], "reported": "median of the five runs",
-            "pipelining": "inputs of step i+1 copied and results of step i-1 read back while step i computes"}
+            "pipelining": "inputs of step i+1 copied and results of step i-1 read back while step i computes",
+            # the compute stream's own time per step in the same runs (CUDA events from the first
+            # step's start to the last step's end: the first input copy and the last result copy,
+            # which nothing overlaps, are outside it) and the SM clocks sampled during the runs
+            "compute_stream_ms_per_step": [round(m, 3) for m in stream_ms], "clocks": clk.summary()}
 
 
 def _comparison(attn, torch, dev, stream, inputs, iomodel, peaks):
