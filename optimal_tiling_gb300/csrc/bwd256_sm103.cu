@@ -24,8 +24,9 @@
 //     while block i still holds two, and the second can only load once dK of block i has read
 //     the slot it takes.  Tensor memory: dK (256 columns), S, dP, dQ^T (2 x 64).  Eight warps
 //     turn S and dP into dS (thread = key, each warp 32 queries of a block), four drain dQ^T
-//     into the fp32 accumulator with 16-byte atomic adds from registers (no shared memory is
-//     left for a staging tile), one loads, three issue (S^T and dK; dP^T; dQ^T).
+//     into the fp32 accumulator with atomic adds from registers (a warp adds one 128-byte line
+//     of an accumulator row per instruction; no shared memory is left for a staging tile), one
+//     loads, three issue (S^T and dK; dP^T; dQ^T).
 //   pass A (dV): K resident, Q_i and dO_i in two-stage rings of their own (Q released once S^T
 //     has read it, dO with the block's row terms once dV has: a stage shared by both held Q until
 //     dV and put the next load's latency between dV and the next S^T, 3.0 ms for this pass on
@@ -34,7 +35,7 @@
 //     columns), S (2 x 64).
 //
 // Both passes run as one grid each on the caller's stream, pass B first (its CTAs take about
-// twice as long) and pass A as a programmatic dependent launch: neither reads what the other
+// two and a half times as long) and pass A as a programmatic dependent launch: neither reads what the other
 // writes, so pass A's CTAs take the SMs that pass B's free.  Against the one-pass kernel at
 // smaller d the products are 12 N^2 d instead of 10 N^2 d (S^T twice).
 //
