@@ -113,6 +113,7 @@ struct CfgB {
 };
 
 struct BarsA {
+    static_assert(CfgA::kStages == 2 && CfgA::kNumBars == 15, "barrier indices below");
     uint32_t base;
     __device__ uint32_t kv() const { return base; }
     __device__ uint32_t qfull(int s) const { return base + 8u * (1 + s); }
@@ -126,6 +127,7 @@ struct BarsA {
 };
 
 struct BarsB {
+    static_assert(CfgB::kUnits == 3 && CfgB::kNumBars == 21, "barrier indices below");
     uint32_t base;
     __device__ uint32_t kv() const { return base; }
     __device__ uint32_t qfull(int u) const { return base + 8u * (1 + u); }
@@ -591,6 +593,8 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
     }
 
+    // a tile that visits no query block still received its K (and V) tile: let that copy land first
+    if (n == 0 && tid == 0) mbar_wait(bars.kv(), 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -780,6 +784,8 @@ bwd256_dv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         }
     }
 
+    // a tile that visits no query block still received its K (and V) tile: let that copy land first
+    if (n == 0 && tid == 0) mbar_wait(bars.kv(), 0, abort_flag, p.dev_status);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
