@@ -35,9 +35,10 @@
 //     columns), S (2 x 64).
 //
 // Both passes run as one grid each on the caller's stream, pass B first (its CTAs take about
-// two and a half times as long) and pass A as a programmatic dependent launch: neither reads what the other
-// writes, so pass A's CTAs take the SMs that pass B's free.  Against the one-pass kernel at
-// smaller d the products are 12 N^2 d instead of 10 N^2 d (S^T twice).
+// two and a half times as long) and pass A as a programmatic dependent launch: neither reads what
+// the other writes, so pass A's CTAs take the SMs that pass B's free; pass A's last CTA waits for
+// pass B to complete before it ends, so that later work on the stream follows both.  Against the
+// one-pass kernel at smaller d the products are 12 N^2 d instead of 10 N^2 d (S^T twice).
 //
 // Masks, 64-row mask blocks and partial tiles (N % 128 != 0) follow the one-pass kernel: query
 // blocks that no kept mask entry covers are skipped, keys of a removed 64-key half get
@@ -792,6 +793,12 @@ bwd256_dv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // This grid runs beside pass B as its dependent launch, and later work on the stream (the
+    // dQ conversion) reads the accumulator that pass B adds into.  The grid's last CTA (launched
+    // last, so it waits only for pass B's tail) ends by waiting for pass B to complete: this grid
+    // then completes after pass B.  Its other CTAs leave their SMs at once.
+    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <bool TAIL>
