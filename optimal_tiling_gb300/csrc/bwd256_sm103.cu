@@ -23,10 +23,13 @@
 //     block i and the second half after it: the third unit slot lets the first half load
 //     while block i still holds two, and the second can only load once dK of block i has read
 //     the slot it takes.  Tensor memory: dK (256 columns), S, dP, dQ^T (2 x 64).  Eight warps
-//     turn S and dP into dS (thread = key, each warp 32 queries of a block), four drain dQ^T
-//     into the fp32 accumulator with atomic adds from registers (a warp adds one 128-byte line
-//     of an accumulator row per instruction; no shared memory is left for a staging tile), one
-//     loads, three issue (S^T and dK; dP^T; dQ^T).
+//     turn S and dP into dS (thread = key, each warp 32 queries of a block), one loads, three
+//     issue (S^T and dK; dP^T; dQ^T).  dQ^T goes into the fp32 accumulator with atomic adds from
+//     registers (a warp adds one 128-byte line of an accumulator row per instruction; no shared
+//     memory is left for a staging tile): four drain warps take M half 0 (d 0-127), the eight
+//     dS warps M half 1 right after publishing the next block's dS (with the four drain warps
+//     alone the pass took 6% longer: their adds, throttled by the memory pipe, held back the
+//     buffer's release, and with it dQ^T, dS and the loop).
 //   pass A (dV): K resident, Q_i and dO_i in two-stage rings of their own (Q released once S^T
 //     has read it, dO with the block's row terms once dV has: a stage shared by both held Q until
 //     dV and put the next load's latency between dV and the next S^T, 3.0 ms for this pass on
@@ -312,7 +315,7 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_init(bars.pfull(), 8);
         mbar_init(bars.dsfree(), 2);        // dK (issuer 0) and dQ^T (issuer 2) read dS
         mbar_init(bars.dqfull(), 1);
-        mbar_init(bars.dqfree(), 4);        // one lane of each drain warp
+        mbar_init(bars.dqfree(), 12);       // one lane of each drain warp and of each dS warp
         mbar_init(bars.kvdone(), 1);
         for (int r = 0; r < 3; ++r) mbar_init(bars.drain(r), 1);
         fence_barrier_init();
@@ -474,8 +477,28 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const float sl2 = p.scale * kLog2e;
         const bool key_ok = !TAIL || kvt * BKV + key < p.N;
         uint8_t *ds_gen = sm + C::kDsOff;
-        int iq = -1;
+        int iq = -1, iq_prev = -1;
         bool ok = true;
+        // M half 1 of dQ^T of block j (d = 128 + 32 (warp % 4) + lane; queries 32 h ..): read, release,
+        // add into the accumulator (the drain warps take M half 0)
+        auto drain_half1 = [&](int j, int iqj) -> bool {
+            bool w = mbar_wait(bars.dqfull(), (uint32_t)j & 1u, abort_flag, p.dev_status);
+            w = __all_sync(0xffffffffu, w);
+            if (!w) return false;
+            tc_fence_after();
+            uint32_t r[32];
+            tmem_ld32(lane_base + C::kColQ + BQ + h * 32, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.dqfree());
+            float *col = dQacc + (size_t)(TAIL ? head * npad + iqj * BQ : head * p.N + iqj * BQ) * D +
+                         (size_t)(h * 32) * D + 128 + key;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) atomicAdd(col + (size_t)q * D, __uint_as_float(r[q]));
+            return true;
+        };
         for (int it = 0; it < n; ++it) {
             iq = qb.next(iq);
             const bool row_kept = qb.half_kept(iq, key);  // warp-uniform: 32 keys lie in one half
@@ -538,7 +561,10 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.pfull());
+            if (it >= 1 && !drain_half1(it - 1, iq_prev)) { ok = false; break; }
+            iq_prev = iq;
         }
+        if (ok && n > 0) ok = drain_half1(n - 1, iq_prev);
         // ------------------------------------------------------------ dK epilogue
         // staged over the Q units and the dS tile, once dK and the last dQ^T (which reads dS)
         // are complete
@@ -555,10 +581,11 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
     } else if (warp < kTmaWarp) {
         // ------------------------------------------------------------ dQ drain warps 8-11
-        // Thread t = d index within an M half (tensor memory lane); column q = query of the block.
-        // For each query the 32 lanes of a warp add 32 consecutive floats of the accumulator row
-        // (one 128-byte line; 16-byte adds of four consecutive d after a 4 x 4 lane transpose
-        // make the same number of line requests and measured 10% slower on this pass).
+        // M half 0 of dQ^T (d 0-127; the dS warps take half 1).  Thread t = d index (tensor memory
+        // lane); column q = query of the block.  For each query the 32 lanes of a warp add 32
+        // consecutive floats of the accumulator row (one 128-byte line; 16-byte adds of four
+        // consecutive d after a 4 x 4 lane transpose make the same number of line requests and
+        // measured 10% slower on this pass).
         const int t = tid - kDqWarp0 * 32;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         bool alive = true;
@@ -571,21 +598,17 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             if (!ok) continue;
             tc_fence_after();
             float *row0 = dQacc + (size_t)(TAIL ? head * npad + iq * BQ : head * p.N + iq * BQ) * D + t;
-#pragma unroll 1
-            for (int mh = 0; mh < 2; ++mh) {
+            {
                 uint32_t r0[32], r1[32];
-                tmem_ld32(lane_base + C::kColQ + mh * BQ, r0);
-                tmem_ld32(lane_base + C::kColQ + mh * BQ + 32, r1);
+                tmem_ld32(lane_base + C::kColQ, r0);
+                tmem_ld32(lane_base + C::kColQ + 32, r1);
                 tmem_wait_ld();
                 reg_fence(r0);
                 reg_fence(r1);
-                if (mh == 1) {
-                    // the whole dQ^T buffer is in registers: the next block's products may start
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars.dqfree());
-                }
-                float *col = row0 + mh * 128;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.dqfree());
+                float *col = row0;
 #pragma unroll
                 for (int q = 0; q < 32; ++q) atomicAdd(col + (size_t)q * D, __uint_as_float(r0[q]));
 #pragma unroll
