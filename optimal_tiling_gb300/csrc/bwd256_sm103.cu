@@ -443,7 +443,8 @@ bwd256_dkdq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             } else {
                 for (int it = 0; it < n && ok; ++it) {
                     if (!(ok = mbar_wait(bars.pfull(), (uint32_t)it & 1u, abort_flag, p.dev_status))) break;
-                    // one dQ^T buffer: the drain warps must have read dQ^T of the block before
+                    // one dQ^T buffer: the drain warps (M half 0) and the dS warps (M half 1) must
+                    // have read dQ^T of the block before
                     if (it >= 1 && !(ok = mbar_wait(bars.dqfree(), (uint32_t)(it - 1) & 1u, abort_flag, p.dev_status)))
                         break;
                     tc_fence_after();
