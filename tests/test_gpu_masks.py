@@ -116,6 +116,20 @@ def test_bf16_backward_per_head_masks(oracle_mod, N, block, d):
         assert np.all(dk[0, h][~cols] == 0) and np.all(dv[0, h][~cols] == 0)
 
 
+def test_bf16_backward_fine_masks_many_blocks_d256(oracle_mod):
+    """64-row per-head masks on the two-pass d = 256 backward with many query blocks per key tile
+    (N = 2048: 32 blocks of 64 rows, 16 key tiles a head), whole tensors against the oracle."""
+    B, H, N, d, block = 1, 2, 2048, 256, 64
+    x = inputs.make_inputs(B, H, N, d, torch.bfloat16, seed=91)
+    mask = _masks(B * H, N, block, seed=13)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _fwd(x, scale, mask, block)
+    dq, dk, dv = _bwd(x, scale, mask, block, o, lse)
+    gQ, gK, gV = oracle_mod.bwd_naive_m(x["q"], x["k"], x["v"], x["do"], scale, _oracle_mask(mask, B, H), block)
+    for name, got, ref in (("dQ", dq, gQ), ("dK", dk, gK), ("dV", dv, gV)):
+        assert rel_l2(got, ref) <= TOL_BF16_GRAD_RL2, name
+
+
 def _same_grads(g1, g2):
     """dK and dV come out of one CTA each: bit-identical.  dQ is summed over key
     tiles by fp32 reductions whose order is not fixed, so two runs may differ in
